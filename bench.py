@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 MoE router gate on GB300.
+
+One step = one router call (runtime NVFP4 quantization of the activations,
+block-scaled NVFP4 gate GEMM, fused sigmoid / biased top-k / renormalise /
+scale epilogue) over one batch of the prefill workload: T = 4096 tokens,
+D = 7168, E = 256 experts, k = 8, bf16 activations (per-token LogNormal scale),
+NVFP4 gate weight resident on the GPU.  Synthetic, seeded inputs.
+
+Printed (rank 0, one JSON line): prefill tokens/s over exactly --steps timed
+steps (inputs resident in HBM, four rotating 58.7 MB activation buffers so no
+step reads its input from L2), plus
+  e2e           the same call with the batch copied from pinned host memory and
+                the ids/weights copied back inside every timed step;
+  roofline      the dominant kernel's algorithmic bytes (or flops) per launch /
+                its mean CUDA-event duration in a second pass with per-kernel
+                events, against MEASURED_PEAKS.json;
+  kernels       every kernel of the step, the same way;
+  decode        the decode router (T = 1, 8, 64) as CUDA-graph replays;
+  cpu_baseline  the CPU oracle on a bounded sample of the same batch;
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+
+--impl reference times the CPU oracle itself on the host cores (the pages
+publish no implementation to run).  Multi-GPU (torchrun): independent replicas,
+one batch per rank, no collective on the data path; value = all ranks' tokens /
+the slowest rank's time.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+METRIC = ("router tokens/s (prefill) & µs/call (decode T=1); % of FP4 tensor / HBM roofline")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense ratio (fp4 13.5 PF vs bf16 2.25 PF)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        busy = [r[0] for r in rows if r[0] > 0.5 * r[1]] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_tokens_per_s(w, x32_all, packed_w, bias, budget_s=12.0, rows_per_call=64):
+    """Time the oracle (as it stands) routing slices of the batch for about
+    `budget_s` seconds; the per-tensor gsa is the whole batch's."""
+    from oracle import quantize as Q, gemm, router
+    gsa = Q.global_scale(x32_all)
+    wq, ws, wg = packed_w
+    t0 = time.perf_counter()
+    done = 0
+    r0 = 0
+    while True:
+        rows = x32_all[r0:r0 + rows_per_call]
+        xq, xs, _ = Q.quantize(rows, gsa=gsa)
+        L, _ = gemm.logits(xq, xs, gsa, wq, ws, wg)
+        router.route(L, bias, w.k, w.routed_scaling, w.raw)
+        done += rows.shape[0]
+        r0 = (r0 + rows_per_call) % x32_all.shape[0]
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el, done, el
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def kernel_names(path):
+    return ["amax", "quantize", "gemm_topk"] if path == "tc" else ["decode_router"]
+
+
+def algorithmic(w, T, name):
+    """(bytes, flops) the method must move / compute per launch of `name`."""
+    D, N, k = w.D, w.N, w.k
+    x_bytes = T * D * 2
+    xq = T * (D // 2 + D // 16)
+    wq = N * (D // 2 + D // 16)
+    out = T * k * 8
+    if name == "amax":
+        return x_bytes, 0
+    if name == "quantize":
+        return x_bytes + xq, 0
+    if name == "gemm_topk":
+        return xq + wq + N * 4 + out, 2 * T * D * N
+    return x_bytes + wq + N * 4 + out, 2 * T * D * N           # decode_router
+
+
+def traffic_table():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by kernel;
+    an entry counts only while the kernel's source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    out = {}
+    if not os.path.exists(p):
+        return out
+    for line in open(p):
+        parts = line.split("#")[0].split()
+        if len(parts) == 4:
+            name, nbytes, src, digest = parts
+            f = os.path.join(ROOT, "nvfp4_router_gate_gb300", "csrc", src)
+            if os.path.exists(f) and hashlib.sha256(open(f, "rb").read()).hexdigest()[:16] == digest:
+                out[name] = float(nbytes)
+    return out
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import nvfp4_router_gate_gb300 as R
+    from nvfp4_router_gate_gb300 import _native
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WL.WORKLOADS["prefill"]
+    T = w.T
+    x_np = WL.make_x(w, seed=WL.SEED + rank)
+    W_np = WL.make_w(w)
+    bias_np = WL.make_bias(w)
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    NBUF = 4                                          # 4 x 58.7 MB > 129 MB L2
+    xs = [dev_bf16(x_np) for _ in range(NBUF)]
+    bias = torch.from_numpy(bias_np).to(dev)
+    W_fp4, W_sf, w_gsa = R.nvfp4_pack_weight(dev_bf16(W_np))
+    ws = R.new_workspace(R.router_gate_workspace_size(T, w.D, w.N, w.k), dev)
+    ids = [torch.empty((T, w.k), dtype=torch.int32, device=dev) for _ in range(NBUF)]
+    wts = [torch.empty((T, w.k), dtype=torch.float32, device=dev) for _ in range(NBUF)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        R.router_gate_topk(xs[i % NBUF], W_fp4, W_sf, w_gsa, bias, w.k, w.routed_scaling,
+                           out_ids=ids[i % NBUF], out_w=wts[i % NBUF], workspace=ws)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # per-kernel pass (events between the launches)
+    names = kernel_names("tc")
+    n_prof = max(3, min(args.steps, 500))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))] for _ in range(n_prof)]
+    for e in evs:                                     # torch creates the CUDA event lazily
+        for ev in e:
+            ev.record(stream)
+    torch.cuda.synchronize()
+    handles = [ctypes_array(e) for e in evs]
+    lib = _native.lib()
+    for i in range(n_prof):
+        lib.nvr_set_profile_events(handles[i][0], len(names))
+        step(i)
+    lib.nvr_set_profile_events(None, 0)
+    torch.cuda.synchronize()
+    per = {n: [] for n in names}
+    for e in evs:
+        for j, n in enumerate(names):
+            per[n].append(e[2 * j].elapsed_time(e[2 * j + 1]))
+    hbm, bf16, peak_kind = load_peaks()
+    fp4_peak = bf16 * FP4_OVER_BF16
+    traffic = traffic_table()
+    tot = sum(statistics.mean(v) for v in per.values())
+    kernels = {}
+    for n in names:
+        t_ms = statistics.mean(per[n])
+        b, f = algorithmic(w, T, n)
+        ent = {"ms": t_ms, "share": t_ms / tot}
+        if n == "gemm_topk":
+            ach = f / (t_ms / 1e3) / 1e12
+            ent.update({"bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s",
+                        "frac": ach / fp4_peak,
+                        "hbm_achieved_gbs": b / (t_ms / 1e3) / 1e9})
+        else:
+            ach = b / (t_ms / 1e3) / 1e9
+            ent.update({"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm})
+        ent["traffic"] = traffic.get(n)
+        kernels[n] = ent
+    dom = max(names, key=lambda n: kernels[n]["ms"])
+    roof = {k: kernels[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = dom
+    roof["peak_source"] = peak_kind + (" (fp4 = bf16 x 6 nominal ratio)" if dom == "gemm_topk" else "")
+
+    # end to end: pinned host batch in, ids/weights out, every step
+    x_host = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_host = torch.empty((T, w.k), dtype=torch.int32).pin_memory()
+    w_host = torch.empty((T, w.k), dtype=torch.float32).pin_memory()
+    n_e2e = max(3, min(args.steps, 200))
+
+    def e2e_step(i):
+        xs[i % NBUF].copy_(x_host, non_blocking=True)
+        step(i)
+        ids_host.copy_(ids[i % NBUF], non_blocking=True)
+        w_host.copy_(wts[i % NBUF], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * T * n_e2e / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x_host.numel() * 2),
+           "d2h_bytes_per_step": int(ids_host.numel() * 4 + w_host.numel() * 4), "steps": n_e2e}
+
+    # decode router: T = 1, 8, 64 as CUDA-graph replays
+    decode = {}
+    if not args.skip_decode:
+        dw = WL.WORKLOADS["decode"]
+        gate = R.RouterGate(dev_bf16(WL.make_w(dw)), torch.from_numpy(WL.make_bias(dw)).to(dev),
+                            k=dw.k, routed_scaling=dw.routed_scaling, max_tokens=64)
+        for Td in (1, 8, 64):
+            xd = dev_bf16(WL.make_x(dw.with_T(Td)))
+            s2 = torch.cuda.Stream()
+            s2.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s2):
+                for _ in range(3):
+                    gate(xd)
+            torch.cuda.current_stream().wait_stream(s2)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                gate(xd)
+            for _ in range(50):
+                g.replay()
+            torch.cuda.synchronize()
+            reps = 1000
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            decode["T%d_us_per_call" % Td] = us
+        decode["launches_T1"] = 1
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        from oracle import pipeline
+        x32 = WL.bf16_bits_to_float32(x_np)
+        packed = pipeline.pack_weight(WL.bf16_bits_to_float32(W_np))
+        tps, done, el = oracle_tokens_per_s(w, x32, packed, bias_np)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": "%d tokens of the T=4096 batch in 64-token slices (%.1f s), batch gsa; "
+                         "NumPy quantize + float64 GEMM + epilogue" % (done, el)}
+
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1*ue4m3->f32", "data": "synthetic",
+        "config": {"workload": "prefill router T=4096 D=7168 E=256 k=8, bf16 x with per-token "
+                               "LogNormal(0,1) scale, NVFP4 gate W~N(0,0.02), bias U(-0.05,0.05), "
+                               "routed_scaling 2.5",
+                   "T": T, "D": w.D, "E": w.N, "k": w.k,
+                   "l2": "inputs larger than L2: 4 rotating 58.7 MB activation buffers",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "e2e": e2e, "gpu_launches": 3 * args.steps, "roofline": roof, "kernels": kernels,
+        "decode": decode, "cpu_baseline": cpu, "clocks": clocks,
+    }
+
+
+def ctypes_array(events):
+    import ctypes
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def run_reference(args, rank):
+    """The CPU oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    from oracle import pipeline
+    w = WL.WORKLOADS["prefill"]
+    x32 = WL.bf16_bits_to_float32(WL.make_x(w))
+    W_np = WL.make_w(w)
+    bias = WL.make_bias(w)
+    packed = pipeline.pack_weight(WL.bf16_bits_to_float32(W_np))
+    budget = min(15.0, max(1.0, 60.0 / max(1, args.steps + args.warmup)))   # ~1 minute in all
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(w, x32, packed, bias, budget_s=0.5)
+    vals, done, el = [], 0, 0.0
+    for _ in range(args.steps):
+        v, d, e = oracle_tokens_per_s(w, x32, packed, bias, budget_s=budget)
+        vals.append(v)
+        done += d
+        el += e
+    value = done / el
+    sample = ("%d steps, each ~%.1f s of 64-token slices of the T=4096 prefill batch (batch gsa); "
+              "NumPy quantize + float64 GEMM + epilogue" % (args.steps, budget))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "prefill router T=4096 D=7168 E=256 k=8 (CPU oracle sample)",
+                       "T": w.T, "D": w.D, "E": w.N, "k": w.k},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+        if out is not None:
+            print(json.dumps(out))
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    from nvfp4_router_gate_gb300 import build
+    build.build()
+    out = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

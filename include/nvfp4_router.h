@@ -1,0 +1,237 @@
+/*
+ * nvfp4_router.h -- C ABI of the GB300 (sm_103a) NVFP4 MoE router gate.
+ *
+ * One router call turns a batch of token activations x [T, D] into, per token,
+ * the k selected expert ids and their routing weights:
+ *
+ *   1. runtime NVFP4 quantization of x: one global scale per call,
+ *      gsa = max|x| / (6 * 448), 16-element blocks along D with an E4M3 scale
+ *      byte each and E2M1 4-bit codes
+ *      ("nvfp4-megamoe-kernel commit 04cf8ca: dsv4/layers/router.py",
+ *      runtime-gsa section; "commit df05289: dsv4/layers/grouped_linear.py",
+ *      zero-sync fused quantize section);
+ *   2. the block-scaled NVFP4 gate GEMM  logits = x . W_gate^T  against
+ *      NVFP4-packed expert weights (router.py page, NVFP4 gate section);
+ *   3. the fused "activation_topk" epilogue: sigmoid scores, top-k on
+ *      score + bias, gather of the unbiased scores, renormalisation by their
+ *      sum and multiplication by routed_scaling, written as int32 ids and fp32
+ *      weights ("commit e0f60b9: dsv4/kernels/router/__init__.py",
+ *      activation_topk section).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All array pointers are DEVICE pointers owned by the caller.  The library
+ *   never allocates or frees device memory and keeps no per-call host state;
+ *   the only global state is a per-device cache of attributes (SM count,
+ *   kernel attributes), set on first use.
+ * - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t,
+ *   NULL = legacy default stream).  They never synchronise the host and never
+ *   copy the global scales to the host, so they can be captured in a CUDA
+ *   graph.  Errors found on the host are returned before any launch.
+ * - Arguments checked on the host (status NVR_ERR_INVALID_ARG unless noted):
+ *   null pointers; T < 0, D <= 0, D % 64 != 0, N <= 0; dtype not BF16/F32;
+ *   k < 1, k > 16, k > N; array pointers not 16-byte aligned
+ *   (NVR_ERR_ALIGNMENT); workspace smaller than the size query returns
+ *   (NVR_ERR_WORKSPACE).  T == 0 is a valid empty call that launches nothing.
+ * - A failed launch returns NVR_ERR_CUDA (the CUDA error is consumed).
+ * - Device-side bounded waits that time out (never expected in a correct
+ *   build; each wait is limited to about one second) store NVR_ERR_TIMEOUT in
+ *   the workspace status word, which nvr_read_device_status returns.
+ * - Workspace: caller-allocated device memory of at least the size the
+ *   matching *_workspace_size function returns, 256-byte aligned, ZEROED ONCE
+ *   before first use.  Every call leaves its counters at zero again, so the
+ *   same workspace serves any number of calls on one stream.  Calls that share
+ *   a workspace must not run concurrently.  After a call that returned an
+ *   error or timed out, zero the workspace again.
+ * - Non-finite inputs (NaN, Inf) are outside the contract: the output is
+ *   unspecified but the kernels do not fault.
+ *
+ * Data layouts
+ * ------------
+ * - x: [T, D] row-major, bf16 (NVR_BF16) or fp32 (NVR_F32).
+ * - packed codes: [rows, D/2] uint8, element 2j in the low nibble of byte j.
+ * - scale bytes, NVR_SF_LINEAR: [rows, D/16] uint8 row-major.
+ * - scale bytes, NVR_SF_TILED: the tensor-core tile layout: tiles of 128 rows
+ *   x 4 scale columns (512 bytes); inside a tile the byte of (row r, column c)
+ *   sits at 16*(r%32) + 4*((r%128)/32) + (c%4); tile (r/128, c/4) starts at
+ *   ((r/128)*(D/64) + c/4) * 512.  Rows are padded to a multiple of 128 with
+ *   zero bytes; the buffer holds nvr_sf_bytes(rows, D, NVR_SF_TILED) bytes.
+ * - global scales: one fp32 in device memory.
+ */
+#ifndef NVFP4_ROUTER_H
+#define NVFP4_ROUTER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvr_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+  NVR_OK = 0,
+  NVR_ERR_INVALID_ARG = 1,
+  NVR_ERR_UNSUPPORTED = 2,
+  NVR_ERR_ALIGNMENT = 3,
+  NVR_ERR_WORKSPACE = 4,
+  NVR_ERR_CUDA = 5,
+  NVR_ERR_TIMEOUT = 6
+} nvr_status;
+
+typedef enum { NVR_BF16 = 0, NVR_F32 = 1 } nvr_dtype;
+
+typedef enum { NVR_SF_LINEAR = 0, NVR_SF_TILED = 1 } nvr_sf_layout;
+
+/* router_gate_topk flags */
+enum {
+  /* Raw-logit head: no sigmoid, bias, renormalisation or scaling.  The top-k
+   * is taken on the fp32 logits and out_w receives the selected logits. */
+  NVR_FLAG_RAW_LOGITS = 1u,
+  /* Kernel choice for tests and benchmarks.  By default the shape decides:
+   * T <= 16 tokens (with T*D and N small enough for one CTA's shared memory)
+   * run the single-launch decode kernel, everything else the tensor-core
+   * pipeline.  FORCE_TENSOR_CORE always takes the tensor-core pipeline;
+   * FORCE_DECODE takes the single-launch kernel or returns
+   * NVR_ERR_UNSUPPORTED when the shape is outside its limits.  Both give
+   * results within the same tolerances; they are not bit-identical (the
+   * fp32 accumulation order of the logits differs). */
+  NVR_FLAG_FORCE_TENSOR_CORE = 2u,
+  NVR_FLAG_FORCE_DECODE = 4u
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvr_status_string(nvr_status s);
+
+/* Bytes of a scale-byte buffer for [rows, D] in the given layout
+ * (0 for invalid arguments). */
+size_t nvr_sf_bytes(int64_t rows, int64_t D, nvr_sf_layout layout);
+
+/* Workspace bytes nvfp4_quantize_act / nvfp4_pack_weight need for up to
+ * `rows` rows of length D. */
+size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t D);
+
+/*
+ * nvfp4_quantize_act -- runtime NVFP4 quantization of one activation tensor.
+ *
+ * Source: "nvfp4-megamoe-kernel commit 04cf8ca: dsv4/layers/router.py",
+ * runtime-gsa section (gsa = max|x| / (6.0 * 448.0), so x/gsa <= 2688), and
+ * "commit df05289: dsv4/layers/grouped_linear.py", zero-sync fused quantize
+ * section (all rows flattened into one tensor, one global scale, computed
+ * and kept on the GPU).
+ *
+ * Computes, in IEEE fp32 with round-to-nearest-even:
+ *   amax = max |x| over all T*D elements; *x_gsa = amax / 2688;
+ *   per element y = x / gsa; per 16-element block sy = max|y| / 6,
+ *   scale byte = E4M3(sy) (nearest-even, saturating at 448);
+ *   code = E2M1(y / dec(byte)) (nearest-even, saturating at 6, sign kept);
+ *   a block whose scale byte is 0 has all codes 0; amax == 0 gives gsa 0 and
+ *   all-zero output.
+ *
+ *   x         [T, D] input (bf16 or fp32 per dt), 16-byte aligned
+ *   x_fp4     out [T, D/2] packed codes
+ *   x_sf      out scale bytes in `sf_layout` (nvr_sf_bytes(T, D, sf_layout))
+ *   x_gsa     out, one fp32 (device)
+ *   workspace nvfp4_quantize_workspace_size(T, D) bytes, zeroed once
+ * Two kernels (amax with a grid-level reduce, then quantize); no host sync.
+ */
+nvr_status nvfp4_quantize_act(const void* x, nvr_dtype dt, int64_t T, int64_t D,
+                              uint8_t* x_fp4, uint8_t* x_sf, nvr_sf_layout sf_layout,
+                              float* x_gsa, void* workspace, size_t ws_bytes,
+                              nvr_stream_t stream);
+
+/*
+ * nvfp4_pack_weight -- load-time NVFP4 quantization of the gate weight.
+ *
+ * Source: "nvfp4-megamoe-kernel commit 04cf8ca: dsv4/layers/router.py",
+ * NVFP4 gate section (BF16 gate weights are quantized and loaded into the
+ * NVFP4 linear layer); "commit df05289", lm_head item (BF16 weight quantized
+ * to NVFP4 at load time).
+ *
+ * The same arithmetic as nvfp4_quantize_act applied to W [N, D] with its own
+ * global scale *w_gsa; scales always in the NVR_SF_TILED layout
+ * (W_sf holds nvr_sf_bytes(N, D, NVR_SF_TILED) bytes).  Called once at load;
+ * W_fp4, W_sf and w_gsa then stay resident and are passed to router_gate_topk.
+ */
+nvr_status nvfp4_pack_weight(const void* W, nvr_dtype dt, int64_t N, int64_t D,
+                             uint8_t* W_fp4, uint8_t* W_sf, float* w_gsa,
+                             void* workspace, size_t ws_bytes, nvr_stream_t stream);
+
+/* Workspace bytes router_gate_topk / router_gate_logits need for up to
+ * T_max tokens with this D, N and k (k is ignored by router_gate_logits). */
+size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k);
+
+/*
+ * router_gate_topk -- the whole router call: quantize x, NVFP4 gate GEMM,
+ * fused sigmoid / biased top-k / renormalise / scale epilogue.
+ *
+ * Sources: the three sections cited at the top of this file; the fused
+ * single-kernel GEMM + router epilogue with a row-level top-k across
+ * N-subtiles ("commit 04cf8ca", fused dispatch section; "commit e0f60b9",
+ * fused decode kernel notes).
+ *
+ *   x            [T, D] activations (bf16 or fp32 per dt)
+ *   W_fp4        [N, D/2] packed gate weight from nvfp4_pack_weight
+ *   W_scales     its scale bytes (NVR_SF_TILED)
+ *   w_gsa        its global scale (device fp32)
+ *   bias         [N] fp32 score-correction bias added to the scores for
+ *                selection only, or NULL for none (ignored in RAW mode)
+ *   k            experts per token, 1 <= k <= min(16, N)
+ *   routed_scaling  multiplies the renormalised weights
+ *   flags        0 or NVR_FLAG_RAW_LOGITS
+ *   out_ids      out [T, k] int32: expert ids, best first (key descending,
+ *                equal keys: lower id first)
+ *   out_w        out [T, k] fp32: routed_scaling * s_id / sum of the k
+ *                selected sigmoid scores s (RAW: the selected logits)
+ *   workspace    router_gate_workspace_size(T, D, N, k) bytes, zeroed once
+ *
+ * The logits never leave the chip on the tensor-core path: they are consumed
+ * from tensor memory by the epilogue.  Small batches (decode) run as a single
+ * kernel launch; larger ones as amax, quantize and GEMM+top-k launches.
+ */
+nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
+                            const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,
+                            int64_t N, const float* bias, int k, float routed_scaling,
+                            uint32_t flags, int32_t* out_ids, float* out_w,
+                            void* workspace, size_t ws_bytes, nvr_stream_t stream);
+
+/*
+ * router_gate_logits -- test hook: the same quantization and gate GEMM as
+ * router_gate_topk, writing the fp32 logits [T, N] (row-major,
+ * logit = acc * gsa_x * gsa_w) instead of the epilogue's outputs.  Used to
+ * check the GEMM on its own and to measure what writing logits to memory
+ * costs.  flags: 0, NVR_FLAG_FORCE_TENSOR_CORE or NVR_FLAG_FORCE_DECODE
+ * (RAW_LOGITS is invalid here).  Workspace as for router_gate_topk.
+ */
+nvr_status router_gate_logits(const void* x, nvr_dtype dt, int64_t T, int64_t D,
+                              const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,
+                              int64_t N, uint32_t flags, float* logits, void* workspace,
+                              size_t ws_bytes, nvr_stream_t stream);
+
+/*
+ * nvr_set_profile_events -- measurement hook (no counterpart on the pages; it
+ * serves the benchmark's per-kernel roofline).  When `events` is not NULL,
+ * every later call of nvfp4_quantize_act, nvfp4_pack_weight,
+ * router_gate_topk and router_gate_logits records events[2*i] just before and
+ * events[2*i+1] just after its i-th kernel launch (i < n_pairs), on the call's
+ * stream; launches beyond n_pairs are not bracketed.  The events are
+ * cudaEvent_t handles created by the caller.  Recording an event between two
+ * launches removes their programmatic overlap, so time whole calls with the
+ * hook off.  NULL (or n_pairs <= 0) turns the hook off.  Process-wide
+ * setting; not thread-safe.
+ */
+nvr_status nvr_set_profile_events(void* const* events, int n_pairs);
+
+/*
+ * nvr_read_device_status -- copy the workspace status word to *out (blocking
+ * read on `stream`; do not call during stream capture).  NVR_OK unless a
+ * device-side bounded wait timed out (NVR_ERR_TIMEOUT).
+ */
+nvr_status nvr_read_device_status(const void* workspace, nvr_stream_t stream, nvr_status* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_ROUTER_H */

@@ -1,0 +1,191 @@
+"""GB300 (sm_103a) NVFP4 MoE router gate: Python binding of the C ABI.
+
+Every step of the router runs in the library's CUDA kernels; this module only
+checks tensor arguments, allocates outputs with PyTorch when the caller does not
+pass them, and forwards raw device pointers and the current CUDA stream.
+
+Functions (same names as include/nvfp4_router.h):
+
+* ``nvfp4_quantize_act(x, sf_layout="linear")`` -> (x_fp4, x_sf, x_gsa)
+* ``nvfp4_pack_weight(W)`` -> (W_fp4, W_sf, w_gsa)  (tile-layout scales)
+* ``router_gate_topk(x, W_fp4, W_sf, w_gsa, bias, k, routed_scaling, raw=False)``
+  -> (ids int32 [T, k], weights fp32 [T, k])
+* ``router_gate_logits(x, W_fp4, W_sf, w_gsa)`` -> logits fp32 [T, N]
+* ``router_gate_workspace_size``, ``nvfp4_quantize_workspace_size``,
+  ``nvr_sf_bytes``, ``nvr_read_device_status``
+
+``RouterGate`` keeps the packed weight, the workspace and the output buffers
+resident so that a call allocates nothing (CUDA-graph capturable).
+"""
+
+import ctypes
+
+import torch
+
+from . import _native
+from ._native import (NVR_FLAG_FORCE_DECODE, NVR_FLAG_FORCE_TENSOR_CORE, NVR_FLAG_RAW_LOGITS,
+                      RouterError)
+
+__all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits",
+           "router_gate_workspace_size", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
+           "nvr_read_device_status", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
+           "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "new_workspace"]
+
+_LAYOUTS = {"linear": _native.NVR_SF_LINEAR, "tiled": _native.NVR_SF_TILED}
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return _native.NVR_BF16
+    if t.dtype == torch.float32:
+        return _native.NVR_F32
+    raise TypeError("activations must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _dev(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def nvr_sf_bytes(rows, D, layout="linear"):
+    return int(_native.lib().nvr_sf_bytes(rows, D, _LAYOUTS[layout]))
+
+
+def nvfp4_quantize_workspace_size(rows, D):
+    return int(_native.lib().nvfp4_quantize_workspace_size(rows, D))
+
+
+def router_gate_workspace_size(T_max, D, N, k=8):
+    return int(_native.lib().router_gate_workspace_size(T_max, D, N, k))
+
+
+def new_workspace(nbytes, device=None):
+    """A zeroed, 256-byte aligned workspace (torch allocations are aligned)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def nvfp4_quantize_act(x, sf_layout="linear", x_fp4=None, x_sf=None, x_gsa=None, workspace=None,
+                       stream=None):
+    """Runtime NVFP4 quantization of x [T, D] (bf16/fp32) with one global scale."""
+    T, D = x.shape
+    dev = x.device
+    if x_fp4 is None:
+        x_fp4 = torch.empty((T, D // 2), dtype=torch.uint8, device=dev)
+    if x_sf is None:
+        x_sf = torch.empty(nvr_sf_bytes(T, D, sf_layout), dtype=torch.uint8, device=dev)
+    if x_gsa is None:
+        x_gsa = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(nvfp4_quantize_workspace_size(T, D), dev)
+    st = _native.lib().nvfp4_quantize_act(
+        _dev(x, "x"), _dtype_code(x), T, D, _dev(x_fp4, "x_fp4"), _dev(x_sf, "x_sf"),
+        _LAYOUTS[sf_layout], _dev(x_gsa, "x_gsa"), _dev(workspace, "workspace"),
+        workspace.numel(), _stream(stream))
+    _native.check("nvfp4_quantize_act", st)
+    return x_fp4, x_sf, x_gsa
+
+
+def nvfp4_pack_weight(W, W_fp4=None, W_sf=None, w_gsa=None, workspace=None, stream=None):
+    """Load-time NVFP4 quantization of the gate weight W [N, D]; tile-layout scales."""
+    N, D = W.shape
+    dev = W.device
+    if W_fp4 is None:
+        W_fp4 = torch.empty((N, D // 2), dtype=torch.uint8, device=dev)
+    if W_sf is None:
+        W_sf = torch.empty(nvr_sf_bytes(N, D, "tiled"), dtype=torch.uint8, device=dev)
+    if w_gsa is None:
+        w_gsa = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(nvfp4_quantize_workspace_size(N, D), dev)
+    st = _native.lib().nvfp4_pack_weight(
+        _dev(W, "W"), _dtype_code(W), N, D, _dev(W_fp4, "W_fp4"), _dev(W_sf, "W_sf"),
+        _dev(w_gsa, "w_gsa"), _dev(workspace, "workspace"), workspace.numel(), _stream(stream))
+    _native.check("nvfp4_pack_weight", st)
+    return W_fp4, W_sf, w_gsa
+
+
+def router_gate_topk(x, W_fp4, W_sf, w_gsa, bias=None, k=8, routed_scaling=1.0, raw=False,
+                     out_ids=None, out_w=None, workspace=None, flags=0, stream=None):
+    """Route x [T, D]: returns (ids int32 [T, k], weights fp32 [T, k])."""
+    T, D = x.shape
+    N = W_fp4.shape[0]
+    dev = x.device
+    if out_ids is None:
+        out_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if out_w is None:
+        out_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(router_gate_workspace_size(T, D, N, k), dev)
+    f = int(flags) | (NVR_FLAG_RAW_LOGITS if raw else 0)
+    st = _native.lib().router_gate_topk(
+        _dev(x, "x"), _dtype_code(x), T, D, _dev(W_fp4, "W_fp4"), _dev(W_sf, "W_sf"),
+        _dev(w_gsa, "w_gsa"), N, None if bias is None else _dev(bias, "bias"), int(k),
+        float(routed_scaling), f, _dev(out_ids, "out_ids"), _dev(out_w, "out_w"),
+        _dev(workspace, "workspace"), workspace.numel(), _stream(stream))
+    _native.check("router_gate_topk", st)
+    return out_ids, out_w
+
+
+def router_gate_logits(x, W_fp4, W_sf, w_gsa, logits=None, workspace=None, flags=0, stream=None):
+    """Test hook: the gate logits [T, N] fp32 of the quantized operands."""
+    T, D = x.shape
+    N = W_fp4.shape[0]
+    dev = x.device
+    if logits is None:
+        logits = torch.empty((T, N), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(router_gate_workspace_size(T, D, N, 1), dev)
+    st = _native.lib().router_gate_logits(
+        _dev(x, "x"), _dtype_code(x), T, D, _dev(W_fp4, "W_fp4"), _dev(W_sf, "W_sf"),
+        _dev(w_gsa, "w_gsa"), N, int(flags), _dev(logits, "logits"), _dev(workspace, "workspace"),
+        workspace.numel(), _stream(stream))
+    _native.check("router_gate_logits", st)
+    return logits
+
+
+def nvr_read_device_status(workspace, stream=None):
+    """The workspace status word (0 = ok, 6 = a device-side wait timed out)."""
+    out = ctypes.c_int(0)
+    st = _native.lib().nvr_read_device_status(_dev(workspace, "workspace"), _stream(stream),
+                                              ctypes.byref(out))
+    _native.check("nvr_read_device_status", st)
+    return out.value
+
+
+class RouterGate:
+    """Resident router: packed NVFP4 gate weight, bias, workspace and outputs.
+
+    ``gate(x)`` routes up to ``max_tokens`` tokens and returns views of the
+    resident output buffers; nothing is allocated per call, so a call can be
+    captured in a CUDA graph.
+    """
+
+    def __init__(self, W, bias=None, k=8, routed_scaling=1.0, raw=False, max_tokens=4096):
+        self.N, self.D = W.shape
+        self.k, self.routed_scaling, self.raw = int(k), float(routed_scaling), bool(raw)
+        dev = W.device
+        self.W_fp4, self.W_sf, self.w_gsa = nvfp4_pack_weight(W)
+        self.bias = None if bias is None else bias.to(device=dev, dtype=torch.float32).contiguous()
+        self.max_tokens = int(max_tokens)
+        self.workspace = new_workspace(
+            router_gate_workspace_size(self.max_tokens, self.D, self.N, self.k), dev)
+        self.ids = torch.empty((self.max_tokens, self.k), dtype=torch.int32, device=dev)
+        self.weights = torch.empty((self.max_tokens, self.k), dtype=torch.float32, device=dev)
+
+    def __call__(self, x, flags=0, stream=None):
+        T = x.shape[0]
+        if T > self.max_tokens:
+            raise ValueError("batch of %d tokens exceeds max_tokens=%d" % (T, self.max_tokens))
+        ids, w = self.ids[:T], self.weights[:T]
+        router_gate_topk(x, self.W_fp4, self.W_sf, self.w_gsa, self.bias, self.k, self.routed_scaling,
+                         self.raw, out_ids=ids, out_w=w, workspace=self.workspace, flags=flags,
+                         stream=stream)
+        return ids, w

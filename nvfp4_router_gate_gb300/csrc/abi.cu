@@ -1,0 +1,320 @@
+// abi.cu -- the extern "C" entry points of include/nvfp4_router.h: argument
+// checks (all on the host, before any launch), the workspace layout, and the
+// choice between the single-launch decode kernel and the amax -> quantize ->
+// tensor-core GEMM+top-k pipeline.
+#include <mutex>
+
+#include "nvr_internal.h"
+
+namespace nvr {
+
+TensorMapEncodeFn tensor_map_encoder() {
+  static TensorMapEncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<TensorMapEncodeFn>(p);
+  });
+  return fn;
+}
+
+int device_sm_count() {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+int amax_grid(int64_t n_elems, bool bf16, int num_sms) {
+  const int64_t nvec = n_elems * (bf16 ? 2 : 4) / 16;
+  int64_t want = (nvec + kAmaxThreads * 4 - 1) / (kAmaxThreads * 4);   // >= 4 vectors per thread
+  int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 4;
+  if (cap > kMaxAmaxGrid) cap = kMaxAmaxGrid;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  return static_cast<int>(want);
+}
+
+static size_t a256(size_t v) { return (v + 255) / 256 * 256; }
+
+WsLayout quantize_ws_layout(int64_t rows, int64_t D) {
+  (void)rows; (void)D;
+  WsLayout L;
+  L.control = 0;
+  L.amax_partials = 256;
+  L.scalars = a256(L.amax_partials + kMaxAmaxGrid * 4);
+  L.total = L.scalars + 256;
+  return L;
+}
+
+static int split_bound(int m_tiles, int n_tiles) {
+  // the most splits plan_gemm can choose on any GPU with <= 256 SMs
+  int s = 256 / (m_tiles > 0 ? m_tiles : 1);
+  if (s < 1) s = 1;
+  if (s > n_tiles) s = n_tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s;
+}
+
+WsLayout router_ws_layout(int64_t T, int64_t D, int64_t N) {
+  WsLayout L = quantize_ws_layout(T, D);
+  const int64_t rows_pad = (T + 127) / 128 * 128;
+  const int m_tiles = static_cast<int>(rows_pad / 128);
+  const int n_tiles = static_cast<int>((N + 127) / 128);
+  L.tickets = L.total;
+  L.x_codes = a256(L.tickets + static_cast<size_t>(m_tiles) * 4);
+  L.x_sf = a256(L.x_codes + static_cast<size_t>(rows_pad) * (D / 2));
+  L.partials = a256(L.x_sf + static_cast<size_t>(rows_pad) * (D / 16));
+  const int splits = split_bound(m_tiles, n_tiles);
+  const size_t part = splits > 1 ? static_cast<size_t>(m_tiles) * splits * 128 * kMaxKmax * 16 : 0;
+  L.decode = a256(L.partials + part);
+  const size_t dec = T <= 16 ? static_cast<size_t>(T) * N * 8 : 0;
+  L.total = a256(L.decode + dec);
+  return L;
+}
+
+}  // namespace nvr
+
+using namespace nvr;
+
+namespace {
+
+// measurement hook (nvr_set_profile_events)
+void* const* g_prof_events = nullptr;
+int g_prof_pairs = 0;
+
+struct ProfileScope {
+  cudaStream_t s;
+  int i = 0;
+  explicit ProfileScope(cudaStream_t st) : s(st) {}
+  void before() {
+    if (g_prof_events && i < g_prof_pairs) cudaEventRecord(static_cast<cudaEvent_t>(g_prof_events[2 * i]), s);
+  }
+  void after() {
+    if (g_prof_events && i < g_prof_pairs) cudaEventRecord(static_cast<cudaEvent_t>(g_prof_events[2 * i + 1]), s);
+    ++i;
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+nvr_status check_common(const void* x, nvr_dtype dt, int64_t T, int64_t D, const void* ws) {
+  if (!x || !ws) return NVR_ERR_INVALID_ARG;
+  if (T < 0 || D <= 0 || D % 64 != 0 || D > (1 << 24)) return NVR_ERR_INVALID_ARG;
+  if (dt != NVR_BF16 && dt != NVR_F32) return NVR_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NVR_ERR_ALIGNMENT;
+  return NVR_OK;
+}
+
+nvr_status quantize_impl(const void* x, nvr_dtype dt, int64_t rows, int64_t D, uint8_t* codes,
+                         uint8_t* sf, nvr_sf_layout layout, float* gsa, void* ws, size_t ws_bytes,
+                         cudaStream_t s) {
+  nvr_status st = check_common(x, dt, rows, D, ws);
+  if (st != NVR_OK) return st;
+  if (!codes || !sf || !gsa) return NVR_ERR_INVALID_ARG;
+  if (layout != NVR_SF_LINEAR && layout != NVR_SF_TILED) return NVR_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(sf) || (reinterpret_cast<uintptr_t>(gsa) & 3u)) return NVR_ERR_ALIGNMENT;
+  const WsLayout L = quantize_ws_layout(rows, D);
+  if (ws_bytes < L.total) return NVR_ERR_WORKSPACE;
+  if (rows == 0) return NVR_OK;
+  const int sms = device_sm_count();
+  if (sms <= 0) return NVR_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const bool bf16 = dt == NVR_BF16;
+  float* amax = reinterpret_cast<float*>(w + L.scalars + 4);
+  ProfileScope prof(s);
+  prof.before();
+  cudaError_t e = launch_amax(x, bf16, rows * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
+                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), gsa, amax,
+                              amax_grid(rows * D, bf16, sms), s);
+  prof.after();
+  if (e != cudaSuccess) return NVR_ERR_CUDA;
+  prof.before();
+  e = launch_quantize(x, bf16, rows, D, layout == NVR_SF_TILED, amax, codes, sf, s);
+  prof.after();
+  return e == cudaSuccess ? NVR_OK : NVR_ERR_CUDA;
+}
+
+nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
+                       const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias, int k,
+                       float routed_scaling, uint32_t flags, int32_t* out_ids, float* out_w,
+                       float* logits, void* ws, size_t ws_bytes, cudaStream_t s) {
+  nvr_status st = check_common(x, dt, T, D, ws);
+  if (st != NVR_OK) return st;
+  if (!W_fp4 || !W_sf || !w_gsa || N <= 0 || N > (1 << 28)) return NVR_ERR_INVALID_ARG;
+  if (!logits && (!out_ids || !out_w || k < 1 || k > kMaxKmax || k > N)) return NVR_ERR_INVALID_ARG;
+  if (flags & ~static_cast<uint32_t>(NVR_FLAG_RAW_LOGITS | NVR_FLAG_FORCE_TENSOR_CORE | NVR_FLAG_FORCE_DECODE))
+    return NVR_ERR_INVALID_ARG;
+  if ((flags & NVR_FLAG_FORCE_TENSOR_CORE) && (flags & NVR_FLAG_FORCE_DECODE)) return NVR_ERR_INVALID_ARG;
+  if (!aligned16(W_fp4) || !aligned16(W_sf) || (reinterpret_cast<uintptr_t>(w_gsa) & 3u) ||
+      (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
+      (out_ids && (reinterpret_cast<uintptr_t>(out_ids) & 3u)) ||
+      (out_w && (reinterpret_cast<uintptr_t>(out_w) & 3u)) ||
+      (logits && (reinterpret_cast<uintptr_t>(logits) & 3u)))
+    return NVR_ERR_ALIGNMENT;
+  const WsLayout L = router_ws_layout(T, D, N);
+  if (ws_bytes < L.total) return NVR_ERR_WORKSPACE;
+  if (T == 0) return NVR_OK;
+  const int sms = device_sm_count();
+  if (sms <= 0) return NVR_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const bool bf16 = dt == NVR_BF16;
+  const bool raw = (flags & NVR_FLAG_RAW_LOGITS) != 0;
+  if (logits) k = 1;
+
+  const DecodePlan dp = plan_decode(T, D, N, sms);
+  const bool use_decode = (flags & NVR_FLAG_FORCE_DECODE) ? true
+                          : (flags & NVR_FLAG_FORCE_TENSOR_CORE) ? false
+                          : dp.ok;
+  if (use_decode) {
+    if (!dp.ok) return NVR_ERR_UNSUPPORTED;
+    float* keys = reinterpret_cast<float*>(w + L.decode);
+    float* scores = keys + T * N;
+    ProfileScope prof(s);
+    prof.before();
+    cudaError_t e = launch_decode(x, bf16, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
+                                  out_ids, out_w, logits, keys, scores,
+                                  reinterpret_cast<uint32_t*>(w + kWsDecodeTicket), dp, s);
+    prof.after();
+    return e == cudaSuccess ? NVR_OK : NVR_ERR_CUDA;
+  }
+  float* x_gsa = reinterpret_cast<float*>(w + L.scalars);
+  float* amax = x_gsa + 1;
+  uint8_t* xc = w + L.x_codes;
+  uint8_t* xsf = w + L.x_sf;
+  ProfileScope prof(s);
+  prof.before();
+  cudaError_t e = launch_amax(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
+                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, amax,
+                              amax_grid(T * D, bf16, sms), s);
+  prof.after();
+  if (e != cudaSuccess) return NVR_ERR_CUDA;
+  prof.before();
+  e = launch_quantize(x, bf16, T, D, true, amax, xc, xsf, s);
+  prof.after();
+  if (e != cudaSuccess) return NVR_ERR_CUDA;
+  const GemmPlan g = plan_gemm(T, N, sms);
+  prof.before();
+  st = launch_gemm_topk(xc, xsf, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
+                        out_ids, out_w, logits, reinterpret_cast<float4*>(w + L.partials),
+                        reinterpret_cast<uint32_t*>(w + L.tickets),
+                        reinterpret_cast<uint32_t*>(w + kWsStatus), g, s);
+  prof.after();
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvr_status_string(nvr_status s) {
+  switch (s) {
+    case NVR_OK: return "ok";
+    case NVR_ERR_INVALID_ARG: return "invalid argument";
+    case NVR_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case NVR_ERR_ALIGNMENT: return "pointer not aligned (16 bytes for arrays, 256 for the workspace)";
+    case NVR_ERR_WORKSPACE: return "workspace too small";
+    case NVR_ERR_CUDA: return "CUDA error";
+    case NVR_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t nvr_sf_bytes(int64_t rows, int64_t D, nvr_sf_layout layout) {
+  if (rows < 0 || D <= 0 || D % 64 != 0) return 0;
+  if (layout == NVR_SF_LINEAR) return static_cast<size_t>(rows) * (D / 16);
+  if (layout == NVR_SF_TILED) return static_cast<size_t>((rows + 127) / 128 * 128) * (D / 16);
+  return 0;
+}
+
+size_t nvfp4_quantize_workspace_size(int64_t rows, int64_t D) {
+  return quantize_ws_layout(rows, D).total;
+}
+
+nvr_status nvfp4_quantize_act(const void* x, nvr_dtype dt, int64_t T, int64_t D, uint8_t* x_fp4,
+                              uint8_t* x_sf, nvr_sf_layout sf_layout, float* x_gsa, void* workspace,
+                              size_t ws_bytes, nvr_stream_t stream) {
+  return quantize_impl(x, dt, T, D, x_fp4, x_sf, sf_layout, x_gsa, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvr_status nvfp4_pack_weight(const void* W, nvr_dtype dt, int64_t N, int64_t D, uint8_t* W_fp4,
+                             uint8_t* W_sf, float* w_gsa, void* workspace, size_t ws_bytes,
+                             nvr_stream_t stream) {
+  return quantize_impl(W, dt, N, D, W_fp4, W_sf, NVR_SF_TILED, w_gsa, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k) {
+  (void)k;
+  if (T_max < 0 || D <= 0 || D % 64 != 0 || N <= 0) return 0;
+  // An upper bound of router_ws_layout(T, D, N).total over every T <= T_max:
+  // the split-partials and decode regions do not grow monotonically with T.
+  const int64_t rows_pad = (T_max + 127) / 128 * 128;
+  const int m_max = static_cast<int>(rows_pad / 128);
+  const int n_tiles = static_cast<int>((N + 127) / 128);
+  size_t part = 0;
+  for (int m = 1; m <= m_max; ++m) {
+    const int sp = split_bound(m, n_tiles);
+    if (sp > 1) {
+      const size_t v = static_cast<size_t>(m) * sp * 128 * kMaxKmax * 16;
+      if (v > part) part = v;
+    }
+  }
+  const int64_t t_dec = T_max < 16 ? T_max : 16;
+  return quantize_ws_layout(T_max, D).total + static_cast<size_t>(m_max) * 4 +
+         static_cast<size_t>(rows_pad) * (D / 2) + static_cast<size_t>(rows_pad) * (D / 16) + part +
+         static_cast<size_t>(t_dec) * N * 8 + 8 * 256;
+}
+
+nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
+                            const uint8_t* W_scales, const float* w_gsa, int64_t N, const float* bias,
+                            int k, float routed_scaling, uint32_t flags, int32_t* out_ids,
+                            float* out_w, void* workspace, size_t ws_bytes, nvr_stream_t stream) {
+  if (!out_ids || !out_w) return NVR_ERR_INVALID_ARG;
+  return router_impl(x, dt, T, D, W_fp4, W_scales, w_gsa, N, bias, k, routed_scaling, flags, out_ids,
+                     out_w, nullptr, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvr_status router_gate_logits(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
+                              const uint8_t* W_scales, const float* w_gsa, int64_t N, uint32_t flags,
+                              float* logits, void* workspace, size_t ws_bytes, nvr_stream_t stream) {
+  if (!logits) return NVR_ERR_INVALID_ARG;
+  if (flags & NVR_FLAG_RAW_LOGITS) return NVR_ERR_INVALID_ARG;
+  return router_impl(x, dt, T, D, W_fp4, W_scales, w_gsa, N, nullptr, 1, 1.0f, flags, nullptr, nullptr,
+                     logits, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvr_status nvr_set_profile_events(void* const* events, int n_pairs) {
+  if (events && n_pairs > 0) {
+    g_prof_events = events;
+    g_prof_pairs = n_pairs;
+  } else {
+    g_prof_events = nullptr;
+    g_prof_pairs = 0;
+  }
+  return NVR_OK;
+}
+
+nvr_status nvr_read_device_status(const void* workspace, nvr_stream_t stream, nvr_status* out) {
+  if (!workspace || !out) return NVR_ERR_INVALID_ARG;
+  uint32_t v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, static_cast<const uint8_t*>(workspace) + kWsStatus, 4, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return NVR_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NVR_ERR_CUDA;
+  *out = static_cast<nvr_status>(v);
+  return NVR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// nvr_internal.h -- host-side declarations shared by the router's .cu files:
+// launch configurations, the workspace layout and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4_router.h"
+#include "nvr_device.cuh"
+
+namespace nvr {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kQuantThreads = 256;
+constexpr int kMaxAmaxGrid = 4096;       // partial slots in the workspace
+constexpr int kMaxSplits = 256;          // N splits per M tile (bounds the workspace)
+constexpr int kMaxKmax = 16;             // largest top-k list
+constexpr int kMaxDevices = 64;
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
+// link-time dependency on libcuda).
+typedef CUresult (*TensorMapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                      const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                      const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                      CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+TensorMapEncodeFn tensor_map_encoder();
+
+// Number of SMs of the current device (cached per device); 0 on error.
+int device_sm_count();
+
+struct GemmPlan {
+  int m_tiles = 0, n_tiles = 0, n_splits = 1;
+};
+GemmPlan plan_gemm(int64_t T, int64_t N, int num_sms);
+
+// Decode (single-launch) path limits and plan.
+struct DecodePlan {
+  bool ok = false;
+  int tmax = 0;        // template bucket >= T
+  int epc = 0;         // experts per CTA
+  int grid = 0;
+  size_t smem = 0;
+};
+DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms);
+
+// Byte offsets inside the caller's workspace.
+struct WsLayout {
+  size_t control = 0;        // 256 bytes: status word and tickets
+  size_t amax_partials = 0;  // kMaxAmaxGrid x u32
+  size_t scalars = 0;        // x gsa, x amax (router path) -- 256 bytes
+  size_t tickets = 0;        // m_tiles x u32
+  size_t x_codes = 0;        // [rows_pad, D/2]
+  size_t x_sf = 0;           // tile layout, rows_pad rows
+  size_t partials = 0;       // m_tiles x n_splits x 128 x kMaxKmax x float4
+  size_t decode = 0;         // decode scratch: keys and scores [T, N] fp32
+  size_t total = 0;
+};
+WsLayout router_ws_layout(int64_t T, int64_t D, int64_t N);
+WsLayout quantize_ws_layout(int64_t rows, int64_t D);
+
+// ----------------------------------------------------------------- launchers
+cudaError_t launch_amax(const void* x, bool bf16, int64_t n_elems, uint32_t* partials,
+                        uint32_t* ticket, float* gsa_out, float* amax_out, int grid,
+                        cudaStream_t s);
+cudaError_t launch_quantize(const void* x, bool bf16, int64_t rows, int64_t D, bool tiled,
+                            const float* amax, uint8_t* codes, uint8_t* sf, cudaStream_t s);
+int amax_grid(int64_t n_elems, bool bf16, int num_sms);
+
+nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const float* x_gsa,
+                            int64_t T, int64_t D, const uint8_t* W_codes, const uint8_t* W_sf,
+                            const float* w_gsa, int64_t N, const float* bias, int k,
+                            float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
+                            float* logits, float4* partials, uint32_t* tickets, uint32_t* status,
+                            const GemmPlan& g, cudaStream_t s);
+
+cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const uint8_t* W_codes,
+                          const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,
+                          int k, float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
+                          float* logits, float* ws_keys, float* ws_scores, uint32_t* ticket,
+                          const DecodePlan& plan, cudaStream_t s);
+
+}  // namespace nvr

@@ -30,7 +30,7 @@ are closer than the logit tolerance allows to separate; routing weights within
 
 import numpy as np
 
-from .router import sigmoid64, routed_weights
+from .router import sigmoid64, routed_weights, selection_keys
 
 LOGIT_REL = 1e-3
 LOGIT_ABS_FRAC = 2.0 ** -15
@@ -133,3 +133,39 @@ def check_topk(gpu_ids, gpu_w, L64, bound64, keys32, bias=None, routed_scaling=1
 def topk_ok(res):
     """True when a ``check_topk`` result has no failures."""
     return all(v == 0 for kk, v in res.items() if kk != "exempt_rows")
+
+
+def check_topk_candidates(gpu_ids, gpu_w, cand_ids, cand_L, cand_B, rest_max, raw=True,
+                          bias=None, routed_scaling=1.0):
+    """``check_topk`` for a head too wide to keep every logit: the oracle keeps,
+    per row, its best candidates (ids, float64 logits, bounds) and the largest
+    key - slack over all other outputs (``rest_max``).  A GPU id outside the
+    candidates counts as a set failure."""
+    gpu_ids = np.asarray(gpu_ids, dtype=np.int64)
+    T, k = gpu_ids.shape
+    res = {"bad_range": 0, "bad_dup": 0, "bad_order": 0, "bad_set": 0, "bad_tie": 0,
+           "bad_weight": 0, "exempt_rows": 0}
+    for t in range(T):
+        cid = np.asarray(cand_ids[t], dtype=np.int64)
+        pos = {int(c): i for i, c in enumerate(cid)}
+        g = gpu_ids[t]
+        if len(set(g.tolist())) != k:
+            res["bad_dup"] += 1
+            continue
+        if any(int(e) not in pos for e in g):
+            res["bad_set"] += 1
+            continue
+        idx = np.array([pos[int(e)] for e in g])
+        L = np.asarray(cand_L[t], np.float64)[None, :]
+        B = np.asarray(cand_B[t], np.float64)[None, :]
+        keys = selection_keys(L, bias, raw)
+        # the candidate list plus one stand-in for everything else
+        sub = check_topk(idx[None, :], np.asarray(gpu_w[t:t + 1]), L, B, keys, bias,
+                         routed_scaling, raw)
+        tau = key_slack(L, B, keys, bias, raw)[0]
+        hi = keys[0][idx].astype(np.float64) + tau[idx]
+        if rest_max[t] > hi.min():
+            sub["bad_set"] += 1
+        for kk in res:
+            res[kk] += sub[kk]
+    return res

@@ -1,0 +1,133 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every
+symbol include/*.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+
+import ctypes
+import glob
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib():
+    from nvfp4_router_gate_gb300 import _native, build
+    if not os.path.exists(_native.LIB_PATH):
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("library not built and no nvcc")
+        build.build()
+    return _native
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\**\s+\**([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    nat = _lib()
+    names = _declared_functions()
+    assert len(names) >= 9
+    L = nat.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(nat.SIGNATURES)
+
+
+def test_status_strings_and_sizes():
+    nat = _lib()
+    L = nat.lib()
+    for code in range(7):
+        assert L.nvr_status_string(code)
+    assert L.nvr_sf_bytes(4, 256, nat.NVR_SF_LINEAR) == 64
+    assert L.nvr_sf_bytes(4, 256, nat.NVR_SF_TILED) == 128 * 16
+    assert L.nvr_sf_bytes(130, 7168, nat.NVR_SF_TILED) == 256 * 448
+    assert L.nvr_sf_bytes(4, 100, nat.NVR_SF_LINEAR) == 0          # D % 64 != 0
+    # the workspace bound is monotone in T_max
+    prev = 0
+    for T in [1, 2, 16, 17, 128, 129, 4096, 16384]:
+        v = L.router_gate_workspace_size(T, 7168, 256, 8)
+        assert v >= prev
+        prev = v
+
+
+def test_host_argument_checks_without_gpu():
+    nat = _lib()
+    L = nat.lib()
+    fake = ctypes.c_void_p(0x10000)          # aligned, never dereferenced
+    odd = ctypes.c_void_p(0x10008)           # 8-byte aligned only
+    ws_n = L.router_gate_workspace_size(4, 256, 16, 2)
+    # null activations
+    st = L.router_gate_topk(None, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    # D not a multiple of 64
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 200, fake, fake, fake, 16, None, 2, 1.0, 0,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    # k out of range
+    for k in (0, 17, 32):
+        st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, k, 1.0, 0,
+                                fake, fake, fake, ws_n, None)
+        assert st == nat.NVR_ERR_INVALID_ARG
+    # k > N
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 4, None, 8, 1.0, 0,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    # bad dtype, bad flags, conflicting flags
+    st = L.router_gate_topk(fake, 7, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 64,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0,
+                            nat.NVR_FLAG_FORCE_DECODE | nat.NVR_FLAG_FORCE_TENSOR_CORE,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    # misaligned activations / workspace
+    st = L.router_gate_topk(odd, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_ALIGNMENT
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
+                            fake, fake, odd, ws_n, None)
+    assert st == nat.NVR_ERR_ALIGNMENT
+    # workspace too small
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
+                            fake, fake, fake, 16, None)
+    assert st == nat.NVR_ERR_WORKSPACE
+    # empty batch: valid, launches nothing
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 0, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_OK
+    # quantize: bad layout, small workspace, empty
+    qn = L.nvfp4_quantize_workspace_size(4, 256)
+    assert L.nvfp4_quantize_act(fake, nat.NVR_F32, 4, 256, fake, fake, 5, fake, fake, qn, None) == \
+        nat.NVR_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_act(fake, nat.NVR_F32, 4, 256, fake, fake, 0, fake, fake, 8, None) == \
+        nat.NVR_ERR_WORKSPACE
+    assert L.nvfp4_quantize_act(fake, nat.NVR_F32, 0, 256, fake, fake, 0, fake, fake, qn, None) == \
+        nat.NVR_OK
+    assert L.nvfp4_pack_weight(None, nat.NVR_F32, 4, 256, fake, fake, fake, fake, qn, None) == \
+        nat.NVR_ERR_INVALID_ARG
+    # logits hook rejects the raw flag
+    assert L.router_gate_logits(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, nat.NVR_FLAG_RAW_LOGITS,
+                                fake, fake, ws_n, None) == nat.NVR_ERR_INVALID_ARG
+    assert L.nvr_read_device_status(None, None, None) == nat.NVR_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from nvfp4_router_gate_gb300 import _native
+    monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_native, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _native.lib()

@@ -1,0 +1,227 @@
+"""GPU parity of the gate GEMM and the fused router epilogue against the
+oracle, through the C ABI, on every workload: the tiny router, decode
+(T = 1, 8, 64), prefill (T = 4096), the adversarial large batch (T = 16384,
+E = 384) and the wide-N raw head (N = 129280, k = 1 and 8), plus ragged
+shapes, both kernels (single-launch decode and tensor-core), exact integer
+logits, determinism, CUDA-graph replay and workspace reuse."""
+
+import os
+import sys
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+import workloads as WL  # noqa: E402
+from oracle import formats, quantize as Q, gemm, router, compare  # noqa: E402
+from gpu_util import Case, to_device, as_f32  # noqa: E402
+
+sys.path.insert(0, os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden"))
+
+TC = 2       # NVR_FLAG_FORCE_TENSOR_CORE
+DEC = 4      # NVR_FLAG_FORCE_DECODE
+
+
+def _logits(case, flags):
+    import nvfp4_router_gate_gb300 as R
+    out = R.router_gate_logits(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, flags=flags)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,T,flags", [("tiny", 4, DEC), ("tiny", 4, TC), ("decode", 8, DEC),
+                                          ("decode", 8, TC), ("prefill", 300, TC),
+                                          ("adversarial", 40, TC)])
+def test_logits_within_tolerance(name, T, flags):
+    case = Case(WL.WORKLOADS[name].with_T(T))
+    g = _logits(case, flags)
+    L, B = case.oracle_rows(np.arange(T))
+    assert compare.check_logits(g, L, B) == 0
+    # much tighter than the contract in practice: report the worst relative error
+    rel = np.abs(g - L) / (compare.LOGIT_ABS_FRAC * B + np.abs(L) + 1e-30)
+    assert rel.max() < 1e-4
+
+
+def _grid_operands(rng, rows, D, amax_block):
+    """Inputs whose NVFP4 quantization is exact: gsa = 1 (one element 2688 =
+    6 * 448 alone in block `amax_block` of row 0) and block scales 2**b,
+    b in [-1, 1], with a +-6 leading every other block."""
+    vals = formats.decode_e2m1(rng.integers(0, 16, (rows, D)))
+    vals[:, ::16] = 6.0 * rng.choice([-1, 1], (rows, D // 16))
+    b = rng.integers(-1, 2, (rows, D // 16))
+    x = vals * np.repeat(2.0 ** b, 16, axis=1)
+    x[0, 16 * amax_block:16 * (amax_block + 1)] = 0.0
+    x[0, 16 * amax_block] = 2688.0
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("flags", [DEC, TC])
+def test_exact_integer_logits(flags):
+    """Grid-valued operands: products are multiples of 1/16 and every partial
+    sum stays below 2**20 in magnitude, so any fp32 summation order is exact
+    and the GPU logits must equal the oracle's bits."""
+    import nvfp4_router_gate_gb300 as R
+    rng = np.random.default_rng(21)
+    T, N, D = 8, 136, 512
+    x = _grid_operands(rng, T, D, 0)
+    W = _grid_operands(rng, N, D, 1)      # the two 2688s never meet in one product
+    xd, Wd = to_device(x, "f32"), to_device(W, "f32")
+    wf, ws, wg = R.nvfp4_pack_weight(Wd)
+    out = R.router_gate_logits(xd, wf, ws, wg, flags=flags)
+    torch.cuda.synchronize()
+    xq, xs, xg = Q.quantize(x)
+    wq, wsb, wgg = Q.quantize(W)
+    assert xg == 1.0 and wgg == 1.0
+    L, _ = gemm.logits(xq, xs, xg, wq, wsb, wgg)
+    assert np.array_equal(out.cpu().numpy().astype(np.float64), L)
+
+
+@pytest.mark.parametrize("flags", [DEC, TC])
+def test_tiny_router(flags):
+    case = Case(WL.WORKLOADS["tiny"])
+    ids, w = case.run(flags)
+    res = case.check(ids, w, np.arange(case.w.T))
+    assert compare.topk_ok(res) and res["exempt_rows"] == 0, res
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_decode_router(T):
+    case = Case(WL.WORKLOADS["decode"].with_T(T))
+    ids, w = case.run()
+    res = case.check(ids, w, np.arange(T))
+    assert compare.topk_ok(res), res
+    if T <= 8:
+        ids2, w2 = case.run(TC)                      # the other kernel agrees too
+        res2 = case.check(ids2, w2, np.arange(T))
+        assert compare.topk_ok(res2), res2
+
+
+def test_prefill_router_sampled_rows():
+    case = Case(WL.WORKLOADS["prefill"])
+    ids, w = case.run()
+    rows = np.unique(np.concatenate([np.arange(0, 4096, 37), np.arange(4090, 4096), [127, 128, 129]]))
+    res = case.check(ids, w, rows)
+    assert compare.topk_ok(res), res
+
+
+@pytest.mark.parametrize("T", [129, 300])
+def test_ragged_batches_all_rows(T):
+    case = Case(WL.WORKLOADS["prefill"].with_T(T))
+    ids, w = case.run()
+    res = case.check(ids, w, np.arange(T))
+    assert compare.topk_ok(res), res
+
+
+def test_adversarial_router():
+    case = Case(WL.WORKLOADS["adversarial"])
+    ids, w = case.run()
+    rows = np.unique(np.concatenate([np.arange(0, 16384, 61), np.arange(16376, 16384),
+                                     np.arange(0, 64)]))
+    res = case.check(ids, w, rows)
+    assert compare.topk_ok(res), res
+    # all-zero rows (t % 4 == 1): every logit is exactly 0, so the ids are 0..7
+    # and each weight is routed_scaling / 8
+    zero = np.arange(1, 16384, 4)
+    assert np.all(ids[zero] == np.arange(8))
+    assert np.allclose(w[zero], 2.5 / 8, atol=1e-6)
+    # 1e4 rows saturate the sigmoid: weights are 2.5/8 up to 1e-5
+    big = np.arange(2, 16384, 4)
+    assert np.all(np.abs(w[big].sum(axis=1) - 2.5) < 1e-4)
+
+
+def test_adversarial_tie_probe():
+    """Experts 2j+1 duplicate 2j: exact ties in every row must keep the lower id first."""
+    case = Case(WL.Workload("tie_probe", 256, 7168, 384, 8, 2.5, False, "bf16", "adversarial", 0.02,
+                            "zero", tie_probe=True))
+    ids, w = case.run()
+    res = case.check(ids, w, np.arange(256))
+    assert compare.topk_ok(res), res
+    for row in ids:
+        pos = {int(e): i for i, e in enumerate(row)}
+        for e, i in pos.items():
+            if e < 16 and e % 2 == 1 and (e - 1) in pos:
+                assert pos[e - 1] < i                # the even copy comes first
+
+
+GOLDEN_WIDE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "wide_n_expected.npz")
+
+
+@pytest.mark.parametrize("k", [1, 8])
+def test_wide_n_raw_head(k):
+    """All 32 tokens of the N = 129280 raw head against the oracle's stored
+    answer (tests/golden/make_wide_n_expected.py: quantizing the weight on the
+    CPU takes minutes)."""
+    if not os.path.exists(GOLDEN_WIDE):
+        pytest.skip("tests/golden/wide_n_expected.npz not generated")
+    gold = np.load(GOLDEN_WIDE)
+    w = WL.WORKLOADS["wide_n"].with_k(k)
+    case = Case(w, with_oracle_w=False)
+    import make_wide_n_expected as gen
+    if gen.input_digest(w) != str(gold["digest"]):
+        pytest.fail("the seeded generator no longer reproduces the stored inputs")
+    assert case.w_gsa.item() == float(gold["w_gsa"])
+    ids, wts = case.run()
+    res = compare.check_topk_candidates(ids, wts, gold["ids"], gold["logits"], gold["bounds"],
+                                        gold["rest_max"], raw=True)
+    assert compare.topk_ok(res), res
+
+
+def test_determinism_and_graph_replay():
+    import nvfp4_router_gate_gb300 as R
+    for T in (1, 300):
+        w = WL.WORKLOADS["decode"].with_T(T) if T == 1 else WL.WORKLOADS["prefill"].with_T(T)
+        gate = R.RouterGate(to_device(WL.make_w(w), w.dtype), torch.from_numpy(WL.make_bias(w)).cuda(),
+                            k=8, routed_scaling=2.5, max_tokens=T)
+        x = to_device(WL.make_x(w), w.dtype)
+        ids0, w0 = [t.clone() for t in gate(x)]
+        ids1, w1 = [t.clone() for t in gate(x)]
+        assert torch.equal(ids0, ids1) and torch.equal(w0, w1)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            gate(x)                                  # warm up on the capture stream
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            gate(x)
+        gate.ids.zero_()
+        for _ in range(20):
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(gate.ids[:T], ids0) and torch.equal(gate.weights[:T], w0)
+        assert R.nvr_read_device_status(gate.workspace) == 0
+
+
+def test_workspace_reuse_across_shapes():
+    import nvfp4_router_gate_gb300 as R
+    w = WL.WORKLOADS["prefill"]
+    case = Case(w.with_T(600))
+    ws = R.new_workspace(R.router_gate_workspace_size(600, 7168, 256, 8))
+    for T in (600, 1, 9, 128, 600, 16):
+        x = case.x_dev[:T].contiguous()
+        ids, wt = R.router_gate_topk(x, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5,
+                                     workspace=ws)
+        torch.cuda.synchronize()
+        sub = Case.__new__(Case)
+        sub.__dict__.update(case.__dict__)
+        sub.x32 = case.x32[:T]
+        sub.w = w.with_T(T)
+        res = sub.check(ids.cpu().numpy(), wt.cpu().numpy(), np.arange(T))
+        assert compare.topk_ok(res), (T, res)
+    assert R.nvr_read_device_status(ws) == 0
+
+
+def test_gpu_argument_errors():
+    import nvfp4_router_gate_gb300 as R
+    case = Case(WL.WORKLOADS["tiny"])
+    with pytest.raises(R.RouterError):
+        R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, None, k=17)
+    # the wide head needs the tensor-core path: forcing the decode kernel is refused
+    big = torch.zeros((32, 7168), dtype=torch.bfloat16, device="cuda")
+    wf = torch.zeros((20000, 3584), dtype=torch.uint8, device="cuda")
+    wsf = torch.zeros(R.nvr_sf_bytes(20000, 7168, "tiled"), dtype=torch.uint8, device="cuda")
+    with pytest.raises(R.RouterError, match="unsupported"):
+        R.router_gate_topk(big, wf, wsf, case.w_gsa, None, k=1, flags=DEC)
