@@ -131,6 +131,23 @@ def oracle_tokens_per_s(w, x32_all, packed_w, bias, budget_s=12.0, rows_per_call
     return done / el, done, el
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(v, world, device):
+    """The largest value of `v` over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, steps, max_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def kernel_names(path):
@@ -219,13 +236,9 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
+    value = job_throughput(world, T, args.steps, ms)
 
     # per-kernel pass (events between the launches)
     names = kernel_names("tc")
@@ -291,12 +304,8 @@ def run_gpu(args, rank, world, local_rank):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * T * n_e2e / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": job_throughput(world, T, n_e2e, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": int(x_host.numel() * 2),
            "d2h_bytes_per_step": int(ids_host.numel() * 4 + w_host.numel() * 4), "steps": n_e2e}
 

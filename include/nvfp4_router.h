@@ -98,7 +98,13 @@ enum {
    * results within the same tolerances; they are not bit-identical (the
    * fp32 accumulation order of the logits differs). */
   NVR_FLAG_FORCE_TENSOR_CORE = 2u,
-  NVR_FLAG_FORCE_DECODE = 4u
+  NVR_FLAG_FORCE_DECODE = 4u,
+  /* Failure-detection test hook (with FORCE_TENSOR_CORE only): the tensor-core
+   * kernel's MMA issuer issues nothing, so its bounded waits run out after
+   * about one second; the kernel stores NVR_ERR_TIMEOUT in the workspace
+   * status word, releases its tensor memory and returns.  The call itself
+   * returns NVR_OK (the failure is on the device); outputs are unspecified. */
+  NVR_FLAG_TEST_STALL = 1u << 30
 };
 
 /* Human-readable name of a status code (static string, never NULL). */

@@ -26,6 +26,7 @@ NVR_SF_TILED = 1
 NVR_FLAG_RAW_LOGITS = 1
 NVR_FLAG_FORCE_TENSOR_CORE = 2
 NVR_FLAG_FORCE_DECODE = 4
+NVR_FLAG_TEST_STALL = 1 << 30
 
 _p = ctypes.c_void_p
 _i64 = ctypes.c_int64

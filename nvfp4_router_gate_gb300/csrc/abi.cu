@@ -152,9 +152,11 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   if (st != NVR_OK) return st;
   if (!W_fp4 || !W_sf || !w_gsa || N <= 0 || N > (1 << 28)) return NVR_ERR_INVALID_ARG;
   if (!logits && (!out_ids || !out_w || k < 1 || k > kMaxKmax || k > N)) return NVR_ERR_INVALID_ARG;
-  if (flags & ~static_cast<uint32_t>(NVR_FLAG_RAW_LOGITS | NVR_FLAG_FORCE_TENSOR_CORE | NVR_FLAG_FORCE_DECODE))
+  if (flags & ~static_cast<uint32_t>(NVR_FLAG_RAW_LOGITS | NVR_FLAG_FORCE_TENSOR_CORE | NVR_FLAG_FORCE_DECODE |
+                                     NVR_FLAG_TEST_STALL))
     return NVR_ERR_INVALID_ARG;
   if ((flags & NVR_FLAG_FORCE_TENSOR_CORE) && (flags & NVR_FLAG_FORCE_DECODE)) return NVR_ERR_INVALID_ARG;
+  if ((flags & NVR_FLAG_TEST_STALL) && !(flags & NVR_FLAG_FORCE_TENSOR_CORE)) return NVR_ERR_INVALID_ARG;
   if (!aligned16(W_fp4) || !aligned16(W_sf) || (reinterpret_cast<uintptr_t>(w_gsa) & 3u) ||
       (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
       (out_ids && (reinterpret_cast<uintptr_t>(out_ids) & 3u)) ||
@@ -207,7 +209,8 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   st = launch_gemm_topk(xc, xsf, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
                         out_ids, out_w, logits, reinterpret_cast<float4*>(w + L.partials),
                         reinterpret_cast<uint32_t*>(w + L.tickets),
-                        reinterpret_cast<uint32_t*>(w + kWsStatus), g, s);
+                        reinterpret_cast<uint32_t*>(w + kWsStatus), g,
+                        (flags & NVR_FLAG_TEST_STALL) != 0, s);
   prof.after();
   return st;
 }
@@ -289,7 +292,7 @@ nvr_status router_gate_logits(const void* x, nvr_dtype dt, int64_t T, int64_t D,
                               const uint8_t* W_scales, const float* w_gsa, int64_t N, uint32_t flags,
                               float* logits, void* workspace, size_t ws_bytes, nvr_stream_t stream) {
   if (!logits) return NVR_ERR_INVALID_ARG;
-  if (flags & NVR_FLAG_RAW_LOGITS) return NVR_ERR_INVALID_ARG;
+  if (flags & (NVR_FLAG_RAW_LOGITS | NVR_FLAG_TEST_STALL)) return NVR_ERR_INVALID_ARG;
   return router_impl(x, dt, T, D, W_fp4, W_scales, w_gsa, N, nullptr, 1, 1.0f, flags, nullptr, nullptr,
                      logits, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -65,6 +65,7 @@ struct GemmParams {
   float4* partials;            // [m_tiles * n_splits][128][KMAX]
   uint32_t* tickets;           // [m_tiles]
   uint32_t* status;
+  int test_stall;              // test hook: the MMA issuer issues nothing
 };
 
 template <int KMAX>
@@ -101,6 +102,7 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* last_flag = abort_flag + 1;
+  volatile int* epi_abort = abort_flag + 2;     // the epilogue's agreed view of abort_flag
 
   // producer thread: which ring stages were filled, and the parity of each
   // stage's latest fill (bit s)
@@ -117,6 +119,7 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
     for (int b = 0; b < 2; ++b) { mbar_init(acc_full + b, 1); mbar_init(acc_empty + b, 128); }
     *abort_flag = 0;
     *last_flag = 0;
+    *epi_abort = 0;
     fence_mbar_init();
     tma_prefetch_map(&p.tmap_a);
     tma_prefetch_map(&p.tmap_b);
@@ -162,7 +165,7 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && !p.test_stall) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -215,7 +218,9 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
       const int j = split + it * p.n_splits;
       const int buf = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(acc_full + buf, acc_phase, deadline, abort_flag)) { ok = false; break; }
+      // all lanes of a warp take the same branch (tcgen05.ld is warp-wide)
+      const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full + buf, acc_phase, deadline, abort_flag));
+      if (!got) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -251,7 +256,14 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
     if (!ok) {
       report_timeout(p.status);
       *abort_flag = 1;
-    } else if (!p.logits) {
+    }
+    // Agree on one abort decision before the named barriers below: every
+    // epilogue thread has left its loop (bounded waits) and published its
+    // failure; one thread snapshots the flag for all.
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (threadIdx.x == 64) *epi_abort = *abort_flag;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (!*epi_abort && !p.logits) {
       if (p.n_splits == 1) {
         if (active) write_final<KMAX>(tk, p, token);
       } else {
@@ -363,7 +375,7 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
                             const float* w_gsa, int64_t N, const float* bias, int k,
                             float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                             float* logits, float4* partials, uint32_t* tickets, uint32_t* status,
-                            const GemmPlan& g, cudaStream_t s) {
+                            const GemmPlan& g, bool test_stall, cudaStream_t s) {
   GemmParams p;
   if (!encode_codes_map(&p.tmap_a, x_codes, T, D)) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes_map(&p.tmap_b, W_codes, N, D)) return NVR_ERR_UNSUPPORTED;
@@ -373,6 +385,7 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
   p.routed_scaling = routed_scaling;
   p.out_ids = out_ids; p.out_w = out_w; p.logits = logits;
   p.partials = partials; p.tickets = tickets; p.status = status;
+  p.test_stall = test_stall ? 1 : 0;
   const int grid = g.m_tiles * g.n_splits;
   cudaError_t e;
   if (k <= 1) e = launch_k<1>(p, grid, s);

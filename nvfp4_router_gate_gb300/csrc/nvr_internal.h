@@ -73,7 +73,7 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
                             const float* w_gsa, int64_t N, const float* bias, int k,
                             float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                             float* logits, float4* partials, uint32_t* tickets, uint32_t* status,
-                            const GemmPlan& g, cudaStream_t s);
+                            const GemmPlan& g, bool test_stall, cudaStream_t s);
 
 cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const uint8_t* W_codes,
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,

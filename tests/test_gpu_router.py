@@ -225,3 +225,26 @@ def test_gpu_argument_errors():
     wsf = torch.zeros(R.nvr_sf_bytes(20000, 7168, "tiled"), dtype=torch.uint8, device="cuda")
     with pytest.raises(R.RouterError, match="unsupported"):
         R.router_gate_topk(big, wf, wsf, case.w_gsa, None, k=1, flags=DEC)
+
+
+def test_bounded_wait_timeout_reports_status():
+    """Failure detection without a GPU fault: with the test stall hook the
+    tensor-core kernel's MMA issuer issues nothing, its pipeline waits run out
+    after about a second, the kernel records NVR_ERR_TIMEOUT in the workspace
+    status word and returns.  The context stays usable: after re-zeroing the
+    workspace the next call routes correctly."""
+    import nvfp4_router_gate_gb300 as R
+    from nvfp4_router_gate_gb300 import _native
+    case = Case(WL.WORKLOADS["decode"].with_T(8))
+    ws = R.new_workspace(R.router_gate_workspace_size(8, 7168, 256, 8))
+    R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5,
+                       workspace=ws, flags=TC | _native.NVR_FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert R.nvr_read_device_status(ws) == _native.NVR_ERR_TIMEOUT
+    ws.zero_()
+    ids, w = R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5,
+                                workspace=ws, flags=TC)
+    torch.cuda.synchronize()
+    assert R.nvr_read_device_status(ws) == 0
+    res = case.check(ids.cpu().numpy(), w.cpu().numpy(), np.arange(8))
+    assert compare.topk_ok(res), res
