@@ -203,6 +203,35 @@ nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
                             void* workspace, size_t ws_bytes, nvr_stream_t stream);
 
 /*
+ * router_gate_topk_noalloc -- router_gate_topk for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry
+ * point; it exists for code whose host owns every device allocation (a plugin
+ * handed only its input and output buffers) or that must not call an
+ * allocator on its path, and so cannot pass a workspace.
+ *
+ * Same arguments and results as router_gate_topk, without the workspace.
+ * It runs the single-launch decode kernel only (T <= 16 and a shape whose
+ * per-CTA plan fits; otherwise NVR_ERR_UNSUPPORTED); flags may be 0 or
+ * NVR_FLAG_RAW_LOGITS.  Its scratch (keys and scores of every (token, expert)
+ * pair plus a ticket) lives in a fixed 1 MiB array in the library's device
+ * memory, held by every GPU that loads the library until the process exits;
+ * calls with T * N * 8 bytes > 1 MiB - 256 are rejected with
+ * NVR_ERR_WORKSPACE.  It calls no cudaMalloc/cudaFree; it clears the ticket
+ * with cudaMemsetAsync on `stream` before its launch.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture.
+ * - Every call shares the one array: calls whose kernels overlap on the GPU
+ *   (different streams without ordering between them) race and give wrong
+ *   results.  Order them on one stream.
+ */
+nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int64_t T, int64_t D,
+                                    const uint8_t* W_fp4, const uint8_t* W_scales,
+                                    const float* w_gsa, int64_t N, const float* bias, int k,
+                                    float routed_scaling, uint32_t flags, int32_t* out_ids,
+                                    float* out_w, nvr_stream_t stream);
+
+/*
  * router_gate_logits -- test hook: the same quantization and gate GEMM as
  * router_gate_topk, writing the fp32 logits [T, N] (row-major,
  * logit = acc * gsa_x * gsa_w) instead of the epilogue's outputs.  Used to
