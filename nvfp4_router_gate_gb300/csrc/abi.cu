@@ -36,7 +36,7 @@ int device_sm_count() {
 
 int amax_grid(int64_t n_elems, bool bf16, int num_sms) {
   const int64_t nvec = n_elems * (bf16 ? 2 : 4) / 16;
-  int64_t want = (nvec + kAmaxThreads * 4 - 1) / (kAmaxThreads * 4);   // >= 4 vectors per thread
+  int64_t want = (nvec + kAmaxThreads * 8 - 1) / (kAmaxThreads * 8);   // >= 8 vectors per thread
   int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 4;
   if (cap > kMaxAmaxGrid) cap = kMaxAmaxGrid;
   if (want > cap) want = cap;
@@ -125,21 +125,22 @@ nvr_status quantize_impl(const void* x, nvr_dtype dt, int64_t rows, int64_t D, u
   if (!aligned16(codes) || !aligned16(sf) || (reinterpret_cast<uintptr_t>(gsa) & 3u)) return NVR_ERR_ALIGNMENT;
   const WsLayout L = quantize_ws_layout(rows, D);
   if (ws_bytes < L.total) return NVR_ERR_WORKSPACE;
+  if ((rows + 127) / 128 * 128 * (D / 32) >= (int64_t(1) << 31)) return NVR_ERR_UNSUPPORTED;   // 32-bit indexing
   if (rows == 0) return NVR_OK;
   const int sms = device_sm_count();
   if (sms <= 0) return NVR_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const bool bf16 = dt == NVR_BF16;
-  float* amax = reinterpret_cast<float*>(w + L.scalars + 4);
+  float* qrec = reinterpret_cast<float*>(w + L.scalars + 16);    // {gsa, 1/gsa, mode, amax}
   ProfileScope prof(s);
   prof.before();
   cudaError_t e = launch_amax(x, bf16, rows * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
-                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), gsa, amax,
+                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), gsa, qrec,
                               amax_grid(rows * D, bf16, sms), s);
   prof.after();
   if (e != cudaSuccess) return NVR_ERR_CUDA;
   prof.before();
-  e = launch_quantize(x, bf16, rows, D, layout == NVR_SF_TILED, amax, codes, sf, s);
+  e = launch_quantize(x, bf16, rows, D, layout == NVR_SF_TILED, qrec, codes, sf, s);
   prof.after();
   return e == cudaSuccess ? NVR_OK : NVR_ERR_CUDA;
 }
@@ -165,6 +166,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     return NVR_ERR_ALIGNMENT;
   const WsLayout L = router_ws_layout(T, D, N);
   if (ws_bytes < L.total) return NVR_ERR_WORKSPACE;
+  if ((T + 127) / 128 * 128 * (D / 32) >= (int64_t(1) << 31)) return NVR_ERR_UNSUPPORTED;      // 32-bit indexing
   if (T == 0) return NVR_OK;
   const int sms = device_sm_count();
   if (sms <= 0) return NVR_ERR_CUDA;
@@ -173,7 +175,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   const bool raw = (flags & NVR_FLAG_RAW_LOGITS) != 0;
   if (logits) k = 1;
 
-  const DecodePlan dp = plan_decode(T, D, N, sms);
+  const DecodePlan dp = plan_decode(T, D, N, sms, bf16);
   const bool use_decode = (flags & NVR_FLAG_FORCE_DECODE) ? true
                           : (flags & NVR_FLAG_FORCE_TENSOR_CORE) ? false
                           : dp.ok;
@@ -190,18 +192,18 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     return e == cudaSuccess ? NVR_OK : NVR_ERR_CUDA;
   }
   float* x_gsa = reinterpret_cast<float*>(w + L.scalars);
-  float* amax = x_gsa + 1;
+  float* qrec = x_gsa + 4;                                        // {gsa, 1/gsa, mode, amax}
   uint8_t* xc = w + L.x_codes;
   uint8_t* xsf = w + L.x_sf;
   ProfileScope prof(s);
   prof.before();
   cudaError_t e = launch_amax(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
-                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, amax,
+                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec,
                               amax_grid(T * D, bf16, sms), s);
   prof.after();
   if (e != cudaSuccess) return NVR_ERR_CUDA;
   prof.before();
-  e = launch_quantize(x, bf16, T, D, true, amax, xc, xsf, s);
+  e = launch_quantize(x, bf16, T, D, true, qrec, xc, xsf, s);
   prof.after();
   if (e != cudaSuccess) return NVR_ERR_CUDA;
   const GemmPlan g = plan_gemm(T, N, sms);

@@ -26,6 +26,7 @@ namespace nvr {
 
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
+constexpr int kDecodeMaxSmem = 200 * 1024;
 
 struct DecodeParams {
   const void* x;
@@ -61,34 +62,78 @@ __device__ __forceinline__ uint32_t e2m1x4_to_s8x4(uint32_t c16) {
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline size_t decode_smem_bytes(int T, int D, int N, int tmax) {
+constexpr int kMaxBlocksPerThread = 16;   // W blocks a thread prefetches into registers
+constexpr int kMaxT = 16;                 // tokens of one decode call
+
+// Shared memory of one CTA: the raw activations (reused for the last CTA's
+// keys and scores), their signed 2*e2m1 bytes, their block scales and the
+// cross-warp partial sums.
+struct DecodeSmem {
+  size_t raw, xv, xs, red, total;
+};
+__host__ __device__ inline DecodeSmem decode_smem_layout(int T, int D, int N, int elt) {
   const int KB = D / kBlock;
-  return align_up(static_cast<size_t>(T) * D, 16) + static_cast<size_t>(T) * KB * 4 +
-         static_cast<size_t>(kDecodeWarps) * tmax * 4 + static_cast<size_t>(tmax) * 8 * 4 +
-         static_cast<size_t>(N) * 8 + 16 * 4 + 16;
+  DecodeSmem L;
+  L.raw = 0;
+  const size_t raw_bytes = static_cast<size_t>(T) * D * elt;
+  const size_t kv_bytes = static_cast<size_t>(T) * N * 8;
+  L.xv = align_up(raw_bytes > kv_bytes ? raw_bytes : kv_bytes, 16);
+  L.xs = align_up(L.xv + static_cast<size_t>(T) * D, 16);
+  L.red = align_up(L.xs + static_cast<size_t>(T) * KB * 4, 16);
+  L.total = L.red + static_cast<size_t>(kDecodeWarps) * kMaxT * 4;
+  return L;
 }
 
-template <bool kBF16, int TMAX>
-__global__ void __launch_bounds__(kDecodeThreads)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(gmem_src)) : "memory");
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_router_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int T = p.T, D = p.D, N = p.N, KB = D / kBlock;
-  int8_t* xv = reinterpret_cast<int8_t*>(sm);
-  float* xs = reinterpret_cast<float*>(sm + align_up(static_cast<size_t>(T) * D, 16));
-  float* red = xs + T * KB;                       // [warps][TMAX]
-  float* kbuf = red + kDecodeWarps * TMAX + TMAX * 8;
-  float* sbuf = kbuf + N;
-  int* sel = reinterpret_cast<int*>(sbuf + N);    // [16]
+  const DecodeSmem L = decode_smem_layout(T, D, N, kBF16 ? 2 : 4);
+  uint8_t* xraw = sm + L.raw;
+  int8_t* xv = reinterpret_cast<int8_t*>(sm + L.xv);
+  float* xs = reinterpret_cast<float*>(sm + L.xs);
+  float* red = reinterpret_cast<float*>(sm + L.red);          // [warps][kMaxT]
   __shared__ uint32_t s_red[kDecodeWarps];
   __shared__ int s_last;
+  __shared__ int s_sel[kMaxT * 16];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gs = kDecodeThreads / p.epc;                       // threads per expert
+  const int grp = tid / gs, j = tid - grp * gs;
+  const int e = blockIdx.x * p.epc + grp;
 
-  // 1. max |x| over the whole batch
+  // 0. Prefetch this thread's weight blocks into registers (independent of x;
+  //    their latency overlaps everything up to the dot products) and stage x
+  //    in shared memory with one burst of asynchronous 16-byte copies.
+  uint2 wc[kMaxBlocksPerThread];
+  uint32_t wsb[kMaxBlocksPerThread];
+#pragma unroll
+  for (int i = 0; i < kMaxBlocksPerThread; ++i) {
+    const int c = j + i * gs;
+    if (e < N && c < KB) {
+      wc[i] = __ldg(reinterpret_cast<const uint2*>(p.W_codes + static_cast<size_t>(e) * (D / 2) + c * 8));
+      wsb[i] = __ldg(p.W_sf + sf_tile_offset(e, c, KB));
+    } else {
+      wc[i] = make_uint2(0, 0);
+      wsb[i] = 0;
+    }
+  }
   const int64_t nvec = static_cast<int64_t>(T) * D * (kBF16 ? 2 : 4) / 16;
-  const uint4* x4 = static_cast<const uint4*>(p.x);
+  for (int64_t v = tid; v < nvec; v += kDecodeThreads)
+    cp_async16(xraw + 16 * v, static_cast<const uint8_t*>(p.x) + 16 * v);
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // 1. max |x| over the whole batch (from shared memory)
+  const uint4* x4 = reinterpret_cast<const uint4*>(xraw);
   uint32_t m = 0;
-  for (int64_t i = tid; i < nvec; i += kDecodeThreads) m = max(m, absmax_bits16B<kBF16>(__ldg(x4 + i)));
+  for (int64_t v = tid; v < nvec; v += kDecodeThreads) m = max(m, absmax_bits16B<kBF16>(x4[v]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if (lane == 0) s_red[warp] = m;
@@ -98,11 +143,12 @@ decode_router_kernel(const DecodeParams p) {
   for (int w = 0; w < kDecodeWarps; ++w) mb = max(mb, s_red[w]);
   const QuantScale qs = make_quant_scale(__uint_as_float(mb));
 
-  // 2. quantize x into shared memory
+  // 2. quantize x (shared -> shared) with the block quantizer shared with the
+  //    quantize kernel: identical codes and scales
   for (int b = tid; b < T * KB; b += kDecodeThreads) {
     const int t = b / KB, c = b - t * KB;
     Block16 blk;
-    load_block16<kBF16>(p.x, static_cast<size_t>(t) * D + static_cast<size_t>(c) * kBlock, blk);
+    load_block16_shared<kBF16>(xraw, static_cast<size_t>(t) * D + static_cast<size_t>(c) * kBlock, blk);
     uint32_t lo, hi;
     const uint32_t byte = quant_block16(blk, qs, lo, hi);
     uint4 q;
@@ -115,58 +161,52 @@ decode_router_kernel(const DecodeParams p) {
   }
   __syncthreads();
 
-  // 3. logits of this CTA's experts: a group of 256/epc threads per expert
-  const int gs = kDecodeThreads / p.epc;
-  const int grp = tid / gs, j = tid - grp * gs;
-  const int e = blockIdx.x * p.epc + grp;
-  float acc[TMAX];
+  // 3. logits of this CTA's experts: integer dot products of each 16-element
+  //    block (exact), scaled by the two block scales (exact product), fp32 sum.
+  //    The weight blocks are decoded once; the token loop stays rolled.
+  uint32_t wv[kMaxBlocksPerThread][4];
+  float swv[kMaxBlocksPerThread];
 #pragma unroll
-  for (int t = 0; t < TMAX; ++t) acc[t] = 0.0f;
-  if (e < N) {
-    const uint8_t* wrow = p.W_codes + static_cast<size_t>(e) * (D / 2);
-    for (int c = j; c < KB; c += gs) {
-      const uint2 wc = __ldg(reinterpret_cast<const uint2*>(wrow + c * 8));
-      const float sw = e4m3_value(__ldg(p.W_sf + sf_tile_offset(e, c, KB)));
-      const int w0 = static_cast<int>(e2m1x4_to_s8x4(wc.x & 0xFFFFu));
-      const int w1 = static_cast<int>(e2m1x4_to_s8x4(wc.x >> 16));
-      const int w2 = static_cast<int>(e2m1x4_to_s8x4(wc.y & 0xFFFFu));
-      const int w3 = static_cast<int>(e2m1x4_to_s8x4(wc.y >> 16));
+  for (int i = 0; i < kMaxBlocksPerThread; ++i) {
+    swv[i] = e4m3_value(wsb[i]);
+    wv[i][0] = e2m1x4_to_s8x4(wc[i].x & 0xFFFFu);
+    wv[i][1] = e2m1x4_to_s8x4(wc[i].x >> 16);
+    wv[i][2] = e2m1x4_to_s8x4(wc[i].y & 0xFFFFu);
+    wv[i][3] = e2m1x4_to_s8x4(wc[i].y >> 16);
+  }
+#pragma unroll 1
+  for (int t = 0; t < T; ++t) {
+    float acc = 0.0f;
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        if (t < T) {
-          const uint4 xq = *reinterpret_cast<const uint4*>(xv + static_cast<size_t>(t) * D + c * kBlock);
-          int s = __dp4a(static_cast<int>(xq.x), w0, 0);
-          s = __dp4a(static_cast<int>(xq.y), w1, s);
-          s = __dp4a(static_cast<int>(xq.z), w2, s);
-          s = __dp4a(static_cast<int>(xq.w), w3, s);
-          // |s| <= 16 * 144 and both scales have 4 significant bits: the
-          // product is exact, only the accumulation rounds
-          acc[t] = __fmaf_rn(static_cast<float>(s), __fmul_rn(xs[t * KB + c], sw), acc[t]);
-        }
+    for (int i = 0; i < kMaxBlocksPerThread; ++i) {
+      const int c = j + i * gs;
+      if (e < N && c < KB) {
+        const uint4 xq = *reinterpret_cast<const uint4*>(xv + static_cast<size_t>(t) * D + c * kBlock);
+        int sdot = __dp4a(static_cast<int>(xq.x), static_cast<int>(wv[i][0]), 0);
+        sdot = __dp4a(static_cast<int>(xq.y), static_cast<int>(wv[i][1]), sdot);
+        sdot = __dp4a(static_cast<int>(xq.z), static_cast<int>(wv[i][2]), sdot);
+        sdot = __dp4a(static_cast<int>(xq.w), static_cast<int>(wv[i][3]), sdot);
+        // |sdot| <= 16 * 144 and both scales have 4 significant bits: the
+        // product is exact, only the accumulation rounds
+        acc = __fmaf_rn(static_cast<float>(sdot), __fmul_rn(xs[t * KB + c], swv[i]), acc);
       }
     }
-  }
 #pragma unroll
-  for (int t = 0; t < TMAX; ++t) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], o);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) red[warp * TMAX + t] = acc[t];
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) red[warp * kMaxT + t] = acc;
   }
   __syncthreads();
 
   // 4. per (expert, token): logit, score, key
-  if (tid < p.epc * TMAX) {
-    const int g = tid / TMAX, t = tid - g * TMAX;
+  if (tid < p.epc * kMaxT) {
+    const int g = tid / kMaxT, t = tid - g * kMaxT;
     const int e2 = blockIdx.x * p.epc + g;
     if (t < T && e2 < N) {
       const int wpg = kDecodeWarps / p.epc;
-      float s = 0.0f;
-      for (int w = 0; w < wpg; ++w) s = __fadd_rn(s, red[(g * wpg + w) * TMAX + t]);
+      float sacc = 0.0f;
+      for (int w = 0; w < wpg; ++w) sacc = __fadd_rn(sacc, red[(g * wpg + w) * kMaxT + t]);
       const float gscale = __fmul_rn(qs.gsa, __ldg(p.w_gsa));
-      const float l = __fmul_rn(__fmul_rn(s, 0.25f), gscale);   // the sums count 2a * 2b
+      const float l = __fmul_rn(__fmul_rn(sacc, 0.25f), gscale);   // the sums count 2a * 2b
       const size_t o = static_cast<size_t>(t) * N + e2;
       if (p.logits) {
         p.logits[o] = l;
@@ -182,61 +222,112 @@ decode_router_kernel(const DecodeParams p) {
   }
   if (p.logits) return;
 
-  // 5. the last CTA selects, renormalises and writes
+  // 5. the last CTA to finish selects, renormalises and writes
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int t = 0; t < T; ++t) {
-    for (int n = tid; n < N; n += kDecodeThreads) {
-      kbuf[n] = __ldcg(p.ws_keys + static_cast<size_t>(t) * N + n);
-      sbuf[n] = __ldcg(p.ws_scores + static_cast<size_t>(t) * N + n);
-    }
-    __syncthreads();
-    for (int n = tid; n < N; n += kDecodeThreads) {
-      const float kn = kbuf[n];
+  float* kbuf = reinterpret_cast<float*>(xraw);                 // x is no longer needed
+  float* sbuf = kbuf + static_cast<size_t>(T) * N;
+  for (int i = tid; i < T * N; i += kDecodeThreads) {
+    kbuf[i] = __ldcg(p.ws_keys + i);
+    sbuf[i] = __ldcg(p.ws_scores + i);
+  }
+  __syncthreads();
+  if (T * N <= 2 * kDecodeThreads) {
+    // Small batches: every thread ranks one or two (token, expert) keys
+    // against the token's N keys (key descending, lower id first); the k
+    // lowest ranks are the selection, in order.
+    for (int pr = tid; pr < T * N; pr += kDecodeThreads) {
+      const int t = pr / N, n = pr - t * N;
+      const float* kt = kbuf + static_cast<size_t>(t) * N;
+      const float kn = kt[n];
       int rank = 0;
       for (int q = 0; q < N; ++q) {
-        const float kq = kbuf[q];
+        const float kq = kt[q];
         rank += (kq > kn || (kq == kn && q < n)) ? 1 : 0;
       }
-      if (rank < p.k) sel[rank] = n;
+      if (rank < p.k) s_sel[t * 16 + rank] = n;
     }
     __syncthreads();
-    if (tid == 0) {
+    if (tid < T) {
+      const int t = tid;
+      const float* st = sbuf + static_cast<size_t>(t) * N;
       float sum = 0.0f;
-      for (int i = 0; i < p.k; ++i) sum = __fadd_rn(sum, sbuf[sel[i]]);
-      for (int i = 0; i < p.k; ++i) {
-        const float sc = sbuf[sel[i]];
-        p.out_ids[static_cast<size_t>(t) * p.k + i] = sel[i];
-        p.out_w[static_cast<size_t>(t) * p.k + i] =
+      for (int r = 0; r < p.k; ++r) sum = __fadd_rn(sum, st[s_sel[t * 16 + r]]);
+      for (int r = 0; r < p.k; ++r) {
+        const int n = s_sel[t * 16 + r];
+        const float sc = st[n];
+        p.out_ids[static_cast<size_t>(t) * p.k + r] = n;
+        p.out_w[static_cast<size_t>(t) * p.k + r] =
             p.raw ? sc : (sum > 0.0f ? __fdiv_rn(__fmul_rn(p.routed_scaling, sc), sum) : 0.0f);
       }
     }
-    __syncthreads();
+    if (tid == 0) *p.ticket = 0u;
+    return;
+  }
+  // one warp per token: every lane keeps a sorted list of the best of its
+  // keys (n = lane, lane + 32, ...); k rounds of a warp-wide argmax over the
+  // list heads (key descending, lower id first) pick the winners in order
+  for (int t = warp; t < T; t += kDecodeWarps) {
+    TopK<16> tk;
+    tk.init();
+    const float* kt = kbuf + static_cast<size_t>(t) * N;
+    const float* st = sbuf + static_cast<size_t>(t) * N;
+    for (int n = lane; n < N; n += 32) tk.push(kt[n], n, st[n]);
+    float sum = 0.0f;
+    int32_t* oid = p.out_ids + static_cast<size_t>(t) * p.k;
+    float* ow = p.out_w + static_cast<size_t>(t) * p.k;
+    for (int r = 0; r < p.k; ++r) {
+      float bk = tk.key[0];
+      int bi = tk.id[0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        if (topk_better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+      }
+      // the winning lane pops its head
+      const bool mine = tk.id[0] == bi;
+      const float bs = __shfl_sync(0xFFFFFFFFu, tk.sc[0], __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1);
+      if (mine) tk.pop_front();
+      if (lane == 0) {
+        oid[r] = bi;
+        ow[r] = bs;                                            // the score, for now
+        sum = __fadd_rn(sum, bs);
+      }
+    }
+    if (lane == 0 && !p.raw) {
+      for (int r = 0; r < p.k; ++r)
+        ow[r] = sum > 0.0f ? __fdiv_rn(__fmul_rn(p.routed_scaling, ow[r]), sum) : 0.0f;
+    }
   }
   if (tid == 0) *p.ticket = 0u;
 }
 
 // ------------------------------------------------------------------ host side
 
-DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms) {
+DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms, bool bf16) {
   DecodePlan d;
   if (T < 1 || T > 16 || N > 16384 || num_sms < 1) return d;
   d.tmax = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
-  d.smem = decode_smem_bytes(static_cast<int>(T), static_cast<int>(D), static_cast<int>(N), d.tmax);
-  if (d.smem > 200 * 1024) return d;
   int epc = 1;
   while (epc < 8 && (N + epc - 1) / epc > num_sms) epc *= 2;
+  // every thread prefetches at most kMaxBlocksPerThread weight blocks
+  const int64_t gs = kDecodeThreads / epc;
+  if ((D / kBlock + gs - 1) / gs > kMaxBlocksPerThread) return d;
+  d.smem = decode_smem_layout(static_cast<int>(T), static_cast<int>(D), static_cast<int>(N),
+                              bf16 ? 2 : 4).total;
+  if (d.smem > kDecodeMaxSmem) return d;
   d.epc = epc;
   d.grid = static_cast<int>((N + epc - 1) / epc);
   d.ok = true;
   return d;
 }
 
-template <bool kBF16, int TMAX>
+template <bool kBF16>
 static cudaError_t launch_t(const DecodeParams& p, const DecodePlan& plan, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
   int dev = 0;
@@ -244,24 +335,13 @@ static cudaError_t launch_t(const DecodeParams& p, const DecodePlan& plan, cudaS
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_router_kernel<kBF16, TMAX>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    e = cudaFuncSetAttribute(decode_router_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kDecodeMaxSmem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  decode_router_kernel<kBF16, TMAX><<<plan.grid, kDecodeThreads, plan.smem, s>>>(p);
+  decode_router_kernel<kBF16><<<plan.grid, kDecodeThreads, plan.smem, s>>>(p);
   return cudaGetLastError();
-}
-
-template <bool kBF16>
-static cudaError_t launch_dt(const DecodeParams& p, const DecodePlan& plan, cudaStream_t s) {
-  switch (plan.tmax) {
-    case 1: return launch_t<kBF16, 1>(p, plan, s);
-    case 2: return launch_t<kBF16, 2>(p, plan, s);
-    case 4: return launch_t<kBF16, 4>(p, plan, s);
-    case 8: return launch_t<kBF16, 8>(p, plan, s);
-    default: return launch_t<kBF16, 16>(p, plan, s);
-  }
 }
 
 cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const uint8_t* W_codes,
@@ -276,7 +356,7 @@ cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const 
   p.raw = raw ? 1 : 0; p.epc = plan.epc;
   p.out_ids = out_ids; p.out_w = out_w; p.logits = logits;
   p.ws_keys = ws_keys; p.ws_scores = ws_scores; p.ticket = ticket;
-  return bf16 ? launch_dt<true>(p, plan, s) : launch_dt<false>(p, plan, s);
+  return bf16 ? launch_t<true>(p, plan, s) : launch_t<false>(p, plan, s);
 }
 
 }  // namespace nvr

@@ -40,12 +40,16 @@
 
 namespace nvr {
 
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kTileBytes = 128 * 128;              // 128 rows x 128 bytes
 constexpr int kSfSlab = 4 * 512;                   // 4 scale tiles
 constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfSlab;
-constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*align*/;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiChunk = 32;                       // columns per tensor-memory load
+constexpr int kEpiBytes = kEpiChunk * 256 * 4;      // logits of one chunk, every epilogue thread
+constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*bias*/ + kEpiBytes +
+                          1024 /*align*/;
+constexpr int kGemmThreads = 320;                  // producer, MMA, 8 epilogue warps
+constexpr float kFilterMargin = 1e-4f;             // see the epilogue's candidate filter
 constexpr uint32_t kIdesc = idesc_mxf4nvf4(128, 128);
 
 struct GemmParams {
@@ -103,6 +107,8 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* last_flag = abort_flag + 1;
   volatile int* epi_abort = abort_flag + 2;     // the epilogue's agreed view of abort_flag
+  float* s_bias = reinterpret_cast<float*>(smem + kStages * kStageBytes + 1024);   // [2][128]
+  float* s_lg = s_bias + 2 * 128;                   // [kEpiChunk][256] logits, column per thread
 
   // producer thread: which ring stages were filled, and the parity of each
   // stage's latest fill (bit s)
@@ -116,7 +122,7 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(acc_full + b, 1); mbar_init(acc_empty + b, 128); }
+    for (int b = 0; b < 2; ++b) { mbar_init(acc_full + b, 1); mbar_init(acc_empty + b, 256); }
     *abort_flag = 0;
     *last_flag = 0;
     *epi_abort = 0;
@@ -135,48 +141,66 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues the copies.
+    {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int it = 0; it < n_mine && ok; ++it) {
         const int j = split + it * p.n_splits;
         for (int ks = 0; ks < k_stages; ++ks) {
-          if (!mbar_wait(empty + stage, phase ^ 1u, deadline, abort_flag)) { ok = false; break; }
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty + stage, phase ^ 1u, deadline, abort_flag))) {
+            ok = false;
+            break;
+          }
           const int nkk = min(4, KB / 4 - 4 * ks);
           uint8_t* a = smem + stage * kStageBytes;
           uint8_t* b = a + kTileBytes;
           uint8_t* sa = b + kTileBytes;
           uint8_t* sb = sa + kSfSlab;
-          mbar_arrive_expect_tx(full + stage, 2u * kTileBytes + 2u * 512u * nkk);
-          tma_load_2d(a, &p.tmap_a, ks * 128, m_tile * 128, full + stage);
-          tma_load_2d(b, &p.tmap_b, ks * 128, j * 128, full + stage);
-          bulk_load(sa, p.sfa + (static_cast<size_t>(m_tile) * (KB / 4) + 4 * ks) * 512, 512u * nkk, full + stage);
-          bulk_load(sb, p.sfb + (static_cast<size_t>(j) * (KB / 4) + 4 * ks) * 512, 512u * nkk, full + stage);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(full + stage, 2u * kTileBytes + 2u * 512u * nkk);
+            tma_load_2d(a, &p.tmap_a, ks * 128, m_tile * 128, full + stage);
+            tma_load_2d(b, &p.tmap_b, ks * 128, j * 128, full + stage);
+            bulk_load(sa, p.sfa + (static_cast<size_t>(m_tile) * (KB / 4) + 4 * ks) * 512, 512u * nkk,
+                      full + stage);
+            bulk_load(sb, p.sfb + (static_cast<size_t>(j) * (KB / 4) + 4 * ks) * 512, 512u * nkk,
+                      full + stage);
+          }
+          __syncwarp();
           filled_mask |= 1u << stage;
           fill_bits = (fill_bits & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         report_timeout(p.status);
         *abort_flag = 1;
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && !p.test_stall) {
+    // The whole warp runs the loop; one elected lane issues the tensor-core
+    // work and its commits (a commit tracks the issuing thread's operations).
+    if (!p.test_stall) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int it = 0; it < n_mine && ok; ++it) {
         const int buf = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(acc_empty + buf, acc_phase ^ 1u, deadline, abort_flag)) { ok = false; break; }
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_empty + buf, acc_phase ^ 1u, deadline, abort_flag))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * 128;
         for (int ks = 0; ks < k_stages; ++ks) {
-          if (!mbar_wait(full + stage, phase, deadline, abort_flag)) { ok = false; break; }
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + stage, phase, deadline, abort_flag))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const int nkk = min(4, KB / 4 - 4 * ks);
           const uint8_t* a = smem + stage * kStageBytes;
@@ -185,27 +209,36 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
           const uint8_t* sb = sa + kSfSlab;
           const uint32_t sfa_t = tmem + 256 + stage * 32;
           const uint32_t sfb_t = sfa_t + 16;
-          for (int kk = 0; kk < nkk; ++kk) {
-            tc_copy_scales(sfa_t + 4 * kk, desc_scale_tile(smem_u32(sa + 512 * kk)));
-            tc_copy_scales(sfb_t + 4 * kk, desc_scale_tile(smem_u32(sb + 512 * kk)));
+          if (elect_one()) {
+            for (int kk = 0; kk < nkk; ++kk) {
+              tc_copy_scales(sfa_t + 4 * kk, desc_scale_tile(smem_u32(sa + 512 * kk)));
+              tc_copy_scales(sfb_t + 4 * kk, desc_scale_tile(smem_u32(sb + 512 * kk)));
+            }
+            for (int kk = 0; kk < nkk; ++kk) {
+              tc_mma_nvf4(d_tmem, desc_kmajor_sw128(smem_u32(a + 32 * kk)),
+                          desc_kmajor_sw128(smem_u32(b + 32 * kk)), kIdesc, sfa_t + 4 * kk,
+                          sfb_t + 4 * kk, (ks | kk) != 0);
+            }
+            tc_commit(empty + stage);
           }
-          for (int kk = 0; kk < nkk; ++kk) {
-            tc_mma_nvf4(d_tmem, desc_kmajor_sw128(smem_u32(a + 32 * kk)),
-                        desc_kmajor_sw128(smem_u32(b + 32 * kk)), kIdesc, sfa_t + 4 * kk,
-                        sfb_t + 4 * kk, (ks | kk) != 0);
-          }
-          tc_commit(empty + stage);
+          __syncwarp();
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        if (ok) tc_commit(acc_full + buf);
+        if (ok && elect_one()) tc_commit(acc_full + buf);
+        __syncwarp();
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         report_timeout(p.status);
         *abort_flag = 1;
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Eight warps: two per tensor-memory lane quarter, each owning half of
+    // every tile's 128 columns for its 32 token rows, so two warps share each
+    // scheduler and hide each other's latencies.
+    const int etid = threadIdx.x - 64;             // 0..255
+    const int half = etid >> 7;                    // columns [64*half, 64*half + 64) of a tile
     const int quarter = warp & 3;                  // tensor-memory lanes 32*quarter ..
     const int row = quarter * 32 + lane;
     const int64_t token = static_cast<int64_t>(m_tile) * 128 + row;
@@ -218,35 +251,67 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
       const int j = split + it * p.n_splits;
       const int buf = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      // all lanes of a warp take the same branch (tcgen05.ld is warp-wide)
-      const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full + buf, acc_phase, deadline, abort_flag));
+      // Stage this N tile's bias in shared memory while the tile accumulates
+      // (double-buffered by tile parity).
+      float* tb = s_bias + buf * 128;
+      if (etid < 128 && !p.raw && !p.logits) {
+        const int n = j * 128 + etid;
+        tb[etid] = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.0f;
+      }
+      // The epilogue warps agree on the outcome of the wait (one barrier that
+      // also publishes the staged bias), so all of them leave the loop
+      // together on a timeout and tcgen05.ld always runs warp-wide.
+      const bool got = bar_and(1, 256, mbar_wait(acc_full + buf, acc_phase, deadline, abort_flag));
       if (!got) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = half * 2 + cc;               // 32-column chunk of the tile
         float v[32];
         tmem_load32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * 128 + c * 32, v);
-        if (active) {
-          const int n0 = j * 128 + c * 32;
-          if (p.logits) {
+        const int n0 = j * 128 + c * 32;
+        if (p.logits) {
+          if (active) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (n0 + i < p.N) p.logits[token * p.N + n0 + i] = __fmul_rn(v[i], gscale);
-          } else if (p.raw) {
+          }
+        } else if (active) {
+          // Pass 1 (unrolled, cheap): every logit goes to this thread's column
+          // of s_lg; a column is a candidate when its key could beat the
+          // list's current last entry.  With a sigmoid the test uses a fast
+          // approximation (error < 1e-5 for every fp32 logit) against the
+          // threshold lowered by kFilterMargin, so no true candidate is lost.
+          const float thr_k = tk.key[KMAX - 1];
+          const int thr_i = tk.id[KMAX - 1];
+          uint32_t cand = 0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float l = __fmul_rn(v[i], gscale);
-              if (n0 + i < p.N) tk.push(l, n0 + i, l);
+          for (int i = 0; i < 32; ++i) {
+            const float l = __fmul_rn(v[i], gscale);
+            s_lg[i * 256 + etid] = l;
+            bool pass;
+            if (p.raw) {
+              pass = topk_better(l, n0 + i, thr_k, thr_i);
+            } else {
+              const float sa = __fdividef(1.0f, 1.0f + __expf(-l));
+              const float ka = p.bias ? sa + tb[c * 32 + i] : sa;
+              pass = ka >= thr_k - kFilterMargin;
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (n0 + i < p.N) {
-                const float s = sigmoidf_ieee(__fmul_rn(v[i], gscale));
-                const float key = p.bias ? __fadd_rn(s, __ldg(p.bias + n0 + i)) : s;
-                tk.push(key, n0 + i, s);
-              }
+            cand |= static_cast<uint32_t>(pass && (n0 + i < p.N)) << i;
+          }
+          // Pass 2 (rolled): the exact score and key of each candidate, then
+          // the sorted insertion (which rejects those that do not qualify).
+#pragma unroll 1
+          while (cand) {
+            const int i = __ffs(cand) - 1;
+            cand &= cand - 1;
+            const float l = s_lg[i * 256 + etid];
+            float key = l, sc = l;
+            if (!p.raw) {
+              sc = sigmoidf_ieee(l);
+              key = p.bias ? __fadd_rn(sc, tb[c * 32 + i]) : sc;
             }
+            tk.push(key, n0 + i, sc);
           }
         }
       }
@@ -260,40 +325,81 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
     // Agree on one abort decision before the named barriers below: every
     // epilogue thread has left its loop (bounded waits) and published its
     // failure; one thread snapshots the flag for all.
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (threadIdx.x == 64) *epi_abort = *abort_flag;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (etid == 0) *epi_abort = *abort_flag;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     if (!*epi_abort && !p.logits) {
-      if (p.n_splits == 1) {
-        if (active) write_final<KMAX>(tk, p, token);
-      } else {
-        float4* dst = p.partials + (static_cast<size_t>(blockIdx.x) * 128 + row) * KMAX;
+      // The two halves of each row merge: the second hands its list to the
+      // first through shared memory.
+      float* s_m = s_lg;                           // [KMAX][3][128]
+      if (half == 1 && active) {
 #pragma unroll
-        for (int i = 0; i < KMAX; ++i) dst[i] = make_float4(tk.key[i], __int_as_float(tk.id[i]), tk.sc[i], 0.0f);
-        __threadfence();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (threadIdx.x == 64) {
-          const uint32_t t = atomicAdd(p.tickets + m_tile, 1u);
-          *last_flag = (t == static_cast<uint32_t>(p.n_splits - 1)) ? 1 : 0;
+        for (int i = 0; i < KMAX; ++i) {
+          s_m[(i * 3 + 0) * 128 + row] = tk.key[i];
+          s_m[(i * 3 + 1) * 128 + row] = __int_as_float(tk.id[i]);
+          s_m[(i * 3 + 2) * 128 + row] = tk.sc[i];
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (*last_flag) {
-          __threadfence();
-          if (active) {
-            TopK<KMAX> fin;
-            fin.init();
-            const float4* src = p.partials + static_cast<size_t>(m_tile) * p.n_splits * 128 * KMAX;
-            for (int s = 0; s < p.n_splits; ++s) {
-              const float4* e = src + (static_cast<size_t>(s) * 128 + row) * KMAX;
-#pragma unroll
-              for (int i = 0; i < KMAX; ++i) {
-                const float4 v = __ldcg(e + i);
-                fin.push(v.x, __float_as_int(v.y), v.z);
-              }
-            }
-            write_final<KMAX>(fin, p, token);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (half == 0) {
+        if (active) {
+#pragma unroll 1
+          for (int i = 0; i < KMAX; ++i) {
+            const float k2 = s_m[(i * 3 + 0) * 128 + row];
+            const int i2 = __float_as_int(s_m[(i * 3 + 1) * 128 + row]);
+            if (!topk_better(k2, i2, tk.key[KMAX - 1], tk.id[KMAX - 1])) break;   // sorted
+            tk.push(k2, i2, s_m[(i * 3 + 2) * 128 + row]);
           }
-          if (threadIdx.x == 64) p.tickets[m_tile] = 0u;
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");   // s_m is reused below
+        if (p.n_splits == 1) {
+          if (active) write_final<KMAX>(tk, p, token);
+        } else {
+          float4* dst = p.partials + (static_cast<size_t>(blockIdx.x) * 128 + row) * KMAX;
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i) dst[i] = make_float4(tk.key[i], __int_as_float(tk.id[i]), tk.sc[i], 0.0f);
+          __threadfence();
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+          if (etid == 0) {
+            const uint32_t t = atomicAdd(p.tickets + m_tile, 1u);
+            *last_flag = (t == static_cast<uint32_t>(p.n_splits - 1)) ? 1 : 0;
+          }
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+          if (*last_flag) {
+            __threadfence();
+            if (active) {
+              TopK<KMAX> fin;
+              fin.init();
+              const float4* src = p.partials + static_cast<size_t>(m_tile) * p.n_splits * 128 * KMAX;
+              // Every split's list is sorted, so a list is read only while its
+              // next entry still beats the merged list's last one.  The heads of
+              // 8 lists are fetched together (staged in shared memory) to
+              // overlap their latencies.
+              float4* s_head = reinterpret_cast<float4*>(s_lg);     // [8][128]
+              for (int s0 = 0; s0 < p.n_splits; s0 += 8) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const int sp = s0 + u;
+                  s_head[u * 128 + row] =
+                      sp < p.n_splits ? __ldcg(src + (static_cast<size_t>(sp) * 128 + row) * KMAX)
+                                      : make_float4(-INFINITY, __int_as_float(0x7FFFFFFF), 0.0f, 0.0f);
+                }
+#pragma unroll 1
+                for (int u = 0; u < 8; ++u) {
+                  float4 h = s_head[u * 128 + row];
+                  const float4* e = src + (static_cast<size_t>(s0 + u) * 128 + row) * KMAX;
+                  int i = 0;
+                  while (topk_better(h.x, __float_as_int(h.y), fin.key[KMAX - 1], fin.id[KMAX - 1])) {
+                    fin.push(h.x, __float_as_int(h.y), h.z);
+                    if (++i >= KMAX) break;
+                    h = __ldcg(e + i);
+                  }
+                }
+              }
+              write_final<KMAX>(fin, p, token);
+            }
+            if (etid == 0) p.tickets[m_tile] = 0u;
+          }
         }
       }
     }

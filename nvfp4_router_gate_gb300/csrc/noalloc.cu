@@ -77,7 +77,7 @@ extern "C" nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int6
   if (T == 0) return NVR_OK;
   const int sms = device_sm_count();
   if (sms <= 0) return NVR_ERR_CUDA;
-  const DecodePlan dp = plan_decode(T, D, N, sms);
+  const DecodePlan dp = plan_decode(T, D, N, sms, dt == NVR_BF16);
   if (!dp.ok) return NVR_ERR_UNSUPPORTED;
   cudaError_t e = cudaSuccess;
   uint8_t* scratch = scratch_for_current_device(&e);

@@ -183,8 +183,11 @@ __device__ __forceinline__ uint32_t f32x8_sign_nibbles(const float* v) {
 // |y_i / s| < 2^-11 for every nonzero scale s >= 2^-9, so the code is the
 // signed zero whatever the last bits of y_i are.  max|y| / 6 and y / s use the
 // same shortcut with b = 6 or b = s in [2^-9, 448].
+// `rcp_tab`, when given, holds RN(1 / dec(b)) for every scale byte b in
+// 1..126 (the same bits __frcp_rn returns).
 __device__ __forceinline__ uint32_t quant_block16(const Block16& blk, const QuantScale& qs,
-                                                  uint32_t& codes_lo, uint32_t& codes_hi) {
+                                                  uint32_t& codes_lo, uint32_t& codes_hi,
+                                                  const float* rcp_tab = nullptr) {
   const float (&x)[16] = blk.v;
   if (qs.mode == 0) { codes_lo = codes_hi = 0; return 0; }
   float y[16];
@@ -208,7 +211,7 @@ __device__ __forceinline__ uint32_t quant_block16(const Block16& blk, const Quan
   const uint32_t byte = e4m3_byte(sy);
   if (byte == 0) { codes_lo = codes_hi = 0; return 0; }
   const float s = e4m3_value(byte);
-  const float rs = __frcp_rn(s);
+  const float rs = rcp_tab ? rcp_tab[byte] : __frcp_rn(s);
   const uint64_t ns2 = f2_pack(-s, -s), rs2 = f2_pack(rs, rs);
   float q[16];
 #pragma unroll
@@ -247,6 +250,28 @@ __device__ __forceinline__ void load_block16(const void* base, size_t elem_off, 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float4 a = __ldg(p + i);
+      blk.v[4 * i] = a.x; blk.v[4 * i + 1] = a.y; blk.v[4 * i + 2] = a.z; blk.v[4 * i + 3] = a.w;
+    }
+    blk.neg_lo = f32x8_sign_nibbles(blk.v);
+    blk.neg_hi = f32x8_sign_nibbles(blk.v + 8);
+  }
+}
+
+// The same from shared memory (16-byte aligned rows).
+template <bool kBF16>
+__device__ __forceinline__ void load_block16_shared(const uint8_t* base, size_t elem_off, Block16& blk) {
+  if (kBF16) {
+    const uint4* q = reinterpret_cast<const uint4*>(base + elem_off * 2);
+    const uint4 a = q[0], b = q[1];
+    bf16x8_to_f32(a, blk.v);
+    bf16x8_to_f32(b, blk.v + 8);
+    blk.neg_lo = bf16x8_sign_nibbles(a.x, a.y, a.z, a.w);
+    blk.neg_hi = bf16x8_sign_nibbles(b.x, b.y, b.z, b.w);
+  } else {
+    const float4* q = reinterpret_cast<const float4*>(base + elem_off * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 a = q[i];
       blk.v[4 * i] = a.x; blk.v[4 * i + 1] = a.y; blk.v[4 * i + 2] = a.z; blk.v[4 * i + 3] = a.w;
     }
     blk.neg_lo = f32x8_sign_nibbles(blk.v);
@@ -313,6 +338,15 @@ struct TopK {
     key[0] = top ? k : key[0];
     id[0] = top ? i : id[0];
     sc[0] = top ? s : sc[0];
+  }
+
+  // Drop the best entry (shift the list up by one; the tail becomes empty).
+  __device__ __forceinline__ void pop_front() {
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) { key[j] = key[j + 1]; id[j] = id[j + 1]; sc[j] = sc[j + 1]; }
+    key[K - 1] = -INFINITY;
+    id[K - 1] = 0x7FFFFFFF;
+    sc[K - 1] = 0.0f;
   }
 };
 

@@ -43,13 +43,13 @@ struct DecodePlan {
   int grid = 0;
   size_t smem = 0;
 };
-DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms);
+DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms, bool bf16);
 
 // Byte offsets inside the caller's workspace.
 struct WsLayout {
   size_t control = 0;        // 256 bytes: status word and tickets
   size_t amax_partials = 0;  // kMaxAmaxGrid x u32
-  size_t scalars = 0;        // x gsa, x amax (router path) -- 256 bytes
+  size_t scalars = 0;        // x gsa (router path), quantizer record {gsa, 1/gsa, mode, amax} -- 256 bytes
   size_t tickets = 0;        // m_tiles x u32
   size_t x_codes = 0;        // [rows_pad, D/2]
   size_t x_sf = 0;           // tile layout, rows_pad rows
@@ -62,10 +62,10 @@ WsLayout quantize_ws_layout(int64_t rows, int64_t D);
 
 // ----------------------------------------------------------------- launchers
 cudaError_t launch_amax(const void* x, bool bf16, int64_t n_elems, uint32_t* partials,
-                        uint32_t* ticket, float* gsa_out, float* amax_out, int grid,
+                        uint32_t* ticket, float* gsa_out, float* qrec, int grid,
                         cudaStream_t s);
 cudaError_t launch_quantize(const void* x, bool bf16, int64_t rows, int64_t D, bool tiled,
-                            const float* amax, uint8_t* codes, uint8_t* sf, cudaStream_t s);
+                            const float* qrec, uint8_t* codes, uint8_t* sf, cudaStream_t s);
 int amax_grid(int64_t n_elems, bool bf16, int num_sms);
 
 nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const float* x_gsa,

@@ -20,20 +20,25 @@
 
 namespace nvr {
 
+// Per-call quantizer constants published by the amax kernel's last CTA:
+// {gsa, RN(1/gsa), division mode (as int bits), amax}.
+constexpr int kQrecWords = 4;
+
 template <bool kBF16>
-__global__ void __launch_bounds__(kAmaxThreads)
+__global__ void __launch_bounds__(kAmaxThreads, 4)
 amax_kernel(const void* __restrict__ x, int64_t n_vec16, uint32_t* __restrict__ partials,
-            uint32_t* __restrict__ ticket, float* __restrict__ gsa_out, float* __restrict__ amax_out) {
+            uint32_t* __restrict__ ticket, float* __restrict__ gsa_out, float* __restrict__ qrec) {
   const uint4* v = static_cast<const uint4*>(x);
   uint32_t m = 0;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  // four independent loads in flight per thread
-  for (; i + 3 * stride < n_vec16; i += 4 * stride) {
-    const uint4 a = __ldg(v + i), b = __ldg(v + i + stride), c = __ldg(v + i + 2 * stride),
-                d = __ldg(v + i + 3 * stride);
-    m = max(m, max(max(absmax_bits16B<kBF16>(a), absmax_bits16B<kBF16>(b)),
-                   max(absmax_bits16B<kBF16>(c), absmax_bits16B<kBF16>(d))));
+  // eight independent 16-byte loads in flight per thread
+  for (; i + 7 * stride < n_vec16; i += 8 * stride) {
+    uint4 a[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) a[u] = __ldg(v + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m = max(m, absmax_bits16B<kBF16>(a[u]));
   }
   for (; i < n_vec16; i += stride) m = max(m, absmax_bits16B<kBF16>(__ldg(v + i)));
 #pragma unroll
@@ -65,64 +70,81 @@ amax_kernel(const void* __restrict__ x, int64_t n_vec16, uint32_t* __restrict__ 
     uint32_t r = 0;
     for (int w = 0; w < kAmaxThreads / 32; ++w) r = max(r, red[w]);
     const float amax = __uint_as_float(r);
-    *gsa_out = __fdiv_rn(amax, kGsaDivisor);
-    if (amax_out) *amax_out = amax;
+    const QuantScale qs = make_quant_scale(amax);
+    *gsa_out = qs.gsa;
+    qrec[0] = qs.gsa;
+    qrec[1] = qs.rgsa;
+    qrec[2] = __int_as_float(qs.mode);
+    qrec[3] = amax;
     *ticket = 0u;                          // ready for the next call
   }
 }
 
-// One thread per (row, 16-element block).  Rows in [rows, rows_pad) only write
-// zero scale bytes (tile layout padding).
+// Two consecutive 16-element blocks of one row per thread: four (bf16) or
+// eight (fp32) 16-byte loads, one 16-byte code store, two scale bytes.  Rows
+// in [rows, rows_pad) only write zero scale bytes (tile layout padding).
 template <bool kBF16, bool kTiled>
 __global__ void __launch_bounds__(kQuantThreads)
-quantize_kernel(const void* __restrict__ x, int64_t rows, int64_t rows_pad, int64_t D,
-                const float* __restrict__ amax_in, uint8_t* __restrict__ codes,
+quantize_kernel(const void* __restrict__ x, uint32_t rows, uint32_t rows_pad, uint32_t D,
+                const float* __restrict__ qrec, uint8_t* __restrict__ codes,
                 uint8_t* __restrict__ sf) {
+  __shared__ float s_rcp[128];                 // RN(1 / dec(b)) for scale bytes b
+  if (threadIdx.x < 128) {
+    const uint32_t b = threadIdx.x;
+    s_rcp[b] = (b >= 1 && b <= 126) ? __frcp_rn(e4m3_value(b)) : 0.0f;
+  }
+  __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t KB = D / kBlock;
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t r = g / KB, c = g - r * KB;
-  // no early return: every lane of the warp takes part in the shuffles below
-  uint32_t byte = 0;
+  const uint32_t KB = D / kBlock;
+  const uint32_t pairs_per_row = KB / 2;
+  const uint32_t g = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t r = g / pairs_per_row;
+  const uint32_t c = 2 * (g - r * pairs_per_row);          // first block of the pair
+  // no early return: every lane of the warp takes part in the shuffle below
+  uint32_t b0 = 0, b1 = 0;
   if (r < rows) {
-    const QuantScale qs = make_quant_scale(__ldcg(amax_in));
+    QuantScale qs;
+    qs.gsa = __ldg(qrec);
+    qs.rgsa = __ldg(qrec + 1);
+    qs.mode = __float_as_int(__ldg(qrec + 2));
+    uint4 q;
     Block16 blk;
-    load_block16<kBF16>(x, static_cast<size_t>(r * D + c * kBlock), blk);
-    uint32_t lo, hi;
-    byte = quant_block16(blk, qs, lo, hi);
-    *reinterpret_cast<uint2*>(codes + r * (D / 2) + c * 8) = make_uint2(lo, hi);
+    const size_t e0 = static_cast<size_t>(r) * D + static_cast<size_t>(c) * kBlock;
+    load_block16<kBF16>(x, e0, blk);
+    b0 = quant_block16(blk, qs, q.x, q.y, s_rcp);
+    load_block16<kBF16>(x, e0 + kBlock, blk);
+    b1 = quant_block16(blk, qs, q.z, q.w, s_rcp);
+    *reinterpret_cast<uint4*>(codes + static_cast<size_t>(r) * (D / 2) + static_cast<size_t>(c) * 8) = q;
   }
   if (kTiled) {
     // blocks 4c'..4c'+3 of a row are 4 consecutive bytes of one tile line:
-    // gather them in the lane holding c % 4 == 0 (KB % 4 == 0, so the four
-    // lanes always share the row)
-    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 1);
-    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
-    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3);
+    // the even lane of each pair of lanes writes them (KB % 4 == 0, so both
+    // lanes hold the same row)
+    const uint32_t o = __shfl_down_sync(0xFFFFFFFFu, b0 | (b1 << 8), 1);
     if ((c & 3) == 0 && r < rows_pad)
-      *reinterpret_cast<uint32_t*>(sf + sf_tile_offset(r, c, KB)) = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      *reinterpret_cast<uint32_t*>(sf + sf_tile_offset(r, c, KB)) = b0 | (b1 << 8) | (o << 16);
   } else if (r < rows) {
-    sf[r * KB + c] = static_cast<uint8_t>(byte);
+    *reinterpret_cast<uint16_t*>(sf + static_cast<size_t>(r) * KB + c) = static_cast<uint16_t>(b0 | (b1 << 8));
   }
 }
 
 // ------------------------------------------------------------------ launchers
 
 cudaError_t launch_amax(const void* x, bool bf16, int64_t n_elems, uint32_t* partials,
-                        uint32_t* ticket, float* gsa_out, float* amax_out, int grid,
+                        uint32_t* ticket, float* gsa_out, float* qrec, int grid,
                         cudaStream_t s) {
   const int64_t n_vec16 = n_elems * (bf16 ? 2 : 4) / 16;
   if (bf16)
-    amax_kernel<true><<<grid, kAmaxThreads, 0, s>>>(x, n_vec16, partials, ticket, gsa_out, amax_out);
+    amax_kernel<true><<<grid, kAmaxThreads, 0, s>>>(x, n_vec16, partials, ticket, gsa_out, qrec);
   else
-    amax_kernel<false><<<grid, kAmaxThreads, 0, s>>>(x, n_vec16, partials, ticket, gsa_out, amax_out);
+    amax_kernel<false><<<grid, kAmaxThreads, 0, s>>>(x, n_vec16, partials, ticket, gsa_out, qrec);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const void* x, bool bf16, int64_t rows, int64_t D, bool tiled,
-                            const float* amax, uint8_t* codes, uint8_t* sf, cudaStream_t s) {
+                            const float* qrec, uint8_t* codes, uint8_t* sf, cudaStream_t s) {
   const int64_t rows_pad = tiled ? (rows + 127) / 128 * 128 : rows;
-  const int64_t n_threads = rows_pad * (D / kBlock);
+  const int64_t n_threads = rows_pad * (D / kBlock / 2);
   const int64_t grid = (n_threads + kQuantThreads - 1) / kQuantThreads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -133,10 +155,12 @@ cudaError_t launch_quantize(const void* x, bool bf16, int64_t rows, int64_t D, b
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (bf16 && tiled) return cudaLaunchKernelEx(&cfg, quantize_kernel<true, true>, x, rows, rows_pad, D, amax, codes, sf);
-  if (bf16) return cudaLaunchKernelEx(&cfg, quantize_kernel<true, false>, x, rows, rows_pad, D, amax, codes, sf);
-  if (tiled) return cudaLaunchKernelEx(&cfg, quantize_kernel<false, true>, x, rows, rows_pad, D, amax, codes, sf);
-  return cudaLaunchKernelEx(&cfg, quantize_kernel<false, false>, x, rows, rows_pad, D, amax, codes, sf);
+  const uint32_t r32 = static_cast<uint32_t>(rows), rp32 = static_cast<uint32_t>(rows_pad),
+                 d32 = static_cast<uint32_t>(D);
+  if (bf16 && tiled) return cudaLaunchKernelEx(&cfg, quantize_kernel<true, true>, x, r32, rp32, d32, qrec, codes, sf);
+  if (bf16) return cudaLaunchKernelEx(&cfg, quantize_kernel<true, false>, x, r32, rp32, d32, qrec, codes, sf);
+  if (tiled) return cudaLaunchKernelEx(&cfg, quantize_kernel<false, true>, x, r32, rp32, d32, qrec, codes, sf);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<false, false>, x, r32, rp32, d32, qrec, codes, sf);
 }
 
 }  // namespace nvr
