@@ -134,9 +134,9 @@ nvr_status quantize_impl(const void* x, nvr_dtype dt, int64_t rows, int64_t D, u
   float* qrec = reinterpret_cast<float*>(w + L.scalars + 16);    // {gsa, 1/gsa, mode, amax}
   ProfileScope prof(s);
   prof.before();
-  cudaError_t e = launch_amax(x, bf16, rows * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
-                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), gsa, qrec,
-                              amax_grid(rows * D, bf16, sms), s);
+  cudaError_t e = launch_amax_bulk(x, bf16, rows * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
+                                   reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), gsa, qrec,
+                                   reinterpret_cast<uint32_t*>(w + kWsStatus), sms, s);
   prof.after();
   if (e != cudaSuccess) return NVR_ERR_CUDA;
   prof.before();
@@ -197,9 +197,9 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   uint8_t* xsf = w + L.x_sf;
   ProfileScope prof(s);
   prof.before();
-  cudaError_t e = launch_amax(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
-                              reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec,
-                              amax_grid(T * D, bf16, sms), s);
+  cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
+                                   reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec,
+                                   reinterpret_cast<uint32_t*>(w + kWsStatus), sms, s);
   prof.after();
   if (e != cudaSuccess) return NVR_ERR_CUDA;
   prof.before();

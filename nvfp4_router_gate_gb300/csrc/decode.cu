@@ -129,6 +129,18 @@ decode_router_kernel(const DecodeParams p) {
     cp_async16(xraw + 16 * v, static_cast<const uint8_t*>(p.x) + 16 * v);
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncthreads();
+  // decode this thread's weight blocks now: their loads were issued first and
+  // have landed by the time x has; this keeps them off the critical path later
+  uint32_t wv[kMaxBlocksPerThread][4];
+  float swv[kMaxBlocksPerThread];
+#pragma unroll
+  for (int i = 0; i < kMaxBlocksPerThread; ++i) {
+    swv[i] = e4m3_value(wsb[i]);
+    wv[i][0] = e2m1x4_to_s8x4(wc[i].x & 0xFFFFu);
+    wv[i][1] = e2m1x4_to_s8x4(wc[i].x >> 16);
+    wv[i][2] = e2m1x4_to_s8x4(wc[i].y & 0xFFFFu);
+    wv[i][3] = e2m1x4_to_s8x4(wc[i].y >> 16);
+  }
 
   // 1. max |x| over the whole batch (from shared memory)
   const uint4* x4 = reinterpret_cast<const uint4*>(xraw);
@@ -164,16 +176,6 @@ decode_router_kernel(const DecodeParams p) {
   // 3. logits of this CTA's experts: integer dot products of each 16-element
   //    block (exact), scaled by the two block scales (exact product), fp32 sum.
   //    The weight blocks are decoded once; the token loop stays rolled.
-  uint32_t wv[kMaxBlocksPerThread][4];
-  float swv[kMaxBlocksPerThread];
-#pragma unroll
-  for (int i = 0; i < kMaxBlocksPerThread; ++i) {
-    swv[i] = e4m3_value(wsb[i]);
-    wv[i][0] = e2m1x4_to_s8x4(wc[i].x & 0xFFFFu);
-    wv[i][1] = e2m1x4_to_s8x4(wc[i].x >> 16);
-    wv[i][2] = e2m1x4_to_s8x4(wc[i].y & 0xFFFFu);
-    wv[i][3] = e2m1x4_to_s8x4(wc[i].y >> 16);
-  }
 #pragma unroll 1
   for (int t = 0; t < T; ++t) {
     float acc = 0.0f;
@@ -214,7 +216,7 @@ decode_router_kernel(const DecodeParams p) {
         p.ws_keys[o] = l;
         p.ws_scores[o] = l;
       } else {
-        const float sc = sigmoidf_ieee(l);
+        const float sc = sigmoid_f32(l);
         p.ws_keys[o] = p.bias ? __fadd_rn(sc, __ldg(p.bias + e2)) : sc;
         p.ws_scores[o] = sc;
       }
@@ -245,7 +247,15 @@ decode_router_kernel(const DecodeParams p) {
       const float* kt = kbuf + static_cast<size_t>(t) * N;
       const float kn = kt[n];
       int rank = 0;
-      for (int q = 0; q < N; ++q) {
+      int q = 0;
+      for (; q + 8 <= N; q += 8) {                 // 8 independent shared loads per step
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float kq = kt[q + u];
+          rank += (kq > kn || (kq == kn && q + u < n)) ? 1 : 0;
+        }
+      }
+      for (; q < N; ++q) {
         const float kq = kt[q];
         rank += (kq > kn || (kq == kn && q < n)) ? 1 : 0;
       }
@@ -276,7 +286,11 @@ decode_router_kernel(const DecodeParams p) {
     tk.init();
     const float* kt = kbuf + static_cast<size_t>(t) * N;
     const float* st = sbuf + static_cast<size_t>(t) * N;
-    for (int n = lane; n < N; n += 32) tk.push(kt[n], n, st[n]);
+    for (int base = 0; base < N; base += 32) {        // same trip count in every lane
+      const int n = base + lane;
+      const bool valid = n < N;
+      tk.push_if(valid ? kt[n] : 0.0f, n, valid ? st[n] : 0.0f, valid);
+    }
     float sum = 0.0f;
     int32_t* oid = p.out_ids + static_cast<size_t>(t) * p.k;
     float* ow = p.out_w + static_cast<size_t>(t) * p.k;

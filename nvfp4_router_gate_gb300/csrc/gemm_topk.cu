@@ -49,7 +49,6 @@ constexpr int kEpiBytes = kEpiChunk * 256 * 4;      // logits of one chunk, ever
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*bias*/ + kEpiBytes +
                           1024 /*align*/;
 constexpr int kGemmThreads = 320;                  // producer, MMA, 8 epilogue warps
-constexpr float kFilterMargin = 1e-4f;             // see the epilogue's candidate filter
 constexpr uint32_t kIdesc = idesc_mxf4nvf4(128, 128);
 
 struct GemmParams {
@@ -276,42 +275,79 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
             for (int i = 0; i < 32; ++i)
               if (n0 + i < p.N) p.logits[token * p.N + n0 + i] = __fmul_rn(v[i], gscale);
           }
-        } else if (active) {
-          // Pass 1 (unrolled, cheap): every logit goes to this thread's column
-          // of s_lg; a column is a candidate when its key could beat the
-          // list's current last entry.  With a sigmoid the test uses a fast
-          // approximation (error < 1e-5 for every fp32 logit) against the
-          // threshold lowered by kFilterMargin, so no true candidate is lost.
-          const float thr_k = tk.key[KMAX - 1];
-          const int thr_i = tk.id[KMAX - 1];
-          uint32_t cand = 0;
+        } else {
+          // Pass 1 (unrolled, branch-free): the exact key of every column of
+          // the chunk; the logits go to this thread's column of s_lg.  A
+          // keys-only sorted insertion (max/min only) of those keys into a copy
+          // of the list's keys yields tau, the exact k-th largest key of the
+          // list and the chunk together.  Only columns with key >= tau can
+          // enter the list, so only they take the (costlier) exact insertion
+          // with ids and scores: at most k of them plus exact ties.
+          float sk[KMAX];
+#pragma unroll
+          for (int q = 0; q < KMAX; ++q) sk[q] = tk.key[q];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float l = __fmul_rn(v[i], gscale);
             s_lg[i * 256 + etid] = l;
-            bool pass;
-            if (p.raw) {
-              pass = topk_better(l, n0 + i, thr_k, thr_i);
-            } else {
-              const float sa = __fdividef(1.0f, 1.0f + __expf(-l));
-              const float ka = p.bias ? sa + tb[c * 32 + i] : sa;
-              pass = ka >= thr_k - kFilterMargin;
+            float key = l;
+            if (!p.raw) {
+              const float sc = sigmoid_f32(l);
+              key = p.bias ? __fadd_rn(sc, tb[c * 32 + i]) : sc;
             }
-            cand |= static_cast<uint32_t>(pass && (n0 + i < p.N)) << i;
+            v[i] = (active && n0 + i < p.N) ? key : -INFINITY;
+#pragma unroll
+            for (int q = KMAX - 1; q > 0; --q) sk[q] = fmaxf(sk[q], fminf(sk[q - 1], v[i]));
+            sk[0] = fmaxf(sk[0], v[i]);
           }
-          // Pass 2 (rolled): the exact score and key of each candidate, then
-          // the sorted insertion (which rejects those that do not qualify).
+          const float tau = sk[KMAX - 1];
+          uint32_t cand = 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            cand |= static_cast<uint32_t>(v[i] != -INFINITY && v[i] >= tau) << i;
+          // Pass 2: the candidates enter the list.  With an 8-entry list, up
+          // to 8 of them are gathered into fixed slots, sorted by a
+          // 19-comparator network and merged with a bitonic merge (no
+          // data-dependent control flow); any further candidates (exact ties
+          // at tau) and lists of other sizes take the exact insertion.  Loops
+          // run the same number of rounds in every lane of the warp (the
+          // warp's largest candidate count), so the lanes stay converged.
+          if constexpr (KMAX == 8) {
+            float gk[8], gs[8];
+            int gi[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const bool has = cand != 0;
+              const int i = has ? __ffs(cand) - 1 : 0;
+              cand &= cand - 1;
+              const float l = s_lg[i * 256 + etid];
+              float key = l, sc = l;
+              if (!p.raw) {
+                sc = sigmoid_f32(l);
+                key = p.bias ? __fadd_rn(sc, tb[c * 32 + i]) : sc;
+              }
+              gk[r] = has ? key : -INFINITY;
+              gi[r] = has ? n0 + i : 0x7FFFFFFF;
+              gs[r] = has ? sc : 0.0f;
+            }
+            if (__any_sync(0xFFFFFFFFu, gk[0] != -INFINITY)) {
+              sort8(gk, gi, gs);
+              tk.merge_sorted8(gk, gi, gs);
+            }
+          }
+          const int rounds = __reduce_max_sync(0xFFFFFFFFu, static_cast<unsigned>(__popc(cand)));
 #pragma unroll 1
-          while (cand) {
-            const int i = __ffs(cand) - 1;
+          for (int r = 0; r < rounds; ++r) {
+            const bool has = cand != 0;
+            const int i = has ? __ffs(cand) - 1 : 0;
             cand &= cand - 1;
             const float l = s_lg[i * 256 + etid];
             float key = l, sc = l;
             if (!p.raw) {
-              sc = sigmoidf_ieee(l);
+              sc = sigmoid_f32(l);
               key = p.bias ? __fadd_rn(sc, tb[c * 32 + i]) : sc;
             }
-            tk.push(key, n0 + i, sc);
+            tk.push_if(key, n0 + i, sc, has);
           }
         }
       }
@@ -342,13 +378,27 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (half == 0) {
-        if (active) {
+        if constexpr (KMAX == 8) {
+          // both lists are sorted: one bitonic merge
+          float bk[8], bs[8];
+          int bi[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            bk[i] = s_m[(i * 3 + 0) * 128 + row];
+            bi[i] = __float_as_int(s_m[(i * 3 + 1) * 128 + row]);
+            bs[i] = s_m[(i * 3 + 2) * 128 + row];
+          }
+          if (active) tk.merge_sorted8(bk, bi, bs);
+        } else {
+          // warp-uniform loop; the half-1 list is sorted, so once no lane of
+          // the warp has a qualifying entry left the rest cannot qualify either
 #pragma unroll 1
           for (int i = 0; i < KMAX; ++i) {
             const float k2 = s_m[(i * 3 + 0) * 128 + row];
             const int i2 = __float_as_int(s_m[(i * 3 + 1) * 128 + row]);
-            if (!topk_better(k2, i2, tk.key[KMAX - 1], tk.id[KMAX - 1])) break;   // sorted
-            tk.push(k2, i2, s_m[(i * 3 + 2) * 128 + row]);
+            const bool q = active && topk_better(k2, i2, tk.key[KMAX - 1], tk.id[KMAX - 1]);
+            if (!__any_sync(0xFFFFFFFFu, q)) break;
+            tk.push_if(k2, i2, s_m[(i * 3 + 2) * 128 + row], q);
           }
         }
         asm volatile("bar.sync 2, 128;" ::: "memory");   // s_m is reused below
@@ -367,37 +417,57 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
           asm volatile("bar.sync 2, 128;" ::: "memory");
           if (*last_flag) {
             __threadfence();
-            if (active) {
-              TopK<KMAX> fin;
-              fin.init();
-              const float4* src = p.partials + static_cast<size_t>(m_tile) * p.n_splits * 128 * KMAX;
-              // Every split's list is sorted, so a list is read only while its
-              // next entry still beats the merged list's last one.  The heads of
-              // 8 lists are fetched together (staged in shared memory) to
-              // overlap their latencies.
-              float4* s_head = reinterpret_cast<float4*>(s_lg);     // [8][128]
-              for (int s0 = 0; s0 < p.n_splits; s0 += 8) {
+            TopK<KMAX> fin;
+            fin.init();
+            const float4* src = p.partials + static_cast<size_t>(m_tile) * p.n_splits * 128 * KMAX;
+            // Every split's list is sorted, so a list is read only while its
+            // next entry still beats the merged list's last one in some lane.
+            // The heads of 8 lists are fetched together (staged in shared
+            // memory) to overlap their latencies.  All loops are warp-uniform.
+            float4* s_head = reinterpret_cast<float4*>(s_lg);     // [8][128]
+            if constexpr (KMAX == 8) {
+              // fold the sorted split lists in with bitonic merges, fetching
+              // the next list while the current one merges
+              float4 nxt[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                  const int sp = s0 + u;
-                  s_head[u * 128 + row] =
-                      sp < p.n_splits ? __ldcg(src + (static_cast<size_t>(sp) * 128 + row) * KMAX)
-                                      : make_float4(-INFINITY, __int_as_float(0x7FFFFFFF), 0.0f, 0.0f);
-                }
+              for (int i = 0; i < 8; ++i) nxt[i] = __ldcg(src + static_cast<size_t>(row) * KMAX + i);
 #pragma unroll 1
-                for (int u = 0; u < 8; ++u) {
-                  float4 h = s_head[u * 128 + row];
-                  const float4* e = src + (static_cast<size_t>(s0 + u) * 128 + row) * KMAX;
-                  int i = 0;
-                  while (topk_better(h.x, __float_as_int(h.y), fin.key[KMAX - 1], fin.id[KMAX - 1])) {
-                    fin.push(h.x, __float_as_int(h.y), h.z);
-                    if (++i >= KMAX) break;
-                    h = __ldcg(e + i);
-                  }
+              for (int sp = 0; sp < p.n_splits; ++sp) {
+                float bk[8], bs[8];
+                int bi[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) { bk[i] = nxt[i].x; bi[i] = __float_as_int(nxt[i].y); bs[i] = nxt[i].z; }
+                if (sp + 1 < p.n_splits) {
+#pragma unroll
+                  for (int i = 0; i < 8; ++i)
+                    nxt[i] = __ldcg(src + (static_cast<size_t>(sp + 1) * 128 + row) * KMAX + i);
+                }
+                fin.merge_sorted8(bk, bi, bs);
+              }
+            }
+            for (int s0 = 0; KMAX != 8 && s0 < p.n_splits; s0 += 8) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int sp = s0 + u;
+                s_head[u * 128 + row] =
+                    sp < p.n_splits ? __ldcg(src + (static_cast<size_t>(sp) * 128 + row) * KMAX)
+                                    : make_float4(-INFINITY, __int_as_float(0x7FFFFFFF), 0.0f, 0.0f);
+              }
+#pragma unroll 1
+              for (int u = 0; u < 8; ++u) {
+                float4 h = s_head[u * 128 + row];
+                const float4* e = src + (static_cast<size_t>(s0 + u < p.n_splits ? s0 + u : 0) * 128 + row) * KMAX;
+                bool alive = active;
+#pragma unroll 1
+                for (int i = 0; i < KMAX; ++i) {
+                  alive = alive && topk_better(h.x, __float_as_int(h.y), fin.key[KMAX - 1], fin.id[KMAX - 1]);
+                  if (!__any_sync(0xFFFFFFFFu, alive)) break;
+                  fin.push_if(h.x, __float_as_int(h.y), h.z, alive);
+                  if (i + 1 < KMAX && alive) h = __ldcg(e + i + 1);
                 }
               }
-              write_final<KMAX>(fin, p, token);
             }
+            if (active) write_final<KMAX>(fin, p, token);
             if (etid == 0) p.tickets[m_tile] = 0u;
           }
         }

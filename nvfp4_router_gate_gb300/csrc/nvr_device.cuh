@@ -310,6 +310,52 @@ __device__ __forceinline__ bool topk_better(float ka, int ia, float kb, int ib) 
   return ka > kb || (ka == kb && ia < ib);
 }
 
+// The epilogue's score: sigmoid(l) = 1 / (1 + exp(-l)), branch-free.
+// exp(-l) = 2^t with t = -l*log2(e): t is split Cody-Waite style into its
+// float32 rounding t_hi and the rounding error t_lo (computed exactly with a
+// fused multiply-add plus the low part of log2(e)); 2^t_hi comes from the
+// hardware base-2 exponential (ex2.approx, relative error about 2^-22) and
+// 2^t ~= 2^t_hi * (1 + t_lo * ln 2).  The reciprocal uses the hardware
+// approximation (__fdividef, within 2 ulp, 0 for a denominator above 2^126).
+// The result is within a few ulp of the correctly rounded sigmoid for every
+// float32 logit, exact at l = 0 (0.5) and equal to 1 once exp(-l) < 2^-25.
+// (W. J. Cody, W. Waite, Software Manual for the Elementary Functions, 1980:
+// argument reduction with a split constant.)
+__device__ __forceinline__ float sigmoid_f32(float l) {
+  const float kLog2eHi = 1.44269502162933349609375f;      // RN(log2 e)
+  const float kLog2eLo = 1.925963033500011079e-8f;        // log2 e - kLog2eHi
+  const float t = __fmul_rn(-l, kLog2eHi);
+  const float t_lo = __fadd_rn(__fmaf_rn(-l, kLog2eHi, -t), __fmul_rn(-l, kLog2eLo));
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
+  e = __fmaf_rn(__fmul_rn(e, 0.693147180559945309f), t_lo, e);
+  return __fdividef(1.0f, __fadd_rn(1.0f, e));
+}
+
+// ------------------------------------------------- sorting-network helpers
+// Compare-exchange of slots a and b of a (key, id, score) array so that slot a
+// holds the better pair (key descending, then id ascending).
+template <int N>
+__device__ __forceinline__ void cswap(float (&k)[N], int (&i)[N], float (&s)[N], int a, int b) {
+  const bool sw = topk_better(k[b], i[b], k[a], i[a]);
+  const float tk = sw ? k[b] : k[a], ts = sw ? s[b] : s[a];
+  const int ti = sw ? i[b] : i[a];
+  k[b] = sw ? k[a] : k[b]; s[b] = sw ? s[a] : s[b]; i[b] = sw ? i[a] : i[b];
+  k[a] = tk; s[a] = ts; i[a] = ti;
+}
+
+// Sort 8 pairs best-first with the optimal 19-comparator network
+// (D. E. Knuth, The Art of Computer Programming vol. 3, section 5.3.4).
+__device__ __forceinline__ void sort8(float (&k)[8], int (&i)[8], float (&s)[8]) {
+  cswap(k, i, s, 0, 2); cswap(k, i, s, 1, 3); cswap(k, i, s, 4, 6); cswap(k, i, s, 5, 7);
+  cswap(k, i, s, 0, 4); cswap(k, i, s, 1, 5); cswap(k, i, s, 2, 6); cswap(k, i, s, 3, 7);
+  cswap(k, i, s, 0, 1); cswap(k, i, s, 2, 3); cswap(k, i, s, 4, 5); cswap(k, i, s, 6, 7);
+  cswap(k, i, s, 2, 4); cswap(k, i, s, 3, 5);
+  cswap(k, i, s, 1, 4); cswap(k, i, s, 3, 6);
+  cswap(k, i, s, 1, 2); cswap(k, i, s, 3, 4); cswap(k, i, s, 5, 6);
+}
+
+
 template <int K>
 struct TopK {
   float key[K];
@@ -340,6 +386,48 @@ struct TopK {
     sc[0] = top ? s : sc[0];
   }
 
+  // Warp-uniform insertion: every lane of the warp must call it together
+  // (no lane may have left the surrounding loop); lanes with valid == false
+  // or a pair that does not qualify keep their list.  When no lane has
+  // anything to insert the whole warp skips the work at once.
+  __device__ __forceinline__ void push_if(float k, int i, float s, bool valid) {
+    const bool ins = valid && topk_better(k, i, key[K - 1], id[K - 1]);
+    if (!__any_sync(0xFFFFFFFFu, ins)) return;
+#pragma unroll
+    for (int j = K - 1; j > 0; --j) {
+      const bool above = ins && topk_better(k, i, key[j - 1], id[j - 1]);
+      const bool here = ins && topk_better(k, i, key[j], id[j]);
+      key[j] = above ? key[j - 1] : (here ? k : key[j]);
+      id[j] = above ? id[j - 1] : (here ? i : id[j]);
+      sc[j] = above ? sc[j - 1] : (here ? s : sc[j]);
+    }
+    const bool top = ins && topk_better(k, i, key[0], id[0]);
+    key[0] = top ? k : key[0];
+    id[0] = top ? i : id[0];
+    sc[0] = top ? s : sc[0];
+  }
+
+  // Replace the list by the best 8 of (list, b) where b is sorted best-first
+  // (K == 8): the element-wise better of list[j] and b[7-j] is a bitonic
+  // sequence holding the 8 best; a bitonic half-cleaner cascade sorts it.
+  __device__ __forceinline__ void merge_sorted8(const float (&bk)[8], const int (&bi)[8],
+                                                const float (&bs)[8]) {
+    static_assert(K == 8, "merge_sorted8 needs an 8-entry list");
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool keep = topk_better(key[j], id[j], bk[7 - j], bi[7 - j]);
+      key[j] = keep ? key[j] : bk[7 - j];
+      id[j] = keep ? id[j] : bi[7 - j];
+      sc[j] = keep ? sc[j] : bs[7 - j];
+    }
+#pragma unroll
+    for (int d = 4; d > 0; d >>= 1) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if ((j & d) == 0) cswap(key, id, sc, j, j + d);
+    }
+  }
+
   // Drop the best entry (shift the list up by one; the tail becomes empty).
   __device__ __forceinline__ void pop_front() {
 #pragma unroll
@@ -349,10 +437,5 @@ struct TopK {
     sc[K - 1] = 0.0f;
   }
 };
-
-// The epilogue's per-expert transform: logit -> (selection key, score).
-__device__ __forceinline__ float sigmoidf_ieee(float l) {
-  return __frcp_rn(__fadd_rn(1.0f, expf(-l)));
-}
 
 }  // namespace nvr

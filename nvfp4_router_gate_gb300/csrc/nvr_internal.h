@@ -64,6 +64,9 @@ WsLayout quantize_ws_layout(int64_t rows, int64_t D);
 cudaError_t launch_amax(const void* x, bool bf16, int64_t n_elems, uint32_t* partials,
                         uint32_t* ticket, float* gsa_out, float* qrec, int grid,
                         cudaStream_t s);
+cudaError_t launch_amax_bulk(const void* x, bool bf16, int64_t n_elems, uint32_t* partials,
+                             uint32_t* ticket, float* gsa_out, float* qrec, uint32_t* status,
+                             int grid, cudaStream_t s);
 cudaError_t launch_quantize(const void* x, bool bf16, int64_t rows, int64_t D, bool tiled,
                             const float* qrec, uint8_t* codes, uint8_t* sf, cudaStream_t s);
 int amax_grid(int64_t n_elems, bool bf16, int num_sms);

@@ -17,6 +17,7 @@
 // The quantize kernel is launched with programmatic dependent launch and waits
 // on the amax kernel's results with griddepcontrol.wait.
 #include "nvr_internal.h"
+#include "nvr_tcgen05.cuh"
 
 namespace nvr {
 
@@ -80,6 +81,107 @@ amax_kernel(const void* __restrict__ x, int64_t n_vec16, uint32_t* __restrict__ 
   }
 }
 
+// The same reduction fed by bulk copies: a persistent grid (one CTA per SM)
+// walks its share of 32 KB chunks through a 4-stage shared-memory ring; one
+// thread issues cp.async.bulk for the chunks ahead while all threads reduce
+// the landed ones.  Bulk copies keep far more bytes in flight per SM than
+// per-thread loads, which is what a pure HBM stream needs.  Waits on the ring
+// are bounded (about a second); a timeout is recorded in the status word.
+constexpr int kAmaxChunk = 32 * 1024;
+constexpr int kAmaxStages = 4;
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kAmaxThreads, 1)
+amax_bulk_kernel(const uint8_t* __restrict__ x, int64_t nbytes, uint32_t* __restrict__ partials,
+                 uint32_t* __restrict__ ticket, float* __restrict__ gsa_out,
+                 float* __restrict__ qrec, uint32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kAmaxStages];
+  __shared__ uint32_t red[kAmaxThreads / 32];
+  __shared__ bool last;
+  const int64_t n_chunks = (nbytes + kAmaxChunk - 1) / kAmaxChunk;
+  const int64_t mine = n_chunks > blockIdx.x ? (n_chunks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  auto issue = [&](int64_t i) {                    // chunk i of this CTA into stage i % stages
+    const int64_t q = blockIdx.x + i * gridDim.x;
+    const int64_t off = q * kAmaxChunk;
+    const uint32_t bytes = static_cast<uint32_t>(nbytes - off < kAmaxChunk ? nbytes - off : kAmaxChunk);
+    uint64_t* bar = full + (i % kAmaxStages);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(ring + (i % kAmaxStages) * kAmaxChunk, x + off, bytes, bar);
+  };
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kAmaxStages; ++st) mbar_init(full + st, 1);
+    fence_mbar_init();
+    for (int64_t i = 0; i < mine && i < kAmaxStages; ++i) issue(i);
+  }
+  __syncthreads();
+  const uint64_t deadline = globaltimer_ns() + 1000000000ull;
+  volatile int never = 0;
+  uint32_t m = 0;
+  bool ok = true;
+  for (int64_t i = 0; i < mine; ++i) {
+    const int st = static_cast<int>(i % kAmaxStages);
+    const uint32_t parity = static_cast<uint32_t>((i / kAmaxStages) & 1);
+    ok = __syncthreads_and(mbar_wait(full + st, parity, deadline, &never)) != 0;
+    if (!ok) break;
+    const int64_t off = (blockIdx.x + i * gridDim.x) * static_cast<int64_t>(kAmaxChunk);
+    const int nvec = static_cast<int>((nbytes - off < kAmaxChunk ? nbytes - off : kAmaxChunk) / 16);
+    const uint4* v = reinterpret_cast<const uint4*>(ring + st * kAmaxChunk);
+#pragma unroll 4
+    for (int u = threadIdx.x; u < nvec; u += kAmaxThreads) m = max(m, absmax_bits16B<kBF16>(v[u]));
+    __syncthreads();                                // the stage has been read
+    if (threadIdx.x == 0 && i + kAmaxStages < mine) issue(i + kAmaxStages);
+  }
+  if (!ok) {
+    // wait (bounded) for this CTA's copies still in flight, then give up
+    if (threadIdx.x == 0) {
+      report_timeout(status);
+      const uint64_t drain = globaltimer_ns() + 1000000000ull;
+      for (int64_t i = 0; i < mine; ++i) {
+        if (i + kAmaxStages < mine) continue;       // only the last fills can be pending
+        while (!mbar_try_wait(full + (i % kAmaxStages), static_cast<uint32_t>((i / kAmaxStages) & 1)) &&
+               globaltimer_ns() < drain) {
+        }
+      }
+    }
+    __syncthreads();
+    return;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    for (int w = 0; w < kAmaxThreads / 32; ++w) b = max(b, red[w]);
+    partials[blockIdx.x] = b;
+    __threadfence();
+    last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (!last) return;
+  __threadfence();
+  uint32_t b = 0;
+  for (uint32_t j = threadIdx.x; j < gridDim.x; j += blockDim.x) b = max(b, __ldcg(partials + j));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = b;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int w = 0; w < kAmaxThreads / 32; ++w) r = max(r, red[w]);
+    const float amax = __uint_as_float(r);
+    const QuantScale qs = make_quant_scale(amax);
+    *gsa_out = qs.gsa;
+    qrec[0] = qs.gsa;
+    qrec[1] = qs.rgsa;
+    qrec[2] = __int_as_float(qs.mode);
+    qrec[3] = amax;
+    *ticket = 0u;
+  }
+}
+
 // Two consecutive 16-element blocks of one row per thread: four (bf16) or
 // eight (fp32) 16-byte loads, one 16-byte code store, two scale bytes.  Rows
 // in [rows, rows_pad) only write zero scale bytes (tile layout padding).
@@ -138,6 +240,30 @@ cudaError_t launch_amax(const void* x, bool bf16, int64_t n_elems, uint32_t* par
     amax_kernel<true><<<grid, kAmaxThreads, 0, s>>>(x, n_vec16, partials, ticket, gsa_out, qrec);
   else
     amax_kernel<false><<<grid, kAmaxThreads, 0, s>>>(x, n_vec16, partials, ticket, gsa_out, qrec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_bulk(const void* x, bool bf16, int64_t n_elems, uint32_t* partials,
+                             uint32_t* ticket, float* gsa_out, float* qrec, uint32_t* status,
+                             int grid, cudaStream_t s) {
+  static bool attr_set[kMaxDevices][2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int smem = kAmaxStages * kAmaxChunk;
+  if (!attr_set[dev][bf16]) {
+    e = bf16 ? cudaFuncSetAttribute(amax_bulk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+             : cudaFuncSetAttribute(amax_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev][bf16] = true;
+  }
+  const int64_t nbytes = n_elems * (bf16 ? 2 : 4);
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  if (bf16)
+    amax_bulk_kernel<true><<<grid, kAmaxThreads, smem, s>>>(xb, nbytes, partials, ticket, gsa_out, qrec, status);
+  else
+    amax_bulk_kernel<false><<<grid, kAmaxThreads, smem, s>>>(xb, nbytes, partials, ticket, gsa_out, qrec, status);
   return cudaGetLastError();
 }
 
