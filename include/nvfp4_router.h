@@ -99,7 +99,18 @@ enum {
    * fp32 accumulation order of the logits differs). */
   NVR_FLAG_FORCE_TENSOR_CORE = 2u,
   NVR_FLAG_FORCE_DECODE = 4u,
-  /* Failure-detection test hook (with FORCE_TENSOR_CORE only): the tensor-core
+  /* Tensor-core kernel choice (each implies FORCE_TENSOR_CORE; at most one).
+   * By default heads of up to 256 experts split K over S CTAs per 128-token
+   * tile (S from T, D and the SM count; fp32 partial logits in the workspace,
+   * summed by a second, warp-per-token epilogue kernel), and wider heads split
+   * N across CTAs.  SPLIT_K_2/4/8 force S (NVR_ERR_UNSUPPORTED when N > 256);
+   * SPLIT_N forces the N-split kernel for any N.  Results agree within the
+   * same tolerances; the logits' fp32 summation order differs. */
+  NVR_FLAG_SPLIT_K_2 = 8u,
+  NVR_FLAG_SPLIT_K_4 = 16u,
+  NVR_FLAG_SPLIT_K_8 = 32u,
+  NVR_FLAG_SPLIT_N = 64u,
+  /* Failure-detection test hook (with FORCE_TENSOR_CORE or a SPLIT flag): the tensor-core
    * kernel's MMA issuer issues nothing, so its bounded waits run out after
    * about one second; the kernel stores NVR_ERR_TIMEOUT in the workspace
    * status word, releases its tensor memory and returns.  The call itself
@@ -109,6 +120,11 @@ enum {
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvr_status_string(nvr_status s);
+
+/* Name of the CUDA error behind the most recent NVR_ERR_CUDA returned to this
+ * host thread ("cudaSuccess" if none; static string, never NULL).  No
+ * counterpart on the pages: a diagnostic for launch failures. */
+const char* nvr_last_cuda_error(void);
 
 /* Bytes of a scale-byte buffer for [rows, D] in the given layout
  * (0 for invalid arguments). */
@@ -185,16 +201,21 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k);
  *                selection only, or NULL for none (ignored in RAW mode)
  *   k            experts per token, 1 <= k <= min(16, N)
  *   routed_scaling  multiplies the renormalised weights
- *   flags        0 or NVR_FLAG_RAW_LOGITS
+ *   flags        0 or NVR_FLAG_RAW_LOGITS, optionally with one kernel-choice
+ *                flag (FORCE_TENSOR_CORE, FORCE_DECODE, SPLIT_K_2/4/8,
+ *                SPLIT_N) and, with a tensor-core choice, TEST_STALL
  *   out_ids      out [T, k] int32: expert ids, best first (key descending,
  *                equal keys: lower id first)
  *   out_w        out [T, k] fp32: routed_scaling * s_id / sum of the k
  *                selected sigmoid scores s (RAW: the selected logits)
  *   workspace    router_gate_workspace_size(T, D, N, k) bytes, zeroed once
  *
- * The logits never leave the chip on the tensor-core path: they are consumed
- * from tensor memory by the epilogue.  Small batches (decode) run as a single
- * kernel launch; larger ones as amax, quantize and GEMM+top-k launches.
+ * Small batches (decode) run as a single kernel launch.  Larger ones run as
+ * amax, quantize, GEMM and epilogue launches (programmatic dependent launch
+ * chains them without host involvement): with up to 256 experts the K-split
+ * fp32 partial logits pass through the workspace (L2-resident) to the
+ * epilogue kernel; wider heads consume the logits from tensor memory in the
+ * GEMM kernel itself.
  */
 nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
                             const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,
@@ -236,8 +257,9 @@ nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int64_t T, int6
  * router_gate_topk, writing the fp32 logits [T, N] (row-major,
  * logit = acc * gsa_x * gsa_w) instead of the epilogue's outputs.  Used to
  * check the GEMM on its own and to measure what writing logits to memory
- * costs.  flags: 0, NVR_FLAG_FORCE_TENSOR_CORE or NVR_FLAG_FORCE_DECODE
- * (RAW_LOGITS is invalid here).  Workspace as for router_gate_topk.
+ * costs.  flags: 0 or one kernel-choice flag (FORCE_TENSOR_CORE,
+ * FORCE_DECODE, SPLIT_K_2/4/8, SPLIT_N); RAW_LOGITS and TEST_STALL are
+ * invalid here.  Workspace as for router_gate_topk.
  */
 nvr_status router_gate_logits(const void* x, nvr_dtype dt, int64_t T, int64_t D,
                               const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,

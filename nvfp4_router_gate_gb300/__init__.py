@@ -24,12 +24,14 @@ import torch
 
 from . import _native
 from ._native import (NVR_FLAG_FORCE_DECODE, NVR_FLAG_FORCE_TENSOR_CORE, NVR_FLAG_RAW_LOGITS,
+                      NVR_FLAG_SPLIT_K_2, NVR_FLAG_SPLIT_K_4, NVR_FLAG_SPLIT_K_8, NVR_FLAG_SPLIT_N,
                       RouterError)
 
 __all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits",
            "router_gate_workspace_size", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
            "nvr_read_device_status", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
-           "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "new_workspace"]
+           "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "NVR_FLAG_SPLIT_K_2",
+           "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "new_workspace"]
 
 _LAYOUTS = {"linear": _native.NVR_SF_LINEAR, "tiled": _native.NVR_SF_TILED}
 

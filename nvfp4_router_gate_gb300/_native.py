@@ -26,6 +26,10 @@ NVR_SF_TILED = 1
 NVR_FLAG_RAW_LOGITS = 1
 NVR_FLAG_FORCE_TENSOR_CORE = 2
 NVR_FLAG_FORCE_DECODE = 4
+NVR_FLAG_SPLIT_K_2 = 8
+NVR_FLAG_SPLIT_K_4 = 16
+NVR_FLAG_SPLIT_K_8 = 32
+NVR_FLAG_SPLIT_N = 64
 NVR_FLAG_TEST_STALL = 1 << 30
 
 _p = ctypes.c_void_p
@@ -38,6 +42,7 @@ _f32 = ctypes.c_float
 # name -> (restype, argtypes); the same list the header declares
 SIGNATURES = {
     "nvr_status_string": (ctypes.c_char_p, [_i32]),
+    "nvr_last_cuda_error": (ctypes.c_char_p, []),
     "nvr_sf_bytes": (_sz, [_i64, _i64, _i32]),
     "nvfp4_quantize_workspace_size": (_sz, [_i64, _i64]),
     "nvfp4_quantize_act": (_i32, [_p, _i32, _i64, _i64, _p, _p, _i32, _p, _p, _sz, _p]),
@@ -79,7 +84,10 @@ def status_string(code):
 class RouterError(RuntimeError):
     def __init__(self, fn, code):
         self.code = int(code)
-        super().__init__("%s failed: %s (status %d)" % (fn, status_string(code), int(code)))
+        msg = "%s failed: %s (status %d)" % (fn, status_string(code), int(code))
+        if self.code == NVR_ERR_CUDA:
+            msg += ": " + lib().nvr_last_cuda_error().decode()
+        super().__init__(msg)
 
 
 def check(fn, code):

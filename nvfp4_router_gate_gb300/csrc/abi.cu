@@ -75,11 +75,27 @@ WsLayout router_ws_layout(int64_t T, int64_t D, int64_t N) {
   L.x_sf = a256(L.x_codes + static_cast<size_t>(rows_pad) * (D / 2));
   L.partials = a256(L.x_sf + static_cast<size_t>(rows_pad) * (D / 16));
   const int splits = split_bound(m_tiles, n_tiles);
-  const size_t part = splits > 1 ? static_cast<size_t>(m_tiles) * splits * 128 * kMaxKmax * 16 : 0;
+  size_t part = splits > 1 ? static_cast<size_t>(m_tiles) * splits * 128 * kMaxKmax * 16 : 0;
+  if (N <= 256) {
+    const size_t pk = splitk_partial_rows(T) * 256 * 4;   // K-split partial logits
+    if (pk > part) part = pk;
+  }
   L.decode = a256(L.partials + part);
   const size_t dec = T <= 16 ? static_cast<size_t>(T) * N * 8 : 0;
   L.total = a256(L.decode + dec);
   return L;
+}
+
+}  // namespace nvr
+
+namespace nvr {
+
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+nvr_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return NVR_OK;
+  g_last_cuda_error = e;
+  return NVR_ERR_CUDA;
 }
 
 }  // namespace nvr
@@ -138,11 +154,11 @@ nvr_status quantize_impl(const void* x, nvr_dtype dt, int64_t rows, int64_t D, u
                                    reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), gsa, qrec,
                                    reinterpret_cast<uint32_t*>(w + kWsStatus), sms, s);
   prof.after();
-  if (e != cudaSuccess) return NVR_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   prof.before();
   e = launch_quantize(x, bf16, rows, D, layout == NVR_SF_TILED, qrec, codes, sf, s);
   prof.after();
-  return e == cudaSuccess ? NVR_OK : NVR_ERR_CUDA;
+  return cuda_status(e);
 }
 
 nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
@@ -153,11 +169,18 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   if (st != NVR_OK) return st;
   if (!W_fp4 || !W_sf || !w_gsa || N <= 0 || N > (1 << 28)) return NVR_ERR_INVALID_ARG;
   if (!logits && (!out_ids || !out_w || k < 1 || k > kMaxKmax || k > N)) return NVR_ERR_INVALID_ARG;
+  constexpr uint32_t kKernelFlags = NVR_FLAG_SPLIT_K_2 | NVR_FLAG_SPLIT_K_4 | NVR_FLAG_SPLIT_K_8 | NVR_FLAG_SPLIT_N;
   if (flags & ~static_cast<uint32_t>(NVR_FLAG_RAW_LOGITS | NVR_FLAG_FORCE_TENSOR_CORE | NVR_FLAG_FORCE_DECODE |
-                                     NVR_FLAG_TEST_STALL))
+                                     kKernelFlags | NVR_FLAG_TEST_STALL))
     return NVR_ERR_INVALID_ARG;
+  const uint32_t kernel_flags = flags & kKernelFlags;
+  if (kernel_flags & (kernel_flags - 1)) return NVR_ERR_INVALID_ARG;          // at most one
+  if (kernel_flags) flags |= NVR_FLAG_FORCE_TENSOR_CORE;
   if ((flags & NVR_FLAG_FORCE_TENSOR_CORE) && (flags & NVR_FLAG_FORCE_DECODE)) return NVR_ERR_INVALID_ARG;
   if ((flags & NVR_FLAG_TEST_STALL) && !(flags & NVR_FLAG_FORCE_TENSOR_CORE)) return NVR_ERR_INVALID_ARG;
+  const int forced_split = (flags & NVR_FLAG_SPLIT_K_2) ? 2 : (flags & NVR_FLAG_SPLIT_K_4) ? 4
+                           : (flags & NVR_FLAG_SPLIT_K_8) ? 8 : 0;
+  if (forced_split && N > 256) return NVR_ERR_UNSUPPORTED;
   if (!aligned16(W_fp4) || !aligned16(W_sf) || (reinterpret_cast<uintptr_t>(w_gsa) & 3u) ||
       (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
       (out_ids && (reinterpret_cast<uintptr_t>(out_ids) & 3u)) ||
@@ -189,30 +212,60 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
                                   out_ids, out_w, logits, keys, scores,
                                   reinterpret_cast<uint32_t*>(w + kWsDecodeTicket), dp, s);
     prof.after();
-    return e == cudaSuccess ? NVR_OK : NVR_ERR_CUDA;
+    return cuda_status(e);
   }
   float* x_gsa = reinterpret_cast<float*>(w + L.scalars);
   float* qrec = x_gsa + 4;                                        // {gsa, 1/gsa, mode, amax}
   uint8_t* xc = w + L.x_codes;
   uint8_t* xsf = w + L.x_sf;
+  uint32_t* status = reinterpret_cast<uint32_t*>(w + kWsStatus);
+  const bool stall = (flags & NVR_FLAG_TEST_STALL) != 0;
   ProfileScope prof(s);
   prof.before();
   cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
-                                   reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec,
-                                   reinterpret_cast<uint32_t*>(w + kWsStatus), sms, s);
+                                   reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec, status, sms, s);
   prof.after();
-  if (e != cudaSuccess) return NVR_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
+  // Up to 256 experts: K split over S CTAs with one tensor-core accumulator
+  // for the whole row each, then the epilogue kernel; bf16 activations are
+  // quantized inside the GEMM.  Wider heads: N tiles split across CTAs with a
+  // top-k merge, after the standalone quantize kernel.
+  const int split_k = forced_split                        ? forced_split
+                      : (flags & NVR_FLAG_SPLIT_N) || N > 256 ? 0
+                                                              : plan_splitk(T, D, sms);
+  float* partials = reinterpret_cast<float*>(w + L.partials);
+  if (split_k > 0 && bf16) {
+    prof.before();
+    st = launch_fused_qgemm(static_cast<const uint16_t*>(x), qrec, T, D, W_fp4, W_sf, N, partials, status, split_k,
+                            stall, s);
+    prof.after();
+    if (st != NVR_OK) return st;
+    prof.before();
+    st = launch_router_epilogue(partials, split_k, x_gsa, w_gsa, T, N, bias, k, routed_scaling, raw, out_ids,
+                                out_w, logits, s);
+    prof.after();
+    return st;
+  }
   prof.before();
   e = launch_quantize(x, bf16, T, D, true, qrec, xc, xsf, s);
   prof.after();
-  if (e != cudaSuccess) return NVR_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
+  if (split_k > 0) {
+    prof.before();
+    st = launch_splitk_gemm(xc, xsf, T, D, W_fp4, W_sf, N, partials, status, split_k, stall, s);
+    prof.after();
+    if (st != NVR_OK) return st;
+    prof.before();
+    st = launch_router_epilogue(partials, split_k, x_gsa, w_gsa, T, N, bias, k, routed_scaling, raw, out_ids,
+                                out_w, logits, s);
+    prof.after();
+    return st;
+  }
   const GemmPlan g = plan_gemm(T, N, sms);
   prof.before();
   st = launch_gemm_topk(xc, xsf, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
                         out_ids, out_w, logits, reinterpret_cast<float4*>(w + L.partials),
-                        reinterpret_cast<uint32_t*>(w + L.tickets),
-                        reinterpret_cast<uint32_t*>(w + kWsStatus), g,
-                        (flags & NVR_FLAG_TEST_STALL) != 0, s);
+                        reinterpret_cast<uint32_t*>(w + L.tickets), status, g, stall, s);
   prof.after();
   return st;
 }
@@ -220,6 +273,8 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
 }  // namespace
 
 extern "C" {
+
+const char* nvr_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
 const char* nvr_status_string(nvr_status s) {
   switch (s) {
@@ -274,6 +329,10 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k) {
       const size_t v = static_cast<size_t>(m) * sp * 128 * kMaxKmax * 16;
       if (v > part) part = v;
     }
+  }
+  if (N <= 256) {
+    const size_t pk = splitk_partial_rows(T_max) * 256 * 4;   // monotone in T
+    if (pk > part) part = pk;
   }
   const int64_t t_dec = T_max < 16 ? T_max : 16;
   return quantize_ws_layout(T_max, D).total + static_cast<size_t>(m_max) * 4 +

@@ -1,0 +1,445 @@
+// gemm_fused.cu -- the router for up to 256 experts on bf16 activations: the
+// runtime NVFP4 quantization of x runs inside the K-split tensor-core GEMM,
+// so the quantized activations never exist in memory (sm_103a).
+//
+// Source: "nvfp4-megamoe-kernel commit 04cf8ca: dsv4/layers/router.py"
+// (runtime gsa = max|x| / 2688, NVFP4 activations and gate weight, gate GEMM
+// on Blackwell tensor cores).  Quantization arithmetic as in the standalone
+// quantizer (quant_block16): y = RN(x / gsa), sy = RN(max|y| / 6), E4M3 scale,
+// E2M1 codes of RN(y / scale) with the input's sign; identical codes.
+//
+// Per CTA (tile m of 128 tokens, K-split rank r of S, 320 threads):
+//   warp 0     TMA producer: per stage of 256 K-elements two bf16 x boxes
+//              (128 rows x 128 elements, 32 KB each) into a 3-slot ring, and
+//              the W tile (128 or 256 rows x 128 bytes, 128-byte swizzle) with
+//              its scale slabs into a 2-deep ring;
+//   warps 2-9  quantizers: each warp takes 16 token rows of a box, two rows
+//              per instruction (lanes 0-15 and 16-31); lane l holds 8 bf16 --
+//              half of a 16-element block, whose max comes from lane l ^ 1 by
+//              one shuffle -- and writes 4 bytes of codes into the A tile
+//              (128-byte swizzle, the layout TMA would have produced) and the
+//              block's scale byte into the stage's scale atoms.  Warps 2-5 then
+//              copy the x and W scale atoms into their tensor-memory quarter
+//              (tcgen05.st) and signal the MMA warp; the A tile is
+//              double-buffered;
+//   warp 1     MMA issuer: one tcgen05.mma.kind::mxf4nvf4 (M=128, N=128 or 256,
+//              K=64) per 64-element K step into one fp32 accumulator;
+//   warps 2-9  after the last MMA: TMA store of the fp32 partial (as in
+//              gemm_splitk.cu); the epilogue kernel there finishes the router.
+// Tensor memory: accumulator at columns 0-255; scales of A slot a at
+// 256 + 48 a (x: 4 columns per K step, W: 8).
+#include "nvr_splitk.cuh"
+
+namespace nvr {
+
+namespace {
+
+constexpr int kFStagesW = 2;
+constexpr int kFWTile = 256 * 128;                  // up to 256 W rows x 128 bytes
+constexpr int kFSfb = 2 * 4 * 512;                  // 4 atoms per 128-expert half
+constexpr int kFWStage = kFWTile + kFSfb;
+constexpr int kFXSlots = 3;
+constexpr int kFXBox = 128 * 128 * 2;               // 128 rows x 128 bf16
+constexpr int kFASlots = 2;
+constexpr int kFACodes = 128 * 128;                 // 128 token rows x 128 bytes of codes
+constexpr int kFASfa = 4 * 512;                     // 4 scale atoms
+constexpr int kFASlot = kFACodes + kFASfa;
+constexpr int kFWRing = kFStagesW * kFWStage;
+constexpr int kFXRing = kFXSlots * kFXBox;
+constexpr int kFARing = kFASlots * kFASlot;
+constexpr int kFSmem = kFWRing + kFXRing + kFARing + 2048 /*scale table, barriers*/ + 1024 /*align*/;
+constexpr int kFThreads = 320;
+constexpr int kFRowsPerWarp = 16;
+static_assert(kFWStage % 1024 == 0 && kFASlot % 1024 == 0 && kFXBox % 1024 == 0, "1024-byte aligned tiles");
+static_assert(8 * 8192 <= kFXRing, "store staging fits the x ring");
+
+struct FusedParams {
+  CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
+  CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 x (128 * n_half)
+  CUtensorMap tmap_p;          // partials [S][T][256] fp32, box 32 x 32 x 1
+  const float* qrec;           // quantizer record {gsa, 1/gsa, mode, amax} from the amax kernel
+  const uint8_t* sfb;          // W scales, tile layout
+  int T, D, n_half, S;
+  uint32_t* status;
+  int test_stall;              // test hook: the MMA issuer issues nothing
+};
+
+__device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" :: "r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_u8(uint8_t* p, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" :: "r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// Quantize kG rows of one stage, 8 bf16 values (half of a 16-element block;
+// the other half sits in lane ^ 1) per row and lane.  The rows are
+// independent and the code is branch-free, so their dependency chains
+// interleave.  kMode: 1 = division shortcut (gsa and 1/gsa in [2^-80, 2^80]),
+// 2 = IEEE division.  Writes each row's 4 packed code bytes to codes[] and the
+// block's E4M3 scale byte to bytes[].  s_scale[b] = (dec(b), RN(1/dec(b))).
+template <int kMode, int kG>
+__device__ __forceinline__ void quant_rows(const uint4 (&v)[kG], const QuantScale& qs, const float2* s_scale,
+                                           uint32_t (&codes)[kG], uint32_t (&bytes)[kG]) {
+  const float r6 = 0.16666667163372039794921875f;       // RN(1/6)
+  float x[kG][8];
+  float mx[kG];
+#pragma unroll
+  for (int i = 0; i < kG; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[i][2 * j] = __uint_as_float(w[j] << 16);
+      x[i][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    mx[i] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx[i] = fmaxf(mx[i], fabsf(x[i][j]));
+  }
+#pragma unroll
+  for (int i = 0; i < kG; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xFFFFFFFFu, mx[i], 1));
+  const uint64_t ng2 = f2_pack(-qs.gsa, -qs.gsa), rg2 = f2_pack(qs.rgsa, qs.rgsa);
+#pragma unroll
+  for (int i = 0; i < kG; ++i) {
+    // max|y| = RN(max|x| / gsa): rounding is monotone
+    const float ymax = kMode == 1 ? div_rn(mx[i], qs.gsa, qs.rgsa) : __fdiv_rn(mx[i], qs.gsa);
+    bytes[i] = e4m3_byte(div_rn_short(ymax, 6.0f, r6));
+    const float2 sr = s_scale[bytes[i]];
+    const uint64_t ns2 = f2_pack(-sr.x, -sr.x), rs2 = f2_pack(sr.y, sr.y);
+    float z[8];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const uint64_t y = kMode == 1 ? div_rn2(f2_pack(x[i][j], x[i][j + 1]), ng2, rg2)
+                                    : f2_pack(__fdiv_rn(x[i][j], qs.gsa), __fdiv_rn(x[i][j + 1], qs.gsa));
+      const uint64_t q = div_rn2_short(y, ns2, rs2);
+      z[j] = f2_lo(q);
+      z[j + 1] = f2_hi(q);
+    }
+    const uint32_t c = e2m1_pack8(z[0], z[1], z[2], z[3], z[4], z[5], z[6], z[7]) |
+                       bf16x8_sign_nibbles(v[i].x, v[i].y, v[i].z, v[i].w);
+    codes[i] = bytes[i] ? c : 0u;                       // a zero scale byte: all codes 0
+  }
+}
+
+__global__ void __launch_bounds__(kFThreads, 1)
+fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* wring = smem;
+  uint8_t* xring = wring + kFWRing;
+  uint8_t* aring = xring + kFXRing;
+  float2* s_scale = reinterpret_cast<float2*>(aring + kFARing);        // [128] (dec(b), RN(1/dec(b)))
+  uint64_t* full_w = reinterpret_cast<uint64_t*>(s_scale + 128);
+  uint64_t* empty_w = full_w + kFStagesW;
+  uint64_t* full_x = empty_w + kFStagesW;
+  uint64_t* empty_x = full_x + kFXSlots;
+  uint64_t* a_full = empty_x + kFXSlots;
+  uint64_t* a_empty = a_full + kFASlots;
+  uint64_t* acc_full = a_empty + kFASlots;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  // producer: ring slots with a fill in flight and the parity of their latest fill
+  uint32_t filled_w = 0, bits_w = 0, filled_x = 0, bits_x = 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x / p.S;
+  const int rank = blockIdx.x - m_tile * p.S;
+  const int KB = p.D / kBlock;
+  const int n_st = (KB + 15) / 16;                   // stages of 256 K-elements
+  const int st0 = (rank * n_st) / p.S;
+  const int my_st = ((rank + 1) * n_st) / p.S - st0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kFStagesW; ++s) { mbar_init(full_w + s, 1); mbar_init(empty_w + s, 1); }
+    for (int s = 0; s < kFXSlots; ++s) { mbar_init(full_x + s, 1); mbar_init(empty_x + s, 8); }
+    for (int a = 0; a < kFASlots; ++a) { mbar_init(a_full + a, 4); mbar_init(a_empty + a, 1); }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&p.tmap_x);
+    tma_prefetch_map(&p.tmap_b);
+    tma_prefetch_map(&p.tmap_p);
+  }
+  if (threadIdx.x < 128) {
+    const uint32_t b = threadIdx.x;
+    const bool ok = b >= 1 && b <= 126;
+    s_scale[b] = make_float2(ok ? e4m3_value(b) : 0.0f, ok ? __frcp_rn(e4m3_value(b)) : 0.0f);
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // the amax kernel before us (programmatic launch) must have finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint64_t deadline = globaltimer_ns() + 1000000000ull;   // 1 s
+
+  bool acc_ok = true;     // quantizer warps: the accumulator is complete
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int wst = 0;
+    uint32_t wph = 0;
+    bool ok = true;
+    for (int s = 0; s < my_st && ok; ++s) {
+      const int ks = st0 + s;
+      // the stage's two x boxes (a box past D or T reads zeros)
+      for (int hs = 0; hs < 2; ++hs) {
+        const int xi = 2 * s + hs, xs = xi % kFXSlots;
+        const uint32_t xph = (xi / kFXSlots) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_x + xs, xph ^ 1u, deadline, abort_flag))) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          mbar_arrive_expect_tx(full_x + xs, kFXBox);
+          tma_load_2d(xring + xs * kFXBox, &p.tmap_x, ks * 256 + hs * 128, m_tile * 128, full_x + xs);
+        }
+        __syncwarp();
+        filled_x |= 1u << xs;
+        bits_x = (bits_x & ~(1u << xs)) | (xph << xs);
+      }
+      if (!ok) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_w + wst, wph ^ 1u, deadline, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const int nkk = min(4, KB / 4 - 4 * ks);
+      uint8_t* b = wring + wst * kFWStage;
+      uint8_t* sb = b + kFWTile;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(full_w + wst, static_cast<uint32_t>(p.n_half * (128 * 128 + 512 * nkk)));
+        tma_load_2d(b, &p.tmap_b, ks * 128, 0, full_w + wst);
+        for (int h = 0; h < p.n_half; ++h)
+          bulk_load(sb + h * 2048, p.sfb + (static_cast<size_t>(h) * (KB / 4) + 4 * ks) * 512, 512u * nkk,
+                    full_w + wst);
+      }
+      __syncwarp();
+      filled_w |= 1u << wst;
+      bits_w = (bits_w & ~(1u << wst)) | (wph << wst);
+      if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
+    }
+    if (!ok && lane == 0) {
+      report_timeout(p.status);
+      *abort_flag = 1;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (!p.test_stall) {
+      const uint32_t idesc = idesc_mxf4nvf4(128, 128 * p.n_half);
+      int wst = 0;
+      uint32_t wph = 0;
+      bool ok = true;
+      for (int s = 0; s < my_st; ++s) {
+        const int slot = s & 1;
+        const uint32_t aph = (s >> 1) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(a_full + slot, aph, deadline, abort_flag) &&
+                                         mbar_wait(full_w + wst, wph, deadline, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int ks = st0 + s;
+        const int nkk = min(4, KB / 4 - 4 * ks);
+        const uint8_t* a = aring + slot * kFASlot;
+        const uint8_t* b = wring + wst * kFWStage;
+        const uint32_t sf_t = tmem + 256 + slot * 48;
+        if (elect_one()) {
+          for (int kk = 0; kk < nkk; ++kk)
+            tc_mma_nvf4(tmem, desc_kmajor_sw128(smem_u32(a + 32 * kk)), desc_kmajor_sw128(smem_u32(b + 32 * kk)),
+                        idesc, sf_t + 4 * kk, sf_t + 16 + 8 * kk, (s | kk) != 0);
+          tc_commit(empty_w + wst);
+          tc_commit(a_empty + slot);
+        }
+        __syncwarp();
+        if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
+      }
+      if (ok && my_st > 0 && elect_one()) tc_commit(acc_full);
+      __syncwarp();
+      if (!ok && lane == 0) {
+        report_timeout(p.status);
+        *abort_flag = 1;
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- quantizers
+    QuantScale qs;
+    qs.gsa = __ldg(p.qrec);
+    qs.rgsa = __ldg(p.qrec + 1);
+    qs.mode = __float_as_int(__ldg(p.qrec + 2));
+    const int qw = warp - 2;
+    const int sub = lane >> 4, l16 = lane & 15;       // row of the pair, lane within the row
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int wst = 0;
+    uint32_t wph = 0;
+    bool ok = true;
+    for (int s = 0; s < my_st; ++s) {
+      const int slot = s & 1;
+      const uint32_t aph = (s >> 1) & 1;
+      // All quantizer warps agree (one barrier) that the slot is free -- its
+      // previous MMAs completed -- and that no warp has failed so far.
+      ok = bar_and(2, 256, ok && mbar_wait(a_empty + slot, aph ^ 1u, deadline, abort_flag));
+      if (!ok) break;
+      uint8_t* ac = aring + slot * kFASlot;
+      uint8_t* asf = ac + kFACodes;
+      for (int hs = 0; hs < 2; ++hs) {
+        const int xi = 2 * s + hs, xs = xi % kFXSlots;
+        const uint32_t xph = (xi / kFXSlots) & 1;
+        const bool okx = __all_sync(0xFFFFFFFFu, mbar_wait(full_x + xs, xph, deadline, abort_flag));
+        ok = ok && okx;
+        if (okx) {
+          const uint8_t* xb = xring + xs * kFXBox;
+#pragma unroll
+          for (int g = 0; g < kFRowsPerWarp / 2; g += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
+            uint32_t codes[4], bytes[4];
+            if (qs.mode == 1) {
+              quant_rows<1, 4>(v, qs, s_scale, codes, bytes);
+            } else if (qs.mode == 2) {
+              quant_rows<2, 4>(v, qs, s_scale, codes, bytes);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) { codes[i] = 0u; bytes[i] = 0u; }
+            }
+            const int j = 4 * hs + (l16 >> 2);                     // 16-byte chunk of the code row
+            const int c = 8 * hs + (l16 >> 1);                     // 16-element block of the stage
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = qw * kFRowsPerWarp + 2 * (g + i) + sub;
+              // codes: 4 bytes at chunk j ^ (r % 8), offset 4 * (l16 % 4) (128-byte swizzle)
+              st_shared_u32(ac + r * 128 + (((j ^ (r & 7)) << 4) | ((l16 & 3) << 2)), codes[i]);
+              // scale byte of block c: atom c/4, line r % 32, group (r/32) % 4, byte c % 4
+              if (!(l16 & 1))
+                st_shared_u8(asf + 512 * (c >> 2) + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (c & 3), bytes[i]);
+            }
+          }
+        }
+        // this warp has read its rows of the box
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_x + xs);
+      }
+      // the MMA reads the codes through the async proxy
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 2, 256;" ::: "memory");
+      if (warp < 6) {
+        // ---- scale stagers: x and W scale atoms into this warp's quarter
+        const bool okw = __all_sync(0xFFFFFFFFu, mbar_wait(full_w + wst, wph, deadline, abort_flag));
+        if (okw) {
+          const uint8_t* sb = wring + wst * kFWStage + kFWTile;
+          uint32_t va[16], vb0[16], vb1[16];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint4 t = ld_shared_v4(asf + 512 * kk + 16 * lane);
+            va[4 * kk] = t.x; va[4 * kk + 1] = t.y; va[4 * kk + 2] = t.z; va[4 * kk + 3] = t.w;
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            uint32_t* dst = kk < 2 ? vb0 : vb1;
+            const int o = 8 * (kk & 1);
+            const uint4 t0 = ld_shared_v4(sb + 512 * kk + 16 * lane);
+            const uint4 t1 = ld_shared_v4(sb + 2048 + 512 * kk + 16 * lane);
+            dst[o] = t0.x; dst[o + 1] = t0.y; dst[o + 2] = t0.z; dst[o + 3] = t0.w;
+            dst[o + 4] = t1.x; dst[o + 5] = t1.y; dst[o + 6] = t1.z; dst[o + 7] = t1.w;
+          }
+          const uint32_t t0 = tmem + lane_base + 256 + slot * 48;
+          tmem_store16(t0, va);
+          tmem_store16(t0 + 16, vb0);
+          tmem_store16(t0 + 32, vb1);
+          tmem_store_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(a_full + slot);
+        }
+        ok = ok && okw;
+      }
+      if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
+    }
+    if (!ok && threadIdx.x == 64) {
+      report_timeout(p.status);
+      *abort_flag = 1;
+    }
+    // --------------------------------------------- wait for the accumulator
+    if (my_st > 0) {
+      acc_ok = bar_and(1, 256, mbar_wait(acc_full, 0, deadline, abort_flag));
+      if (!acc_ok && threadIdx.x == 64) {
+        report_timeout(p.status);
+        *abort_flag = 1;
+      }
+    }
+    tc_fence_after();
+    // every x box has been read (the last MMA needed them all): the x ring
+    // stages the stores
+    store_partial_tile(&p.tmap_p, xring, tmem, warp, lane, m_tile, rank, p.n_half, p.T, my_st > 0 && acc_ok);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (*abort_flag && threadIdx.x == 0) {
+    // After an abort, copies may still be landing in this CTA's shared
+    // memory: wait (bounded) for the latest fill of every ring slot.
+    const uint64_t drain = globaltimer_ns() + 1000000000ull;
+    for (int s = 0; s < kFStagesW; ++s)
+      while (((filled_w >> s) & 1u) && !mbar_try_wait(full_w + s, (bits_w >> s) & 1u))
+        if (globaltimer_ns() > drain) break;
+    for (int s = 0; s < kFXSlots; ++s)
+      while (((filled_x >> s) & 1u) && !mbar_try_wait(full_x + s, (bits_x >> s) & 1u))
+        if (globaltimer_ns() > drain) break;
+  }
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// bf16 activations [T, D]: 128 x 128 boxes, no swizzle, zeros outside.
+bool encode_x(CUtensorMap* map, const uint16_t* ptr, int64_t T, int64_t D) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(ptr), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+nvr_status launch_fused_qgemm(const uint16_t* x, const float* qrec, int64_t T, int64_t D, const uint8_t* W_codes,
+                              const uint8_t* W_sf, int64_t N, float* partials, uint32_t* status, int S,
+                              bool test_stall, cudaStream_t s) {
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVR_ERR_CUDA;
+  if (N > 256 || S < 1 || S > kMaxSplitK) return NVR_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(S) * static_cast<size_t>((T + 127) / 128 * 128) > splitk_partial_rows(T))
+    return NVR_ERR_UNSUPPORTED;
+  if (!attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(fused_qgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+    if (e != cudaSuccess) return cuda_status(e);
+    attr_set[dev] = true;
+  }
+  FusedParams g;
+  const int n_half = N > 128 ? 2 : 1;
+  if (!encode_x(&g.tmap_x, x, T, D)) return NVR_ERR_UNSUPPORTED;
+  if (!encode_codes(&g.tmap_b, W_codes, N, D, 128u * n_half)) return NVR_ERR_UNSUPPORTED;
+  if (!encode_partials(&g.tmap_p, partials, T, S)) return NVR_ERR_UNSUPPORTED;
+  g.qrec = qrec; g.sfb = W_sf;
+  g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.n_half = n_half; g.S = S;
+  g.status = status; g.test_stall = test_stall ? 1 : 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((T + 127) / 128 * S));
+  cfg.blockDim = dim3(kFThreads);
+  cfg.dynamicSmemBytes = kFSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_status(cudaLaunchKernelEx(&cfg, fused_qgemm_kernel, g));
+}
+
+}  // namespace nvr

@@ -569,7 +569,7 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
   else if (k <= 4) e = launch_k<4>(p, grid, s);
   else if (k <= 8) e = launch_k<8>(p, grid, s);
   else e = launch_k<16>(p, grid, s);
-  return e == cudaSuccess ? NVR_OK : NVR_ERR_CUDA;
+  return cuda_status(e);
 }
 
 }  // namespace nvr

@@ -91,6 +91,28 @@ __device__ __forceinline__ uint64_t div_rn2(uint64_t a2, uint64_t nb2, uint64_t 
   return f2_fma(r, rb2, q);
 }
 
+// Division by a divisor with a short significand: b = d * 2^k with d an odd
+// integer <= 15 (every E4M3 scale value, and 6).  Then ONE correction gives
+// RN(a/b): q0 = RN(a*rb) is within 2 ulp of a/b; c = q0 + (a - b*q0)*rb
+// (residual exact under a fused multiply-add, one rounding in the final fma)
+// differs from a/b by at most |a/b - q0| * 2^-24 < 2^-23 ulp.  RN(c) can only
+// differ from RN(a/b) if a rounding midpoint M lies within that distance of
+// a/b; but a*2^-k - M*d is a nonzero multiple of ulp/2 (a*2^-k lies on a grid
+// no finer than ulp(a/b), while M*d is an odd multiple of ulp/2), so
+// |a/b - M| >= ulp/(2d) >= ulp/30.  Hypotheses as for div_rn (no overflow,
+// a/b not subnormal); a subnormal quotient is < 0.25 and encodes as a signed
+// zero whatever its last bits.
+__device__ __forceinline__ float div_rn_short(float a, float b, float rb) {
+  const float q = __fmul_rn(a, rb);
+  const float r = __fmaf_rn(-q, b, a);
+  return __fmaf_rn(r, rb, q);
+}
+__device__ __forceinline__ uint64_t div_rn2_short(uint64_t a2, uint64_t nb2, uint64_t rb2) {
+  const uint64_t q = f2_mul(a2, rb2);
+  const uint64_t r = f2_fma(q, nb2, a2);
+  return f2_fma(r, rb2, q);
+}
+
 // ------------------------------------------------------- format conversions
 // E4M3 byte of a non-negative fp32 (nearest-even, saturating at 448).
 __device__ __forceinline__ uint32_t e4m3_byte(float v) {
@@ -178,11 +200,11 @@ __device__ __forceinline__ uint32_t f32x8_sign_nibbles(const float* v) {
 //   y_i = RN(x_i / gsa); sy = RN(max|y| / 6); byte = E4M3(sy);
 //   code_i = E2M1(RN(y_i / dec(byte))) with the sign of x_i (a negative value
 //   that rounds to zero is -0, code 0x8); byte == 0 -> all codes 0.
-// Exactness of the division shortcut: y_i is exact whenever |x_i| >= 2^-100
+// Exactness of the division shortcuts: y_i is exact whenever |x_i| >= 2^-100
 // (mode 1) or always (mode 2).  When |x_i| < 2^-100, |y_i| < 2^-20 and
 // |y_i / s| < 2^-11 for every nonzero scale s >= 2^-9, so the code is the
-// signed zero whatever the last bits of y_i are.  max|y| / 6 and y / s use the
-// same shortcut with b = 6 or b = s in [2^-9, 448].
+// signed zero whatever the last bits of y_i are.  max|y| / 6 and y / s divide
+// by short significands (6 = 3 * 2, s = (8 + m) * 2^(e-10)): div_rn_short.
 // `rcp_tab`, when given, holds RN(1 / dec(b)) for every scale byte b in
 // 1..126 (the same bits __frcp_rn returns).
 __device__ __forceinline__ uint32_t quant_block16(const Block16& blk, const QuantScale& qs,
@@ -207,7 +229,7 @@ __device__ __forceinline__ uint32_t quant_block16(const Block16& blk, const Quan
 #pragma unroll
   for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(y[i]));
   const float r6 = 0.16666667163372039794921875f;       // RN(1/6)
-  const float sy = div_rn(m, 6.0f, r6);
+  const float sy = div_rn_short(m, 6.0f, r6);
   const uint32_t byte = e4m3_byte(sy);
   if (byte == 0) { codes_lo = codes_hi = 0; return 0; }
   const float s = e4m3_value(byte);
@@ -216,7 +238,7 @@ __device__ __forceinline__ uint32_t quant_block16(const Block16& blk, const Quan
   float q[16];
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    const uint64_t v = div_rn2(f2_pack(y[i], y[i + 1]), ns2, rs2);
+    const uint64_t v = div_rn2_short(f2_pack(y[i], y[i + 1]), ns2, rs2);
     q[i] = f2_lo(v);
     q[i + 1] = f2_hi(v);
   }

@@ -30,6 +30,10 @@ TensorMapEncodeFn tensor_map_encoder();
 // Number of SMs of the current device (cached per device); 0 on error.
 int device_sm_count();
 
+// NVR_OK for cudaSuccess, else NVR_ERR_CUDA; records the error for
+// nvr_last_cuda_error (per host thread).
+nvr_status cuda_status(cudaError_t e);
+
 struct GemmPlan {
   int m_tiles = 0, n_tiles = 0, n_splits = 1;
 };
@@ -53,7 +57,7 @@ struct WsLayout {
   size_t tickets = 0;        // m_tiles x u32
   size_t x_codes = 0;        // [rows_pad, D/2]
   size_t x_sf = 0;           // tile layout, rows_pad rows
-  size_t partials = 0;       // m_tiles x n_splits x 128 x kMaxKmax x float4
+  size_t partials = 0;       // N-split top-k lists, or the K-split fp32 partial logits
   size_t decode = 0;         // decode scratch: keys and scores [T, N] fp32
   size_t total = 0;
 };
@@ -77,6 +81,26 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
                             float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                             float* logits, float4* partials, uint32_t* tickets, uint32_t* status,
                             const GemmPlan& g, bool test_stall, cudaStream_t s);
+
+// Router for N <= 256: the GEMM split along K over S CTAs (fp32 partials in
+// the workspace), then the warp-per-token epilogue kernel.
+// splitk_partial_rows(T): rows (of 256 fp32) the partial region holds for T
+// tokens, an upper bound of S * T_pad for every S plan_splitk picks on a GPU
+// with at most 256 SMs; plan_splitk: S for T tokens.
+constexpr int kMaxSplitK = 16;
+size_t splitk_partial_rows(int64_t T);
+int plan_splitk(int64_t T, int64_t D, int num_sms);
+nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64_t T, int64_t D,
+                              const uint8_t* W_codes, const uint8_t* W_sf, int64_t N, float* partials,
+                              uint32_t* status, int S, bool test_stall, cudaStream_t s);
+// The same GEMM on bf16 activations, quantized inside the kernel from the
+// quantizer record qrec {gsa, 1/gsa, mode, amax} of the amax kernel.
+nvr_status launch_fused_qgemm(const uint16_t* x, const float* qrec, int64_t T, int64_t D, const uint8_t* W_codes,
+                              const uint8_t* W_sf, int64_t N, float* partials, uint32_t* status, int S,
+                              bool test_stall, cudaStream_t s);
+nvr_status launch_router_epilogue(const float* partials, int S, const float* x_gsa, const float* w_gsa,
+                                  int64_t T, int64_t N, const float* bias, int k, float routed_scaling,
+                                  bool raw, int32_t* out_ids, float* out_w, float* logits, cudaStream_t s);
 
 cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const uint8_t* W_codes,
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,

@@ -87,7 +87,16 @@ def test_host_argument_checks_without_gpu():
     st = L.router_gate_topk(fake, 7, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
                             fake, fake, fake, ws_n, None)
     assert st == nat.NVR_ERR_INVALID_ARG
-    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 64,
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 128,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    # two kernel-choice flags at once
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0,
+                            nat.NVR_FLAG_SPLIT_K_2 | nat.NVR_FLAG_SPLIT_N,
+                            fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0,
+                            nat.NVR_FLAG_SPLIT_K_4 | nat.NVR_FLAG_FORCE_DECODE,
                             fake, fake, fake, ws_n, None)
     assert st == nat.NVR_ERR_INVALID_ARG
     st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0,

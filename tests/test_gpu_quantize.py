@@ -82,6 +82,34 @@ def test_e2m1_rounding_boundaries():
     _check_exact(rows, to_device(rows, "f32"))
 
 
+def test_e2m1_boundaries_under_every_scale_mantissa():
+    """y / s next to every E2M1 midpoint for block scales with each of the
+    eight E4M3 significands (s = (8 + m) / 8 * 2^e): the quotient's last bit
+    decides the code, which pins the one-correction division by s."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    rows = []
+    for e in (-3, 0, 2):
+        for m in range(8):
+            s = np.float32((8 + m) / 8.0 * 2.0 ** e)
+            base = (mids.astype(np.float64) * float(s)).astype(np.float32)     # exact (<= 7 bits)
+            probes = [base]
+            for d in (1, 2, 3):
+                up, dn = base.copy(), base.copy()
+                for _ in range(d):
+                    up = np.nextafter(up, np.float32(np.inf))
+                    dn = np.nextafter(dn, np.float32(0))
+                probes += [up, dn]
+            p = np.concatenate(probes).astype(np.float32)
+            p = np.concatenate([p, -p])
+            blocks = _probe_block_rows(p, lead=np.float32(6.0) * s)
+            rows.append(blocks)
+    x = np.concatenate(rows)
+    amax_row = np.zeros((4, 64), np.float32)
+    amax_row[0, 0] = 2688.0                           # gsa = 1 (bigger than every lead)
+    x = np.concatenate([amax_row, x]).astype(np.float32)
+    _check_exact(x, to_device(x, "f32"))
+
+
 def test_e4m3_rounding_boundaries():
     """Block maxima whose sy = max/6 lands on and next to every E4M3 midpoint."""
     vals = formats.E4M3_TABLE[:0x7F]

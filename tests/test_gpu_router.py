@@ -23,6 +23,8 @@ sys.path.insert(0, os.path.join(os.path.dirname(os.path.abspath(__file__)), "gol
 
 TC = 2       # NVR_FLAG_FORCE_TENSOR_CORE
 DEC = 4      # NVR_FLAG_FORCE_DECODE
+K2, K4, K8 = 8, 16, 32   # NVR_FLAG_SPLIT_K_2/4/8: K split over that many CTAs
+SPN = 64     # NVR_FLAG_SPLIT_N: the N-split tensor-core kernel
 
 
 def _logits(case, flags):
@@ -34,6 +36,8 @@ def _logits(case, flags):
 
 @pytest.mark.parametrize("name,T,flags", [("tiny", 4, DEC), ("tiny", 4, TC), ("decode", 8, DEC),
                                           ("decode", 8, TC), ("prefill", 300, TC),
+                                          ("prefill", 300, K2), ("prefill", 300, K4),
+                                          ("prefill", 300, K8), ("prefill", 300, SPN),
                                           ("adversarial", 40, TC)])
 def test_logits_within_tolerance(name, T, flags):
     case = Case(WL.WORKLOADS[name].with_T(T))
@@ -58,7 +62,7 @@ def _grid_operands(rng, rows, D, amax_block):
     return x.astype(np.float32)
 
 
-@pytest.mark.parametrize("flags", [DEC, TC])
+@pytest.mark.parametrize("flags", [DEC, TC, K2, K4, K8, SPN])
 def test_exact_integer_logits(flags):
     """Grid-valued operands: products are multiples of 1/16 and every partial
     sum stays below 2**20 in magnitude, so any fp32 summation order is exact
@@ -227,7 +231,8 @@ def test_gpu_argument_errors():
         R.router_gate_topk(big, wf, wsf, case.w_gsa, None, k=1, flags=DEC)
 
 
-def test_bounded_wait_timeout_reports_status():
+@pytest.mark.parametrize("kflag", [TC, SPN])
+def test_bounded_wait_timeout_reports_status(kflag):
     """Failure detection without a GPU fault: with the test stall hook the
     tensor-core kernel's MMA issuer issues nothing, its pipeline waits run out
     after about a second, the kernel records NVR_ERR_TIMEOUT in the workspace
@@ -238,13 +243,148 @@ def test_bounded_wait_timeout_reports_status():
     case = Case(WL.WORKLOADS["decode"].with_T(8))
     ws = R.new_workspace(R.router_gate_workspace_size(8, 7168, 256, 8))
     R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5,
-                       workspace=ws, flags=TC | _native.NVR_FLAG_TEST_STALL)
+                       workspace=ws, flags=kflag | _native.NVR_FLAG_TEST_STALL)
     torch.cuda.synchronize()
     assert R.nvr_read_device_status(ws) == _native.NVR_ERR_TIMEOUT
     ws.zero_()
     ids, w = R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5,
-                                workspace=ws, flags=TC)
+                                workspace=ws, flags=kflag)
     torch.cuda.synchronize()
     assert R.nvr_read_device_status(ws) == 0
     res = case.check(ids.cpu().numpy(), w.cpu().numpy(), np.arange(8))
     assert compare.topk_ok(res), res
+
+
+# ---------------------------------------------------------------- kernel choices
+# Heads of up to 256 experts run on the K-split GEMM (S CTAs per 128-token
+# tile, fp32 partial logits summed by the epilogue kernel); S = 2, 4, 8 and
+# the N-split kernel are forced here on the same inputs.
+
+@pytest.mark.parametrize("flags", [K2, K4, K8, SPN])
+@pytest.mark.parametrize("T", [129, 300])
+def test_kernel_choices_all_rows(T, flags):
+    case = Case(WL.WORKLOADS["prefill"].with_T(T))
+    ids, w = case.run(flags)
+    res = case.check(ids, w, np.arange(T))
+    assert compare.topk_ok(res), res
+
+
+@pytest.mark.parametrize("flags", [K2, K4, K8])
+@pytest.mark.parametrize("k", [1, 3, 16])
+def test_split_k_k_values(flags, k):
+    """k = 1 (a plain arg-max), k = 3 and the largest k = 16."""
+    case = Case(WL.WORKLOADS["decode"].with_T(64).with_k(k))
+    ids, w = case.run(flags)
+    res = case.check(ids, w, np.arange(64))
+    assert compare.topk_ok(res), res
+
+
+@pytest.mark.parametrize("flags", [TC, K2, K4, K8])
+def test_split_k_ties_and_saturated_rows(flags):
+    """The adversarial rows on a 256-expert head: all-zero rows tie all 256
+    keys at 0.5 and saturated rows tie many at 1.0; lower ids must win every
+    tie."""
+    w = WL.Workload("adversarial_256", 512, 7168, 256, 8, 2.5, False, "bf16", "adversarial", 0.02, "zero")
+    case = Case(w)
+    ids, wt = case.run(flags)
+    res = case.check(ids, wt, np.arange(512))
+    assert compare.topk_ok(res), res
+    zero = np.arange(1, 512, 4)
+    assert np.all(ids[zero] == np.arange(8))
+    assert np.allclose(wt[zero], 2.5 / 8, atol=1e-6)
+
+
+@pytest.mark.parametrize("flags", [TC, K2, K8])
+def test_split_k_tie_probe(flags):
+    w = WL.Workload("tie_probe_256", 256, 7168, 256, 8, 2.5, False, "bf16", "adversarial", 0.02,
+                    "zero", tie_probe=True)
+    case = Case(w)
+    ids, wt = case.run(flags)
+    res = case.check(ids, wt, np.arange(256))
+    assert compare.topk_ok(res), res
+    for row in ids:
+        pos = {int(e): i for i, e in enumerate(row)}
+        for e, i in pos.items():
+            if e < 16 and e % 2 == 1 and (e - 1) in pos:
+                assert pos[e - 1] < i
+
+
+@pytest.mark.parametrize("flags", [K2, K4, K8])
+def test_split_k_raw_head(flags):
+    """RAW mode on a 200-expert head (the second 128-expert half is partial)."""
+    w = WL.Workload("raw_200", 64, 7168, 200, 8, 1.0, True, "bf16", "normal", 0.02, "none")
+    case = Case(w)
+    ids, wt = case.run(flags)
+    res = case.check(ids, wt, np.arange(64))
+    assert compare.topk_ok(res), res
+
+
+def test_split_k_flag_rejects_wide_heads():
+    import nvfp4_router_gate_gb300 as R
+    big = torch.zeros((32, 512), dtype=torch.bfloat16, device="cuda")
+    wf = torch.zeros((300, 256), dtype=torch.uint8, device="cuda")
+    wsf = torch.zeros(R.nvr_sf_bytes(300, 512, "tiled"), dtype=torch.uint8, device="cuda")
+    g = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(R.RouterError, match="unsupported"):
+        R.router_gate_topk(big, wf, wsf, g, None, k=8, flags=K4)
+
+
+# ------------------------------------------------ quantization inside the GEMM
+# bf16 activations on heads of up to 256 experts are quantized inside the GEMM
+# kernel; the codes never reach memory.  A one-hot gate weight makes every
+# logit a single product code_x * scale_x * gsa_x * (dequantized 1.0), so the
+# logits expose the kernel's code and scale of each probed x element.
+
+def _one_hot_gate(cols, D):
+    W = np.zeros((len(cols), D), np.float32)
+    W[np.arange(len(cols)), cols] = 1.0
+    return W
+
+
+def _fused_probe_x(rng, T, D):
+    """bf16 rows: half with gsa = 1 and crafted blocks (E2M1 midpoints times
+    each E4M3 significand, their bf16 neighbours, zeros, subnormals), half
+    random with per-token LogNormal scale."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    x = (rng.standard_normal((T, D)) * np.exp(rng.standard_normal((T, 1)))).astype(np.float32)
+    bits = WL.float32_to_bf16_bits(x)
+    for t in range(T // 2):
+        for b in range(D // 16):
+            m, e = (t + b) % 8, (b % 5) - 2
+            s = (8 + m) / 8.0 * 2.0 ** e
+            vals = np.zeros(16, np.float32)
+            vals[0] = 6.0 * s                                   # block scale exactly s
+            probe = mids[(b + np.arange(15)) % 7] * s * rng.choice([-1, 1], 15)
+            vals[1:] = probe
+            vb = WL.float32_to_bf16_bits(vals)
+            k = (t * 7 + b) % 4                                 # bf16 neighbours of the ties
+            vb[1:8] = (vb[1:8].astype(np.int32) + [0, 1, -1, 2, -2, 0, k][:7]).astype(np.uint16)
+            vb[8] = 0x8000 if b % 3 == 0 else 0x0001           # -0 or the smallest subnormal
+            bits[t, 16 * b:16 * b + 16] = vb
+    bits[0, 5] = WL.float32_to_bf16_bits(np.array([2688.0], np.float32))[0]   # gsa = 1 for the first half
+    return bits
+
+
+@pytest.mark.parametrize("flags", [0, K2, K8])
+def test_fused_quantizer_codes_via_one_hot_gate(flags):
+    import nvfp4_router_gate_gb300 as R
+    rng = np.random.default_rng(31)
+    T, D = 192, 512
+    for half_x in range(2):
+        bits = _fused_probe_x(rng, T, D)
+        if half_x:                                     # the random half alone: arbitrary gsa
+            bits = bits[T // 2:].copy()
+        x32 = WL.bf16_bits_to_float32(bits)
+        xd = to_device(bits, "bf16")
+        xq, xs, xg = Q.quantize(x32)
+        for c0 in range(0, D, 256):
+            cols = np.arange(c0, c0 + 256)
+            W = _one_hot_gate(cols, D)
+            wf, wsf, wg = R.nvfp4_pack_weight(to_device(W, "f32"))
+            out = R.router_gate_logits(xd, wf, wsf, wg, flags=flags)
+            torch.cuda.synchronize()
+            wq, wsb, wgg = Q.quantize(W)
+            L, _ = gemm.logits(xq, xs, xg, wq, wsb, wgg)
+            g = out.cpu().numpy().astype(np.float64)
+            err = np.abs(g - L)
+            assert np.all(err <= 1e-6 * np.abs(L)), (half_x, c0, np.argwhere(err > 1e-6 * np.abs(L))[:5])
