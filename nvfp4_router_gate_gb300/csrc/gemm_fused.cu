@@ -21,7 +21,8 @@
 //              block's scale byte into the stage's scale atoms.  Warps 2-5 then
 //              copy the x and W scale atoms into their tensor-memory quarter
 //              (tcgen05.st) and signal the MMA warp; the A tile is
-//              double-buffered;
+//              double-buffered and the warps synchronise only through
+//              mbarriers (a warp may run about a stage ahead of another);
 //   warp 1     MMA issuer: one tcgen05.mma.kind::mxf4nvf4 (M=128, N=128 or 256,
 //              K=64) per 64-element K step into one fp32 accumulator;
 //   warps 2-9  after the last MMA: TMA store of the fp32 partial (as in
@@ -91,9 +92,8 @@ __device__ __forceinline__ void quant_rows(const uint4 (&v)[kG], const QuantScal
       x[i][2 * j] = __uint_as_float(w[j] << 16);
       x[i][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     }
-    mx[i] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) mx[i] = fmaxf(mx[i], fabsf(x[i][j]));
+    // max |x| on the bf16 bit patterns (integer pipe; exact)
+    mx[i] = __uint_as_float(absmax_bits16B<true>(v[i]));
   }
 #pragma unroll
   for (int i = 0; i < kG; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xFFFFFFFFu, mx[i], 1));
@@ -134,7 +134,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   uint64_t* empty_x = full_x + kFXSlots;
   uint64_t* a_full = empty_x + kFXSlots;
   uint64_t* a_empty = a_full + kFASlots;
-  uint64_t* acc_full = a_empty + kFASlots;
+  uint64_t* q_done = a_empty + kFASlots;                               // [kFASlots]
+  uint64_t* acc_full = q_done + kFASlots;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -151,7 +152,11 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFStagesW; ++s) { mbar_init(full_w + s, 1); mbar_init(empty_w + s, 1); }
     for (int s = 0; s < kFXSlots; ++s) { mbar_init(full_x + s, 1); mbar_init(empty_x + s, 8); }
-    for (int a = 0; a < kFASlots; ++a) { mbar_init(a_full + a, 4); mbar_init(a_empty + a, 1); }
+    for (int a = 0; a < kFASlots; ++a) {
+      mbar_init(a_full + a, 4);
+      mbar_init(a_empty + a, 1);
+      mbar_init(q_done + a, 8);
+    }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -274,10 +279,12 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     for (int s = 0; s < my_st; ++s) {
       const int slot = s & 1;
       const uint32_t aph = (s >> 1) & 1;
-      // All quantizer warps agree (one barrier) that the slot is free -- its
-      // previous MMAs completed -- and that no warp has failed so far.
-      ok = bar_and(2, 256, ok && mbar_wait(a_empty + slot, aph ^ 1u, deadline, abort_flag));
-      if (!ok) break;
+      // the slot is free once the MMAs that read it two stages ago completed
+      // (no CTA-wide barrier: warps may run up to about a stage apart)
+      if (!ok || !__all_sync(0xFFFFFFFFu, mbar_wait(a_empty + slot, aph ^ 1u, deadline, abort_flag))) {
+        ok = false;
+        break;
+      }
       uint8_t* ac = aring + slot * kFASlot;
       uint8_t* asf = ac + kFACodes;
       for (int hs = 0; hs < 2; ++hs) {
@@ -321,10 +328,13 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       }
       // the MMA reads the codes through the async proxy
       fence_proxy_async_smem();
-      asm volatile("bar.sync 2, 256;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_done + slot);
       if (warp < 6) {
-        // ---- scale stagers: x and W scale atoms into this warp's quarter
-        const bool okw = __all_sync(0xFFFFFFFFu, mbar_wait(full_w + wst, wph, deadline, abort_flag));
+        // ---- scale stagers: once all eight warps have written the slot, the
+        // x and W scale atoms go into this warp's tensor-memory quarter
+        const bool okw = __all_sync(0xFFFFFFFFu, mbar_wait(q_done + slot, aph, deadline, abort_flag) &&
+                                                     mbar_wait(full_w + wst, wph, deadline, abort_flag));
         if (okw) {
           const uint8_t* sb = wring + wst * kFWStage + kFWTile;
           uint32_t va[16], vb0[16], vb1[16];
@@ -355,7 +365,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       }
       if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
     }
-    if (!ok && threadIdx.x == 64) {
+    if (!ok && lane == 0) {
       report_timeout(p.status);
       *abort_flag = 1;
     }

@@ -294,14 +294,33 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
 }
 
+// Compare-exchange so that v[a] >= v[b]; the 19-comparator 8-sorter (the
+// network of sort8 in nvr_device.cuh) on packed keys.
+__device__ __forceinline__ void cx(uint64_t (&v)[8], int a, int b) {
+  const uint64_t x = v[a], y = v[b];
+  const bool sw = y > x;
+  v[a] = sw ? y : x;
+  v[b] = sw ? x : y;
+}
+__device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
+  cx(v, 0, 2); cx(v, 1, 3); cx(v, 4, 6); cx(v, 5, 7);
+  cx(v, 0, 4); cx(v, 1, 5); cx(v, 2, 6); cx(v, 3, 7);
+  cx(v, 0, 1); cx(v, 2, 3); cx(v, 4, 5); cx(v, 6, 7);
+  cx(v, 2, 4); cx(v, 3, 5);
+  cx(v, 1, 4); cx(v, 3, 6);
+  cx(v, 1, 2); cx(v, 3, 4); cx(v, 5, 6);
+}
+
 // One warp per token.  Lane l owns experts 4l..4l+3 and 128+4l..128+4l+3
-// (coalesced 512-byte rows per partial).  Selection: k rounds of a warp
-// arg-max over the 256 packed keys (two 32-bit max reductions per round: the
-// key's bits, then the complemented id among the lanes holding that key); the
-// winning lane takes its entry out and recomputes its own best.  Exact for any
-// keys, ties included, with no data-dependent trip counts.
+// (coalesced 512-byte rows per partial).  Selection: each lane sorts its 8
+// packed keys; k rounds then take the best head of the warp (two 32-bit max
+// reductions: the key's bits, then the complemented id among the lanes
+// holding that key) and the winning lane pops its head.  Exact for any keys,
+// ties included, with no data-dependent trip counts.  The selected experts'
+// logits come back from a per-warp copy of the row in shared memory.
 __global__ void __launch_bounds__(kEpiWarpsPerCta * 32)
 router_epilogue_kernel(const __grid_constant__ EpiParams p) {
+  __shared__ float4 s_row[kEpiWarpsPerCta][64];     // this warp's 256 logits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kEpiWarpsPerCta + warp;
   int col[8];
@@ -336,40 +355,32 @@ router_epilogue_kernel(const __grid_constant__ EpiParams p) {
       if (col[j] < p.N) p.logits[t * p.N + col[j]] = l[j];
     return;
   }
+  s_row[warp][lane] = make_float4(l[0], l[1], l[2], l[3]);
+  s_row[warp][32 + lane] = make_float4(l[4], l[5], l[6], l[7]);
   uint64_t pk[8];
-  uint64_t m = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float key = p.raw ? l[j] : __fadd_rn(sigmoid_f32(l[j]), b[j]);
     pk[j] = col[j] < p.N ? pack_key(key, col[j]) : 0;
-    m = pk[j] > m ? pk[j] : m;
   }
+  sort8_desc(pk);
   int sel_id = 0;
-  float sel_l = 0.0f;
 #pragma unroll 1
   for (int r = 0; r < p.k; ++r) {
-    const uint32_t hi = static_cast<uint32_t>(m >> 32), lo = static_cast<uint32_t>(m);
+    const uint32_t hi = static_cast<uint32_t>(pk[0] >> 32), lo = static_cast<uint32_t>(pk[0]);
     const uint32_t hmax = __reduce_max_sync(0xFFFFFFFFu, hi);
     const uint32_t lmax = __reduce_max_sync(0xFFFFFFFFu, hi == hmax ? lo : 0u);
-    const int id = static_cast<int>(~lmax);           // the winning expert
-    const int owner = (id & 127) >> 2;                 // the lane holding it
-    const int slot = ((id >> 7) << 2) | (id & 3);
-    float lw = l[0];
+    if (lane == r) sel_id = static_cast<int>(~lmax);   // the winning expert
+    if (hi == hmax && lo == lmax) {                    // its lane (ids are unique)
 #pragma unroll
-    for (int j = 1; j < 8; ++j) lw = slot == j ? l[j] : lw;
-    lw = __shfl_sync(0xFFFFFFFFu, lw, owner & 31);
-    if (lane == r) { sel_id = id; sel_l = lw; }
-    if (lane == owner) {
-      m = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j == slot) pk[j] = 0;
-        m = pk[j] > m ? pk[j] : m;
-      }
+      for (int j = 0; j < 7; ++j) pk[j] = pk[j + 1];
+      pk[7] = 0;
     }
   }
+  __syncwarp();
   // gather the unbiased scores of the routed experts, renormalise, scale
   const bool mine = lane < p.k;
+  const float sel_l = reinterpret_cast<const float*>(s_row[warp])[sel_id & 255];
   const float sc = p.raw ? sel_l : sigmoid_f32(sel_l);
   float sum = mine ? sc : 0.0f;
 #pragma unroll
