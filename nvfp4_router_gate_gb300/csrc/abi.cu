@@ -227,22 +227,21 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   prof.after();
   if (e != cudaSuccess) return cuda_status(e);
   // Up to 256 experts: K split over S CTAs with one tensor-core accumulator
-  // for the whole row each, then the epilogue kernel; bf16 activations are
-  // quantized inside the GEMM.  Wider heads: N tiles split across CTAs with a
-  // top-k merge, after the standalone quantize kernel.
+  // for the whole row each; bf16 activations are quantized inside the GEMM
+  // and routed in the same kernel, fp32 ones take the standalone quantizer,
+  // the K-split GEMM and the epilogue kernel.  Wider heads: N tiles split
+  // across CTAs with a top-k merge, after the standalone quantize kernel.
   const int split_k = forced_split                        ? forced_split
                       : (flags & NVR_FLAG_SPLIT_N) || N > 256 ? 0
                                                               : plan_splitk(T, D, sms);
   float* partials = reinterpret_cast<float*>(w + L.partials);
   if (split_k > 0 && bf16) {
+    // one cluster of S CTAs per token tile: a power of two (each CTA routes
+    // 128/S tokens), at most 8 (the portable cluster size)
+    const int S = split_k >= 8 ? 8 : split_k >= 4 ? 4 : split_k >= 2 ? 2 : 1;
     prof.before();
-    st = launch_fused_qgemm(static_cast<const uint16_t*>(x), qrec, T, D, W_fp4, W_sf, N, partials, status, split_k,
-                            stall, s);
-    prof.after();
-    if (st != NVR_OK) return st;
-    prof.before();
-    st = launch_router_epilogue(partials, split_k, x_gsa, w_gsa, T, N, bias, k, routed_scaling, raw, out_ids,
-                                out_w, logits, s);
+    st = launch_fused_router(static_cast<const uint16_t*>(x), qrec, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k,
+                             routed_scaling, raw, out_ids, out_w, logits, partials, status, S, stall, s);
     prof.after();
     return st;
   }

@@ -1,14 +1,19 @@
-// gemm_fused.cu -- the router for up to 256 experts on bf16 activations: the
-// runtime NVFP4 quantization of x runs inside the K-split tensor-core GEMM,
-// so the quantized activations never exist in memory (sm_103a).
+// gemm_fused.cu -- the router for up to 256 experts on bf16 activations in one
+// launch after the amax kernel: the runtime NVFP4 quantization of x runs
+// inside a K-split tensor-core GEMM and the router epilogue runs in the same
+// kernel, so the quantized activations never exist in memory and the logits
+// only pass through L2 (sm_103a).
 //
 // Source: "nvfp4-megamoe-kernel commit 04cf8ca: dsv4/layers/router.py"
 // (runtime gsa = max|x| / 2688, NVFP4 activations and gate weight, gate GEMM
-// on Blackwell tensor cores).  Quantization arithmetic as in the standalone
-// quantizer (quant_block16): y = RN(x / gsa), sy = RN(max|y| / 6), E4M3 scale,
-// E2M1 codes of RN(y / scale) with the input's sign; identical codes.
+// on Blackwell tensor cores, the single-kernel GEMM + fused router epilogue)
+// and "commit e0f60b9: dsv4/kernels/router/__init__.py" (activation_topk).
+// Quantization arithmetic as in the standalone quantizer (quant_block16):
+// y = RN(x / gsa), sy = RN(max|y| / 6), E4M3 scale, E2M1 codes of
+// RN(y / scale) with the input's sign; identical codes.
 //
-// Per CTA (tile m of 128 tokens, K-split rank r of S, 320 threads):
+// A token tile of 128 rows is split along K over S CTAs (S = 2, 4 or 8) that
+// form one thread-block cluster.  Per CTA (rank r, 320 threads):
 //   warp 0     TMA producer: per stage of 256 K-elements two bf16 x boxes
 //              (128 rows x 128 elements, 32 KB each) into a 3-slot ring, and
 //              the W tile (128 or 256 rows x 128 bytes, 128-byte swizzle) with
@@ -25,8 +30,10 @@
 //              mbarriers (a warp may run about a stage ahead of another);
 //   warp 1     MMA issuer: one tcgen05.mma.kind::mxf4nvf4 (M=128, N=128 or 256,
 //              K=64) per 64-element K step into one fp32 accumulator;
-//   warps 2-9  after the last MMA: TMA store of the fp32 partial (as in
-//              gemm_splitk.cu); the epilogue kernel there finishes the router.
+//   warps 2-9  after the last MMA: the fp32 partial (128 x 256) goes from
+//              tensor memory to partial plane r of the workspace (L2); after a
+//              cluster barrier each CTA routes its own 128/S tokens from the S
+//              planes, one warp per token (TokenRouter, nvr_splitk.cuh).
 // Tensor memory: accumulator at columns 0-255; scales of A slot a at
 // 256 + 48 a (x: 4 columns per K step, W: 8).
 #include "nvr_splitk.cuh"
@@ -57,10 +64,19 @@ static_assert(8 * 8192 <= kFXRing, "store staging fits the x ring");
 struct FusedParams {
   CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
   CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 x (128 * n_half)
-  CUtensorMap tmap_p;          // partials [S][T][256] fp32, box 32 x 32 x 1
   const float* qrec;           // quantizer record {gsa, 1/gsa, mode, amax} from the amax kernel
   const uint8_t* sfb;          // W scales, tile layout
-  int T, D, n_half, S;
+  float* partials;             // [S][T][256] fp32 partial logits (workspace)
+  int T, D, N, n_half, S;
+  // router epilogue
+  const float* x_gsa;
+  const float* w_gsa;
+  const float* bias;           // [N] or null
+  int k, raw;
+  float routed_scaling;
+  int32_t* out_ids;
+  float* out_w;
+  float* logits;               // logits mode: write [T, N] logits instead of the top-k
   uint32_t* status;
   int test_stall;              // test hook: the MMA issuer issues nothing
 };
@@ -162,7 +178,6 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     fence_mbar_init();
     tma_prefetch_map(&p.tmap_x);
     tma_prefetch_map(&p.tmap_b);
-    tma_prefetch_map(&p.tmap_p);
   }
   if (threadIdx.x < 128) {
     const uint32_t b = threadIdx.x;
@@ -176,9 +191,14 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   const uint32_t tmem = *tmem_holder;
   // the amax kernel before us (programmatic launch) must have finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The next call's amax kernel may start streaming its input now: it
+  // publishes its results only after this grid has finished.
+  asm volatile("griddepcontrol.launch_dependents;");
   const uint64_t deadline = globaltimer_ns() + 1000000000ull;   // 1 s
 
   bool acc_ok = true;     // quantizer warps: the accumulator is complete
+  TokenRouter rt;         // quantizer warps: the epilogue's per-lane state
+  float gscale = 0.0f;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int wst = 0;
@@ -266,6 +286,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     }
   } else {
     // ---------------------------------------------------------- quantizers
+    rt.init(p.bias, p.N, p.k, p.raw, p.routed_scaling, lane);       // for the epilogue
+    gscale = __fmul_rn(__ldg(p.x_gsa), __ldg(p.w_gsa));
     QuantScale qs;
     qs.gsa = __ldg(p.qrec);
     qs.rgsa = __ldg(p.qrec + 1);
@@ -380,13 +402,40 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     tc_fence_after();
     // every x box has been read (the last MMA needed them all): the x ring
     // stages the stores
-    store_partial_tile(&p.tmap_p, xring, tmem, warp, lane, m_tile, rank, p.n_half, p.T, my_st > 0 && acc_ok);
+    store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * 256, xring, tmem, warp, lane, m_tile,
+                       p.n_half, p.T, my_st > 0 && acc_ok);
+  }
+
+  // The S CTAs of this token tile form the cluster: after the barrier every
+  // partial row of the tile is visible to all of them.
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  tc_fence_after();
+
+  if (warp >= 2) {
+    // ------------------------------- router epilogue for this CTA's tokens
+    // rank r finishes tokens [r * 128/S, (r+1) * 128/S) of the tile; warp w
+    // takes tokens w-2, w+6, ... (up to four at once, their latencies
+    // overlapping; the A ring holds each warp's copies of its rows)
+    float4* s_row = reinterpret_cast<float4*>(aring) + (warp - 2) * 256;
+    const int per = 128 / p.S;
+    const int64_t t0 = static_cast<int64_t>(m_tile) * 128 + static_cast<int64_t>(rank) * per;
+    for (int i = warp - 2; i < per; i += 32) {
+      int64_t tt[4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int64_t t = t0 + i + 8 * n;
+        tt[n] = (i + 8 * n < per && t < p.T) ? t : -1;
+      }
+      rt.route<4>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row, lane, p.out_ids, p.out_w,
+                  p.logits);
+    }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  asm volatile("griddepcontrol.launch_dependents;");
   if (*abort_flag && threadIdx.x == 0) {
     // After an abort, copies may still be landing in this CTA's shared
     // memory: wait (bounded) for the latest fill of every ring slot.
@@ -417,13 +466,15 @@ bool encode_x(CUtensorMap* map, const uint16_t* ptr, int64_t T, int64_t D) {
 
 }  // namespace
 
-nvr_status launch_fused_qgemm(const uint16_t* x, const float* qrec, int64_t T, int64_t D, const uint8_t* W_codes,
-                              const uint8_t* W_sf, int64_t N, float* partials, uint32_t* status, int S,
-                              bool test_stall, cudaStream_t s) {
+nvr_status launch_fused_router(const uint16_t* x, const float* qrec, const float* x_gsa, int64_t T, int64_t D,
+                               const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
+                               const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
+                               float* out_w, float* logits, float* partials, uint32_t* status, int S,
+                               bool test_stall, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVR_ERR_CUDA;
-  if (N > 256 || S < 1 || S > kMaxSplitK) return NVR_ERR_UNSUPPORTED;
+  if (N > 256 || k > kMaxKmax || S < 1 || S > 8 || 128 % S) return NVR_ERR_UNSUPPORTED;
   if (static_cast<size_t>(S) * static_cast<size_t>((T + 127) / 128 * 128) > splitk_partial_rows(T))
     return NVR_ERR_UNSUPPORTED;
   if (!attr_set[dev]) {
@@ -435,20 +486,26 @@ nvr_status launch_fused_qgemm(const uint16_t* x, const float* qrec, int64_t T, i
   const int n_half = N > 128 ? 2 : 1;
   if (!encode_x(&g.tmap_x, x, T, D)) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes(&g.tmap_b, W_codes, N, D, 128u * n_half)) return NVR_ERR_UNSUPPORTED;
-  if (!encode_partials(&g.tmap_p, partials, T, S)) return NVR_ERR_UNSUPPORTED;
-  g.qrec = qrec; g.sfb = W_sf;
-  g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.n_half = n_half; g.S = S;
+  g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
+  g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_half = n_half; g.S = S;
+  g.x_gsa = x_gsa; g.w_gsa = w_gsa; g.bias = raw ? nullptr : bias;
+  g.k = k; g.raw = raw ? 1 : 0; g.routed_scaling = routed_scaling;
+  g.out_ids = out_ids; g.out_w = out_w; g.logits = logits;
   g.status = status; g.test_stall = test_stall ? 1 : 0;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;           // the S K-splits of a token tile
+  attr[1].val.clusterDim.x = S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((T + 127) / 128 * S));
   cfg.blockDim = dim3(kFThreads);
   cfg.dynamicSmemBytes = kFSmem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cuda_status(cudaLaunchKernelEx(&cfg, fused_qgemm_kernel, g));
 }
 

@@ -281,116 +281,21 @@ struct EpiParams {
   float* logits;               // logits mode: write [T, N] logits instead of the top-k
 };
 
-// (key descending, id ascending) as one unsigned 64-bit order: the float's
-// order-preserving bit pattern above the complemented id.  Never 0 for a
-// non-NaN key, so 0 marks "no entry".
-__device__ __forceinline__ uint64_t pack_key(float key, int id) {
-  const uint32_t b = __float_as_uint(key);
-  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
-}
-
-__device__ __forceinline__ float4 add4(float4 a, float4 b) {
-  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
-}
-
-// Compare-exchange so that v[a] >= v[b]; the 19-comparator 8-sorter (the
-// network of sort8 in nvr_device.cuh) on packed keys.
-__device__ __forceinline__ void cx(uint64_t (&v)[8], int a, int b) {
-  const uint64_t x = v[a], y = v[b];
-  const bool sw = y > x;
-  v[a] = sw ? y : x;
-  v[b] = sw ? x : y;
-}
-__device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
-  cx(v, 0, 2); cx(v, 1, 3); cx(v, 4, 6); cx(v, 5, 7);
-  cx(v, 0, 4); cx(v, 1, 5); cx(v, 2, 6); cx(v, 3, 7);
-  cx(v, 0, 1); cx(v, 2, 3); cx(v, 4, 5); cx(v, 6, 7);
-  cx(v, 2, 4); cx(v, 3, 5);
-  cx(v, 1, 4); cx(v, 3, 6);
-  cx(v, 1, 2); cx(v, 3, 4); cx(v, 5, 6);
-}
-
-// One warp per token.  Lane l owns experts 4l..4l+3 and 128+4l..128+4l+3
-// (coalesced 512-byte rows per partial).  Selection: each lane sorts its 8
-// packed keys; k rounds then take the best head of the warp (two 32-bit max
-// reductions: the key's bits, then the complemented id among the lanes
-// holding that key) and the winning lane pops its head.  Exact for any keys,
-// ties included, with no data-dependent trip counts.  The selected experts'
-// logits come back from a per-warp copy of the row in shared memory.
+// One warp per token (see route_token in nvr_splitk.cuh).
 __global__ void __launch_bounds__(kEpiWarpsPerCta * 32)
 router_epilogue_kernel(const __grid_constant__ EpiParams p) {
-  __shared__ float4 s_row[kEpiWarpsPerCta][64];     // this warp's 256 logits
+  __shared__ float4 s_row[kEpiWarpsPerCta][64];     // each warp's 256 logits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kEpiWarpsPerCta + warp;
-  int col[8];
-  float b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    col[j] = (j < 4 ? 0 : 128) + 4 * lane + (j & 3);
-    // the bias is a caller input that no kernel of this call writes
-    b[j] = (!p.raw && p.bias && col[j] < p.N) ? __ldg(p.bias + col[j]) : 0.0f;
-  }
+  TokenRouter rt;
+  rt.init(p.bias, p.N, p.k, p.raw, p.routed_scaling, lane);
   // the GEMM kernel before us (programmatic launch) must have finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (t >= p.T) return;                              // whole warp
   const float gscale = __fmul_rn(__ldg(p.x_gsa), __ldg(p.w_gsa));
-  const size_t plane = static_cast<size_t>(p.T) * 256;
-  const float* row = p.partials + static_cast<size_t>(t) * 256;
-  float4 a0 = __ldcg(reinterpret_cast<const float4*>(row + 4 * lane));
-  float4 a1 = __ldcg(reinterpret_cast<const float4*>(row + 128 + 4 * lane));
-#pragma unroll 4
-  for (int s = 1; s < p.S; ++s) {                    // partials in rank order
-    const float* r = row + s * plane;
-    a0 = add4(a0, __ldcg(reinterpret_cast<const float4*>(r + 4 * lane)));
-    a1 = add4(a1, __ldcg(reinterpret_cast<const float4*>(r + 128 + 4 * lane)));
-  }
-  const float acc[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-  float l[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) l[j] = __fmul_rn(acc[j], gscale);
-  if (p.logits) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (col[j] < p.N) p.logits[t * p.N + col[j]] = l[j];
-    return;
-  }
-  s_row[warp][lane] = make_float4(l[0], l[1], l[2], l[3]);
-  s_row[warp][32 + lane] = make_float4(l[4], l[5], l[6], l[7]);
-  uint64_t pk[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float key = p.raw ? l[j] : __fadd_rn(sigmoid_f32(l[j]), b[j]);
-    pk[j] = col[j] < p.N ? pack_key(key, col[j]) : 0;
-  }
-  sort8_desc(pk);
-  int sel_id = 0;
-#pragma unroll 1
-  for (int r = 0; r < p.k; ++r) {
-    const uint32_t hi = static_cast<uint32_t>(pk[0] >> 32), lo = static_cast<uint32_t>(pk[0]);
-    const uint32_t hmax = __reduce_max_sync(0xFFFFFFFFu, hi);
-    const uint32_t lmax = __reduce_max_sync(0xFFFFFFFFu, hi == hmax ? lo : 0u);
-    if (lane == r) sel_id = static_cast<int>(~lmax);   // the winning expert
-    if (hi == hmax && lo == lmax) {                    // its lane (ids are unique)
-#pragma unroll
-      for (int j = 0; j < 7; ++j) pk[j] = pk[j + 1];
-      pk[7] = 0;
-    }
-  }
-  __syncwarp();
-  // gather the unbiased scores of the routed experts, renormalise, scale
-  const bool mine = lane < p.k;
-  const float sel_l = reinterpret_cast<const float*>(s_row[warp])[sel_id & 255];
-  const float sc = p.raw ? sel_l : sigmoid_f32(sel_l);
-  float sum = mine ? sc : 0.0f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
-  if (mine) {
-    float w = sc;
-    if (!p.raw) w = sum > 0.0f ? __fdiv_rn(__fmul_rn(p.routed_scaling, sc), sum) : 0.0f;
-    p.out_ids[t * p.k + lane] = sel_id;
-    p.out_w[t * p.k + lane] = w;
-  }
+  const int64_t tt[1] = {t};
+  rt.route<1>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row[warp], lane, p.out_ids, p.out_w,
+              p.logits);
 }
 
 }  // namespace

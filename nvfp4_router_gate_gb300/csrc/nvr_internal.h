@@ -93,11 +93,14 @@ int plan_splitk(int64_t T, int64_t D, int num_sms);
 nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64_t T, int64_t D,
                               const uint8_t* W_codes, const uint8_t* W_sf, int64_t N, float* partials,
                               uint32_t* status, int S, bool test_stall, cudaStream_t s);
-// The same GEMM on bf16 activations, quantized inside the kernel from the
-// quantizer record qrec {gsa, 1/gsa, mode, amax} of the amax kernel.
-nvr_status launch_fused_qgemm(const uint16_t* x, const float* qrec, int64_t T, int64_t D, const uint8_t* W_codes,
-                              const uint8_t* W_sf, int64_t N, float* partials, uint32_t* status, int S,
-                              bool test_stall, cudaStream_t s);
+// The whole router after the amax kernel for bf16 activations and N <= 256:
+// quantization inside the K-split GEMM, partials through L2 and the epilogue
+// in the same kernel (cluster of S CTAs per 128-token tile, S in {1,2,4,8}).
+nvr_status launch_fused_router(const uint16_t* x, const float* qrec, const float* x_gsa, int64_t T, int64_t D,
+                               const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
+                               const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
+                               float* out_w, float* logits, float* partials, uint32_t* status, int S,
+                               bool test_stall, cudaStream_t s);
 nvr_status launch_router_epilogue(const float* partials, int S, const float* x_gsa, const float* w_gsa,
                                   int64_t T, int64_t N, const float* bias, int k, float routed_scaling,
                                   bool raw, int32_t* out_ids, float* out_w, float* logits, cudaStream_t s);

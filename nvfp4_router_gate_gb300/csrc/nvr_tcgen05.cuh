@@ -184,6 +184,15 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ------------------------------------------------------- thread-block clusters
+// Hardware barrier over every thread of every CTA of the cluster; the release /
+// acquire pair makes memory writes before it visible to reads after it in the
+// other CTAs.  Every thread of each CTA must reach it (no early exits).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------- tensor-memory stores, TMA stores
 // 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes (one
 // lane per thread), then the wait for the stores.

@@ -103,6 +103,17 @@ def test_decode_router(T):
         assert compare.topk_ok(res2), res2
 
 
+def test_prefill_router_odd_tile_count():
+    """T = 5000: 40 token tiles, so the planner's K-split is not a power of two
+    and the fused kernel rounds it down (sampled rows, including the ragged
+    last tile)."""
+    case = Case(WL.WORKLOADS["prefill"].with_T(5000))
+    ids, w = case.run()
+    rows = np.unique(np.concatenate([np.arange(0, 5000, 97), np.arange(4990, 5000), [127, 128, 4991]]))
+    res = case.check(ids, w, rows)
+    assert compare.topk_ok(res), res
+
+
 def test_prefill_router_sampled_rows():
     case = Case(WL.WORKLOADS["prefill"])
     ids, w = case.run()
