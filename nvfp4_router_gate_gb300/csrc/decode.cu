@@ -60,6 +60,85 @@ __device__ __forceinline__ uint32_t e2m1x4_to_s8x4(uint32_t c16) {
   return (mag & ~mask) | (neg & mask);
 }
 
+// (key descending, id ascending) as one unsigned 64-bit order: the float's
+// order-preserving bit pattern above the complemented id; 0 marks "none".
+__device__ __forceinline__ uint64_t dec_pack_key(float key, int id) {
+  const uint32_t b = __float_as_uint(key);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(id));
+}
+
+constexpr int kCandCap = 64;
+
+// Top-k (k <= 16) of one token's N <= 256 keys with one warp, in order (key
+// descending, lower id first): lane l holds keys l, l+32, ...  The k-th
+// largest of the 32 lane maxima is a lower bound of the k-th largest key (the
+// k largest maxima are k keys at least that large), so only keys >= it are
+// candidates -- typically k to 2k -- and each candidate's rank among the
+// candidates is its rank overall.
+// More than kCandCap candidates (exact ties) fall back to k rounds of a warp
+// arg-max.  sel[r] receives the expert of rank r; cand is warp scratch.
+__device__ __forceinline__ void warp_topk_256(const float* kt, int N, int k, int lane, uint64_t* cand, int* sel) {
+  uint64_t pk[8];
+  uint64_t mx = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int n = lane + 32 * j;
+    pk[j] = n < N ? dec_pack_key(kt[n], n) : 0;
+    mx = pk[j] > mx ? pk[j] : mx;
+  }
+  // the k-th largest lane maximum: the k largest maxima are k keys at least
+  // that large (0 when fewer than k lanes hold keys: every key is a candidate)
+  cand[lane] = mx;
+  __syncwarp();
+  int mrank = 0;
+#pragma unroll 8
+  for (int q = 0; q < 32; ++q) mrank += cand[q] > mx ? 1 : 0;
+  const uint32_t at_k = __ballot_sync(0xFFFFFFFFu, mx != 0 && mrank == k - 1);
+  const uint64_t bound = at_k ? __shfl_sync(0xFFFFFFFFu, mx, __ffs(at_k) - 1) : 0;
+  __syncwarp();                                    // cand is rewritten below
+  uint32_t cmask = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) cmask |= static_cast<uint32_t>(pk[j] != 0 && pk[j] >= bound) << j;
+  const int cnt = __popc(cmask);
+  int incl = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (total <= kCandCap) {
+    int pos = incl - cnt;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if ((cmask >> j) & 1u) cand[pos++] = pk[j];
+    __syncwarp();
+    for (int ci = lane; ci < total; ci += 32) {
+      const uint64_t me = cand[ci];
+      int rk = 0;
+      for (int q = 0; q < total; ++q) rk += cand[q] > me ? 1 : 0;
+      if (rk < k) sel[rk] = static_cast<int>(~static_cast<uint32_t>(me));
+    }
+  } else {
+    // many equal keys: k rounds of a warp arg-max, the winner's key removed
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+      uint64_t m = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = pk[j] > m ? pk[j] : m;
+      const uint32_t hmax = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(m >> 32));
+      const uint32_t lmax = __reduce_max_sync(0xFFFFFFFFu, static_cast<uint32_t>(m >> 32) == hmax
+                                                               ? static_cast<uint32_t>(m) : 0u);
+      const uint64_t w = (static_cast<uint64_t>(hmax) << 32) | lmax;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pk[j] = pk[j] == w ? 0 : pk[j];
+      if (lane == 0) sel[r] = static_cast<int>(~lmax);
+    }
+  }
+  __syncwarp();
+}
+
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kMaxBlocksPerThread = 16;   // W blocks a thread prefetches into registers
@@ -80,7 +159,10 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int T, int D, int N, in
   L.xv = align_up(raw_bytes > kv_bytes ? raw_bytes : kv_bytes, 16);
   L.xs = align_up(L.xv + static_cast<size_t>(T) * D, 16);
   L.red = align_up(L.xs + static_cast<size_t>(T) * KB * 4, 16);
-  L.total = L.red + static_cast<size_t>(kDecodeWarps) * kMaxT * 4;
+  // cross-warp partial sums, later the last CTA's candidate lists (8 B each)
+  const size_t red_bytes = static_cast<size_t>(kDecodeWarps) * kMaxT * 4;
+  const size_t cand_bytes = static_cast<size_t>(kDecodeWarps) * kCandCap * 8;
+  L.total = L.red + (red_bytes > cand_bytes ? red_bytes : cand_bytes);
   return L;
 }
 
@@ -113,9 +195,14 @@ decode_router_kernel(const DecodeParams p) {
   //    in shared memory with one burst of asynchronous 16-byte copies.
   uint2 wc[kMaxBlocksPerThread];
   uint32_t wsb[kMaxBlocksPerThread];
+  // slots i with i * gs < KB hold blocks (the bound is the same in every
+  // thread, so the unrolled loops below skip the empty slots with a uniform
+  // branch instead of computing on them)
+  const int nb = (KB + gs - 1) / gs;
 #pragma unroll
   for (int i = 0; i < kMaxBlocksPerThread; ++i) {
     const int c = j + i * gs;
+    if (i >= nb) break;
     if (e < N && c < KB) {
       wc[i] = __ldg(reinterpret_cast<const uint2*>(p.W_codes + static_cast<size_t>(e) * (D / 2) + c * 8));
       wsb[i] = __ldg(p.W_sf + sf_tile_offset(e, c, KB));
@@ -129,19 +216,6 @@ decode_router_kernel(const DecodeParams p) {
     cp_async16(xraw + 16 * v, static_cast<const uint8_t*>(p.x) + 16 * v);
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncthreads();
-  // decode this thread's weight blocks now: their loads were issued first and
-  // have landed by the time x has; this keeps them off the critical path later
-  uint32_t wv[kMaxBlocksPerThread][4];
-  float swv[kMaxBlocksPerThread];
-#pragma unroll
-  for (int i = 0; i < kMaxBlocksPerThread; ++i) {
-    swv[i] = e4m3_value(wsb[i]);
-    wv[i][0] = e2m1x4_to_s8x4(wc[i].x & 0xFFFFu);
-    wv[i][1] = e2m1x4_to_s8x4(wc[i].x >> 16);
-    wv[i][2] = e2m1x4_to_s8x4(wc[i].y & 0xFFFFu);
-    wv[i][3] = e2m1x4_to_s8x4(wc[i].y >> 16);
-  }
-
   // 1. max |x| over the whole batch (from shared memory)
   const uint4* x4 = reinterpret_cast<const uint4*>(xraw);
   uint32_t m = 0;
@@ -173,6 +247,20 @@ decode_router_kernel(const DecodeParams p) {
   }
   __syncthreads();
 
+  // decode this thread's weight blocks: their loads were issued first and have
+  // long landed; decoding them only now keeps them off the path to gsa
+  uint32_t wv[kMaxBlocksPerThread][4];
+  float swv[kMaxBlocksPerThread];
+#pragma unroll
+  for (int i = 0; i < kMaxBlocksPerThread; ++i) {
+    if (i >= nb) break;
+    swv[i] = e4m3_value(wsb[i]);
+    wv[i][0] = e2m1x4_to_s8x4(wc[i].x & 0xFFFFu);
+    wv[i][1] = e2m1x4_to_s8x4(wc[i].x >> 16);
+    wv[i][2] = e2m1x4_to_s8x4(wc[i].y & 0xFFFFu);
+    wv[i][3] = e2m1x4_to_s8x4(wc[i].y >> 16);
+  }
+
   // 3. logits of this CTA's experts: integer dot products of each 16-element
   //    block (exact), scaled by the two block scales (exact product), fp32 sum.
   //    The weight blocks are decoded once; the token loop stays rolled.
@@ -182,6 +270,7 @@ decode_router_kernel(const DecodeParams p) {
 #pragma unroll
     for (int i = 0; i < kMaxBlocksPerThread; ++i) {
       const int c = j + i * gs;
+      if (i >= nb) break;
       if (e < N && c < KB) {
         const uint4 xq = *reinterpret_cast<const uint4*>(xv + static_cast<size_t>(t) * D + c * kBlock);
         int sdot = __dp4a(static_cast<int>(xq.x), static_cast<int>(wv[i][0]), 0);
@@ -238,6 +327,26 @@ decode_router_kernel(const DecodeParams p) {
     sbuf[i] = __ldcg(p.ws_scores + i);
   }
   __syncthreads();
+  if (N <= 256) {
+    // one warp per token: candidate selection, then the renormalised weights
+    uint64_t* cand = reinterpret_cast<uint64_t*>(red) + warp * kCandCap;   // red is no longer needed
+    for (int t = warp; t < T; t += kDecodeWarps) {
+      int* sel = s_sel + t * 16;
+      warp_topk_256(kbuf + static_cast<size_t>(t) * N, N, p.k, lane, cand, sel);
+      const float* st = sbuf + static_cast<size_t>(t) * N;
+      const float sc = lane < p.k ? st[sel[lane] & 255] : 0.0f;
+      float sum = sc;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+      if (lane < p.k) {
+        p.out_ids[static_cast<size_t>(t) * p.k + lane] = sel[lane];
+        p.out_w[static_cast<size_t>(t) * p.k + lane] =
+            p.raw ? sc : (sum > 0.0f ? __fdiv_rn(__fmul_rn(p.routed_scaling, sc), sum) : 0.0f);
+      }
+    }
+    if (tid == 0) *p.ticket = 0u;
+    return;
+  }
   if (T * N <= 2 * kDecodeThreads) {
     // Small batches: every thread ranks one or two (token, expert) keys
     // against the token's N keys (key descending, lower id first); the k
