@@ -237,8 +237,14 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   float* partials = reinterpret_cast<float*>(w + L.partials);
   if (split_k > 0 && bf16) {
     // one cluster of S CTAs per token tile: a power of two (each CTA routes
-    // 128/S tokens), at most 8 (the portable cluster size)
-    const int S = split_k >= 8 ? 8 : split_k >= 4 ? 4 : split_k >= 2 ? 2 : 1;
+    // 128/S tokens), no larger than the plan and small enough that every
+    // tile's cluster is resident at once (else the smallest size)
+    const int64_t m_tiles = (T + 127) / 128;
+    int S = 1;
+    for (int c = 16; c >= 2; c >>= 1) {
+      if (c > split_k) continue;
+      if (forced_split || fused_cluster_capacity(c) >= m_tiles) { S = c; break; }
+    }
     prof.before();
     st = launch_fused_router(static_cast<const uint16_t*>(x), qrec, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k,
                              routed_scaling, raw, out_ids, out_w, logits, partials, status, S, stall, s);

@@ -318,6 +318,9 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
           const uint8_t* xb = xring + xs * kFXBox;
 #pragma unroll
           for (int g = 0; g < kFRowsPerWarp / 2; g += 4) {
+            // rows past T only feed accumulator rows that are never stored:
+            // a group that starts past T is skipped (warp-uniform)
+            if (m_tile * 128 + qw * kFRowsPerWarp + 2 * g >= p.T) break;
             uint4 v[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -466,22 +469,61 @@ bool encode_x(CUtensorMap* map, const uint16_t* ptr, int64_t T, int64_t D) {
 
 }  // namespace
 
+// Per-device function attributes: the dynamic shared memory and clusters of
+// up to 16 CTAs (beyond the portable 8; the planner asks first).
+static cudaError_t fused_prepare(int dev) {
+  static bool done[kMaxDevices] = {};
+  if (done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fused_qgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fused_qgemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  done[dev] = true;
+  return cudaSuccess;
+}
+
+// How many clusters of S CTAs of this kernel the device can hold at once
+// (cached per device and size; 0 when the size cannot be scheduled).
+int fused_cluster_capacity(int S) {
+  static int cap[kMaxDevices][5] = {};
+  static bool known[kMaxDevices][5] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  const int slot = S == 1 ? 0 : S == 2 ? 1 : S == 4 ? 2 : S == 8 ? 3 : S == 16 ? 4 : -1;
+  if (slot < 0) return 0;
+  if (known[dev][slot]) return cap[dev][slot];
+  if (fused_prepare(dev) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S);
+  cfg.blockDim = dim3(kFThreads);
+  cfg.dynamicSmemBytes = kFSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fused_qgemm_kernel, &cfg) != cudaSuccess) n = 0;
+  cudaGetLastError();
+  cap[dev][slot] = n;
+  known[dev][slot] = true;
+  return n;
+}
+
 nvr_status launch_fused_router(const uint16_t* x, const float* qrec, const float* x_gsa, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
                                bool test_stall, cudaStream_t s) {
-  static bool attr_set[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVR_ERR_CUDA;
-  if (N > 256 || k > kMaxKmax || S < 1 || S > 8 || 128 % S) return NVR_ERR_UNSUPPORTED;
+  if (N > 256 || k > kMaxKmax || S < 1 || S > 16 || 128 % S) return NVR_ERR_UNSUPPORTED;
   if (static_cast<size_t>(S) * static_cast<size_t>((T + 127) / 128 * 128) > splitk_partial_rows(T))
     return NVR_ERR_UNSUPPORTED;
-  if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(fused_qgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
-    if (e != cudaSuccess) return cuda_status(e);
-    attr_set[dev] = true;
-  }
+  const cudaError_t e = fused_prepare(dev);
+  if (e != cudaSuccess) return cuda_status(e);
   FusedParams g;
   const int n_half = N > 128 ? 2 : 1;
   if (!encode_x(&g.tmap_x, x, T, D)) return NVR_ERR_UNSUPPORTED;

@@ -95,7 +95,9 @@ nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64
                               uint32_t* status, int S, bool test_stall, cudaStream_t s);
 // The whole router after the amax kernel for bf16 activations and N <= 256:
 // quantization inside the K-split GEMM, partials through L2 and the epilogue
-// in the same kernel (cluster of S CTAs per 128-token tile, S in {1,2,4,8}).
+// in the same kernel (cluster of S CTAs per 128-token tile, S in {1,2,4,8,16}).
+// fused_cluster_capacity(S): clusters of S CTAs the device holds at once.
+int fused_cluster_capacity(int S);
 nvr_status launch_fused_router(const uint16_t* x, const float* qrec, const float* x_gsa, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
