@@ -10,26 +10,28 @@
 // and "commit e0f60b9: dsv4/kernels/router/__init__.py" (activation_topk).
 // Quantization arithmetic as in the standalone quantizer (quant_block16):
 // y = RN(x / gsa), sy = RN(max|y| / 6), E4M3 scale, E2M1 codes of
-// RN(y / scale) with the input's sign; identical codes.
+// RN(y / scale) with the input's sign; identical codes and scale bytes,
+// reached by table lookups and bracketing products (quant_rows_bracket) with
+// an exact pass over the rare rows near a rounding boundary.
 //
-// A token tile of 128 rows is split along K over S CTAs (S = 2, 4 or 8) that
-// form one thread-block cluster.  Per CTA (rank r, 320 threads):
+// A token tile of 128 rows is split along K over S CTAs (S = 1 to 16, a power
+// of two) that form one thread-block cluster.  Per CTA (rank r, 320 threads):
 //   warp 0     TMA producer: per stage of 256 K-elements two bf16 x boxes
 //              (128 rows x 128 elements, 32 KB each) into a 3-slot ring, and
 //              the W tile (128 or 256 rows x 128 bytes, 128-byte swizzle) with
 //              its scale slabs into a 2-deep ring;
-//   warps 2-9  quantizers: each warp takes 16 token rows of a box, two rows
-//              per instruction (lanes 0-15 and 16-31); lane l holds 8 bf16 --
-//              half of a 16-element block, whose max comes from lane l ^ 1 by
-//              one shuffle -- and writes 4 bytes of codes into the A tile
-//              (128-byte swizzle, the layout TMA would have produced) and the
-//              block's scale byte into the stage's scale atoms.  Warps 2-5 then
-//              copy the x and W scale atoms into their tensor-memory quarter
-//              (tcgen05.st) and signal the MMA warp; the A tile is
-//              double-buffered and the warps synchronise only through
-//              mbarriers (a warp may run about a stage ahead of another);
-//   warp 1     MMA issuer: one tcgen05.mma.kind::mxf4nvf4 (M=128, N=128 or 256,
-//              K=64) per 64-element K step into one fp32 accumulator;
+//   warps 2-9  quantizers (quant_box): each warp takes 16 token rows of a box
+//              and writes their E2M1 codes into the A tile (128-byte swizzle,
+//              the layout TMA would have produced) and their scale bytes into
+//              the stage's scale atoms; the A tile is double-buffered and the
+//              warps synchronise only through mbarriers (a warp may run about
+//              a stage ahead of another);
+//   warp 1     MMA issuer: once all eight quantizer warps have filled the A
+//              slot, copies the stage's x and W scale atoms into tensor memory
+//              (tcgen05.cp, in order with the MMAs on the otherwise idle
+//              tensor pipe) and issues one tcgen05.mma.kind::mxf4nvf4 (M=128,
+//              N=128 or 256, K=64) per 64-element K step into one fp32
+//              accumulator;
 //   warps 2-9  after the last MMA: the fp32 partial (128 x 256) goes from
 //              tensor memory to partial plane r of the workspace (L2); after a
 //              cluster barrier each CTA routes its own 128/S tokens from the S
@@ -55,7 +57,10 @@ constexpr int kFASlot = kFACodes + kFASfa;
 constexpr int kFWRing = kFStagesW * kFWStage;
 constexpr int kFXRing = kFXSlots * kFXBox;
 constexpr int kFARing = kFASlots * kFASlot;
-constexpr int kFSmem = kFWRing + kFXRing + kFARing + 2048 /*scale table, barriers*/ + 1024 /*align*/;
+constexpr int kFByteTab = 2560;                     // scale bytes of bf16 block maxima (amax down ~20 binades)
+constexpr int kFFixQ = 256;                         // exact-pass queue entries per quantizer warp and box
+constexpr int kFTables = 1024 + 1024 + kFByteTab + 8 * kFFixQ * 2;   // s_scale, s_cc, s_byte, s_fixq
+constexpr int kFSmem = kFWRing + kFXRing + kFARing + kFTables + 512 /*barriers*/ + 1024 /*align*/;
 constexpr int kFThreads = 320;
 constexpr int kFRowsPerWarp = 16;
 static_assert(kFWStage % 1024 == 0 && kFASlot % 1024 == 0 && kFXBox % 1024 == 0, "1024-byte aligned tiles");
@@ -136,6 +141,169 @@ __device__ __forceinline__ void quant_rows(const uint4 (&v)[kG], const QuantScal
   }
 }
 
+// Mode-1 quantizer of kG rows by bracketing products: the scale bytes of
+// quant_rows<1, kG> and, wherever mism[i] is 0, its codes, at a quarter of its
+// multiply-adds.
+//   scale byte: a function of the block's max|x| alone (monotone), looked up
+//     in s_byte[], which holds it for every bf16 max from amax down by 2559
+//     steps (about 20 binades; anything smaller has a zero byte);
+//   code: with c = RN(1/gsa) * RN(1/s) (rounded) and c_lo/hi = c (1 -/+ 2^-20)
+//     (rounded), P_lo/hi = RN(x c_lo/hi) lie on both sides of the exact
+//     q = RN(RN(x / gsa) / s): each of them is within 5 ulp of x / (gsa s) and
+//     q within 2, far inside the 2^-20 margin (16 ulp).  E2M1 rounding is
+//     monotone, so where the two codes agree the exact code equals them.
+//     Where they differ (q within ~2^-20 of a rounding boundary, e.g. an exact
+//     tie), mism[i] != 0 and the row's codes must be recomputed exactly
+//     (quant_cell_exact).
+// s_cc[b] = (c_lo, c_hi) of scale byte b.
+template <int kG>
+__device__ __forceinline__ void quant_rows_bracket(const uint4 (&v)[kG], const uint8_t* s_byte, int byte_base,
+                                                   const float2* s_cc, uint32_t (&codes)[kG],
+                                                   uint32_t (&bytes)[kG], uint32_t (&mism)[kG]) {
+#pragma unroll
+  for (int i = 0; i < kG; ++i) {
+    // the block's max |x| as bf16 bits: this lane's 8 values, then its partner's
+    uint32_t m0, m1, m;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m0) : "r"(v[i].x & 0x7FFF7FFFu), "r"(v[i].y & 0x7FFF7FFFu));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m1) : "r"(v[i].z & 0x7FFF7FFFu), "r"(v[i].w & 0x7FFF7FFFu));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m0), "r"(m1));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(__shfl_xor_sync(0xFFFFFFFFu, m, 1)));
+    const int mb = static_cast<int>(max(m & 0xFFFFu, m >> 16));
+    bytes[i] = s_byte[min(max(mb - byte_base, 0), kFByteTab - 1)];
+  }
+#pragma unroll
+  for (int i = 0; i < kG; ++i) {
+    const float2 cc = s_cc[bytes[i]];
+    const uint64_t lo2 = f2_pack(cc.x, cc.x), hi2 = f2_pack(cc.y, cc.y);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    float a[8], b[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint64_t xp = f2_pack(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+      const uint64_t pl = f2_mul(xp, lo2), ph = f2_mul(xp, hi2);
+      a[2 * j] = f2_lo(pl); a[2 * j + 1] = f2_hi(pl);
+      b[2 * j] = f2_lo(ph); b[2 * j + 1] = f2_hi(ph);
+    }
+    const uint32_t c = e2m1_pack8(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+    mism[i] = c ^ e2m1_pack8(b[0], b[1], b[2], b[3], b[4], b[5], b[6], b[7]);
+    codes[i] = bytes[i] ? c | bf16x8_sign_nibbles(v[i].x, v[i].y, v[i].z, v[i].w) : 0u;
+  }
+}
+
+// Exact mode-1 codes of one row's 8 values (half a block) with a known
+// nonzero scale byte: y = RN(x / gsa) and q = RN(y / s) by the division
+// shortcuts, as in quant_rows<1, 1>.
+__device__ __forceinline__ uint32_t quant_cell_exact(const uint4 v, uint32_t byte, const QuantScale& qs,
+                                                     const float2* s_scale) {
+  const float2 sr = s_scale[byte];
+  const uint64_t ng2 = f2_pack(-qs.gsa, -qs.gsa), rg2 = f2_pack(qs.rgsa, qs.rgsa);
+  const uint64_t ns2 = f2_pack(-sr.x, -sr.x), rs2 = f2_pack(sr.y, sr.y);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float z[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t xp = f2_pack(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+    const uint64_t q = div_rn2_short(div_rn2(xp, ng2, rg2), ns2, rs2);
+    z[2 * j] = f2_lo(q);
+    z[2 * j + 1] = f2_hi(q);
+  }
+  return e2m1_pack8(z[0], z[1], z[2], z[3], z[4], z[5], z[6], z[7]) | bf16x8_sign_nibbles(v.x, v.y, v.z, v.w);
+}
+
+// Per-call quantizer constants and the shared-memory tables built from them.
+struct QuantTables {
+  QuantScale qs;
+  const float2* s_scale;     // [128] (dec(b), RN(1/dec(b)))
+  const float2* s_cc;        // [128] bracketing multipliers of byte b
+  const uint8_t* s_byte;     // [kFByteTab] scale byte of a bf16 block max
+  int byte_base;             // bf16 bits of s_byte[0]
+};
+
+// Stores of one 4-row group: each row's 4 code bytes into the A slot's
+// 128-byte swizzled layout (the one TMA would produce; box hs fills chunks
+// 4hs..4hs+3 of a row) and each block's scale byte into the slot's scale atoms.
+__device__ __forceinline__ void store_group(uint8_t* ac, uint8_t* asf, int hs, int row0, int sub, int l16,
+                                            const uint32_t (&codes)[4], const uint32_t (&bytes)[4]) {
+  const int j = 4 * hs + (l16 >> 2);                     // 16-byte chunk of the code row
+  const int c = 8 * hs + (l16 >> 1);                     // 16-element block of the stage
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = row0 + 2 * i + sub;
+    // codes: 4 bytes at chunk j ^ (r % 8), offset 4 * (l16 % 4)
+    st_shared_u32(ac + r * 128 + (((j ^ (r & 7)) << 4) | ((l16 & 3) << 2)), codes[i]);
+    // scale byte of block c: atom c/4, line r % 32, group (r/32) % 4, byte c % 4
+    if (!(l16 & 1))
+      st_shared_u8(asf + 512 * (c >> 2) + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (c & 3), bytes[i]);
+  }
+}
+
+// One quantizer warp's share of an x box (128 rows x 128 bf16, row stride 256
+// bytes): its 16 rows, two per instruction (lanes 0-15 and 16-31), lane l16
+// holding 8 values -- half of a 16-element block, whose other half sits in
+// lane ^ 1.  Rows at or past row_end are skipped, eight at a time.
+// fixq: this warp's exact-pass queue.  Mode 1 runs the bracketing quantizer
+// and then the exact pass over the queued rows; the other modes (IEEE
+// division, or gsa == 0: all codes zero) run in a loop of their own, so that
+// the hot loop holds no other code.
+__device__ __forceinline__ void quant_box(const uint8_t* xb, uint8_t* ac, uint8_t* asf, int hs, int qw, int lane,
+                                          int row_end, const QuantTables& tb, uint16_t* fixq) {
+  const QuantScale& qs = tb.qs;
+  const int sub = lane >> 4, l16 = lane & 15;
+  if (qs.mode != 1) {
+#pragma unroll 1
+    for (int g = 0; g < kFRowsPerWarp / 2; g += 4) {
+      if (qw * kFRowsPerWarp + 2 * g >= row_end) break;
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
+      uint32_t codes[4] = {0u, 0u, 0u, 0u}, bytes[4] = {0u, 0u, 0u, 0u};
+      if (qs.mode == 2) quant_rows<2, 4>(v, qs, tb.s_scale, codes, bytes);
+      store_group(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
+    }
+    return;
+  }
+  uint32_t n_fix = 0;                                      // queued rows (warp-uniform)
+#pragma unroll
+  for (int g = 0; g < kFRowsPerWarp / 2; g += 4) {
+    // rows past T only feed accumulator rows that are never stored: a group
+    // that starts past T is skipped (warp-uniform)
+    if (qw * kFRowsPerWarp + 2 * g >= row_end) break;
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
+    uint32_t codes[4], bytes[4], mism[4];
+    quant_rows_bracket<4>(v, tb.s_byte, tb.byte_base, tb.s_cc, codes, bytes, mism);
+    // rows whose bracketing codes differ go to the exact pass:
+    // entry = row pair (3 bits) | lane (5 bits) | scale byte << 8
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool need = mism[i] != 0u;
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, need);
+      if (need)
+        fixq[n_fix + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>((g + i) | (lane << 3) | (bytes[i] << 8));
+      n_fix += __popc(bal);
+    }
+    store_group(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
+  }
+  if (n_fix) {
+    // exact pass over the queued rows, one lane per row; the box is still in
+    // shared memory (the caller releases it afterwards)
+    __syncwarp();
+    for (uint32_t e0 = 0; e0 < n_fix; e0 += 32) {
+      if (e0 + lane < n_fix) {
+        const uint32_t ent = fixq[e0 + lane];
+        const int ln = (ent >> 3) & 31, l = ln & 15;
+        const int r = qw * kFRowsPerWarp + 2 * static_cast<int>(ent & 7u) + (ln >> 4);
+        const uint32_t code = quant_cell_exact(ld_shared_v4(xb + r * 256 + 16 * l), ent >> 8, qs, tb.s_scale);
+        const int j = 4 * hs + (l >> 2);
+        st_shared_u32(ac + r * 128 + (((j ^ (r & 7)) << 4) | ((l & 3) << 2)), code);
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kFThreads, 1)
 fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -144,12 +312,14 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   uint8_t* xring = wring + kFWRing;
   uint8_t* aring = xring + kFXRing;
   float2* s_scale = reinterpret_cast<float2*>(aring + kFARing);        // [128] (dec(b), RN(1/dec(b)))
-  uint64_t* full_w = reinterpret_cast<uint64_t*>(s_scale + 128);
+  float2* s_cc = s_scale + 128;                                         // [128] (c_lo, c_hi) of byte b
+  uint8_t* s_byte = reinterpret_cast<uint8_t*>(s_cc + 128);             // [kFByteTab] scale byte of a block max
+  uint16_t* s_fixq = reinterpret_cast<uint16_t*>(s_byte + kFByteTab);   // [8][kFFixQ] rows for the exact pass
+  uint64_t* full_w = reinterpret_cast<uint64_t*>(s_fixq + 8 * kFFixQ);
   uint64_t* empty_w = full_w + kFStagesW;
   uint64_t* full_x = empty_w + kFStagesW;
   uint64_t* empty_x = full_x + kFXSlots;
-  uint64_t* a_full = empty_x + kFXSlots;
-  uint64_t* a_empty = a_full + kFASlots;
+  uint64_t* a_empty = empty_x + kFXSlots;
   uint64_t* q_done = a_empty + kFASlots;                               // [kFASlots]
   uint64_t* acc_full = q_done + kFASlots;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -169,7 +339,6 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     for (int s = 0; s < kFStagesW; ++s) { mbar_init(full_w + s, 1); mbar_init(empty_w + s, 1); }
     for (int s = 0; s < kFXSlots; ++s) { mbar_init(full_x + s, 1); mbar_init(empty_x + s, 8); }
     for (int a = 0; a < kFASlots; ++a) {
-      mbar_init(a_full + a, 4);
       mbar_init(a_empty + a, 1);
       mbar_init(q_done + a, 8);
     }
@@ -256,7 +425,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       for (int s = 0; s < my_st; ++s) {
         const int slot = s & 1;
         const uint32_t aph = (s >> 1) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(a_full + slot, aph, deadline, abort_flag) &&
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(q_done + slot, aph, deadline, abort_flag) &&
                                          mbar_wait(full_w + wst, wph, deadline, abort_flag))) {
           ok = false;
           break;
@@ -268,6 +437,13 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         const uint8_t* b = wring + wst * kFWStage;
         const uint32_t sf_t = tmem + 256 + slot * 48;
         if (elect_one()) {
+          // the stage's scale atoms into tensor memory (in order with the
+          // MMAs on the tensor pipe): x at +4 kk, W half h at +16 + 8 kk + 4 h
+          for (int kk = 0; kk < nkk; ++kk) {
+            tc_copy_scales(sf_t + 4 * kk, desc_scale_tile(smem_u32(a + kFACodes + 512 * kk)));
+            for (int h = 0; h < p.n_half; ++h)
+              tc_copy_scales(sf_t + 16 + 8 * kk + 4 * h, desc_scale_tile(smem_u32(b + kFWTile + 2048 * h + 512 * kk)));
+          }
           for (int kk = 0; kk < nkk; ++kk)
             tc_mma_nvf4(tmem, desc_kmajor_sw128(smem_u32(a + 32 * kk)), desc_kmajor_sw128(smem_u32(b + 32 * kk)),
                         idesc, sf_t + 4 * kk, sf_t + 16 + 8 * kk, (s | kk) != 0);
@@ -293,10 +469,32 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     qs.rgsa = __ldg(p.qrec + 1);
     qs.mode = __float_as_int(__ldg(p.qrec + 2));
     const int qw = warp - 2;
-    const int sub = lane >> 4, l16 = lane & 15;       // row of the pair, lane within the row
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    int wst = 0;
-    uint32_t wph = 0;
+    // bracketing quantizer (mode 1): the scale byte of every bf16 block max
+    // within ~20 binades below amax, and the bracketing multipliers per byte
+    const int byte_base = static_cast<int>(__float_as_uint(__ldg(p.qrec + 3)) >> 16) - (kFByteTab - 1);
+    if (qs.mode == 1) {
+      const float r6 = 0.16666667163372039794921875f;       // RN(1/6)
+      const int qt = static_cast<int>(threadIdx.x) - 64;   // 0..255 over the quantizer warps
+      for (int i = qt; i < kFByteTab; i += 256) {
+        const int b16 = byte_base + i;
+        const float mx = __uint_as_float(static_cast<uint32_t>(max(b16, 0)) << 16);
+        s_byte[i] = static_cast<uint8_t>(e4m3_byte(div_rn_short(div_rn(mx, qs.gsa, qs.rgsa), 6.0f, r6)));
+      }
+      if (qt < 128) {
+        const int b = qt;
+        const bool ok = b >= 1 && b <= 126;
+        const float c = __fmul_rn(qs.rgsa, ok ? __frcp_rn(e4m3_value(b)) : 0.0f);
+        s_cc[b] = make_float2(__fmul_rn(c, 0.99999904632568359375f),     // 1 - 2^-20
+                              __fmul_rn(c, 1.00000095367431640625f));    // 1 + 2^-20
+      }
+    }
+    bar_and(2, 256, true);
+    QuantTables tb;
+    tb.qs = qs;
+    tb.s_scale = s_scale;
+    tb.s_cc = s_cc;
+    tb.s_byte = s_byte;
+    tb.byte_base = byte_base;
     bool ok = true;
     for (int s = 0; s < my_st; ++s) {
       const int slot = s & 1;
@@ -315,37 +513,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         const bool okx = __all_sync(0xFFFFFFFFu, mbar_wait(full_x + xs, xph, deadline, abort_flag));
         ok = ok && okx;
         if (okx) {
-          const uint8_t* xb = xring + xs * kFXBox;
-#pragma unroll
-          for (int g = 0; g < kFRowsPerWarp / 2; g += 4) {
-            // rows past T only feed accumulator rows that are never stored:
-            // a group that starts past T is skipped (warp-uniform)
-            if (m_tile * 128 + qw * kFRowsPerWarp + 2 * g >= p.T) break;
-            uint4 v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
-            uint32_t codes[4], bytes[4];
-            if (qs.mode == 1) {
-              quant_rows<1, 4>(v, qs, s_scale, codes, bytes);
-            } else if (qs.mode == 2) {
-              quant_rows<2, 4>(v, qs, s_scale, codes, bytes);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) { codes[i] = 0u; bytes[i] = 0u; }
-            }
-            const int j = 4 * hs + (l16 >> 2);                     // 16-byte chunk of the code row
-            const int c = 8 * hs + (l16 >> 1);                     // 16-element block of the stage
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = qw * kFRowsPerWarp + 2 * (g + i) + sub;
-              // codes: 4 bytes at chunk j ^ (r % 8), offset 4 * (l16 % 4) (128-byte swizzle)
-              st_shared_u32(ac + r * 128 + (((j ^ (r & 7)) << 4) | ((l16 & 3) << 2)), codes[i]);
-              // scale byte of block c: atom c/4, line r % 32, group (r/32) % 4, byte c % 4
-              if (!(l16 & 1))
-                st_shared_u8(asf + 512 * (c >> 2) + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (c & 3), bytes[i]);
-            }
-          }
+          quant_box(xring + xs * kFXBox, ac, asf, hs, qw, lane, p.T - m_tile * 128, tb, s_fixq + qw * kFFixQ);
         }
         // this warp has read its rows of the box
         __syncwarp();
@@ -355,40 +523,6 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_done + slot);
-      if (warp < 6) {
-        // ---- scale stagers: once all eight warps have written the slot, the
-        // x and W scale atoms go into this warp's tensor-memory quarter
-        const bool okw = __all_sync(0xFFFFFFFFu, mbar_wait(q_done + slot, aph, deadline, abort_flag) &&
-                                                     mbar_wait(full_w + wst, wph, deadline, abort_flag));
-        if (okw) {
-          const uint8_t* sb = wring + wst * kFWStage + kFWTile;
-          uint32_t va[16], vb0[16], vb1[16];
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint4 t = ld_shared_v4(asf + 512 * kk + 16 * lane);
-            va[4 * kk] = t.x; va[4 * kk + 1] = t.y; va[4 * kk + 2] = t.z; va[4 * kk + 3] = t.w;
-          }
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            uint32_t* dst = kk < 2 ? vb0 : vb1;
-            const int o = 8 * (kk & 1);
-            const uint4 t0 = ld_shared_v4(sb + 512 * kk + 16 * lane);
-            const uint4 t1 = ld_shared_v4(sb + 2048 + 512 * kk + 16 * lane);
-            dst[o] = t0.x; dst[o + 1] = t0.y; dst[o + 2] = t0.z; dst[o + 3] = t0.w;
-            dst[o + 4] = t1.x; dst[o + 5] = t1.y; dst[o + 6] = t1.z; dst[o + 7] = t1.w;
-          }
-          const uint32_t t0 = tmem + lane_base + 256 + slot * 48;
-          tmem_store16(t0, va);
-          tmem_store16(t0 + 16, vb0);
-          tmem_store16(t0 + 32, vb1);
-          tmem_store_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(a_full + slot);
-        }
-        ok = ok && okw;
-      }
-      if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
     }
     if (!ok && lane == 0) {
       report_timeout(p.status);
