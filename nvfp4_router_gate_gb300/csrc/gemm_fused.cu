@@ -146,7 +146,8 @@ __device__ __forceinline__ void quant_rows(const uint4 (&v)[kG], const QuantScal
 // multiply-adds.
 //   scale byte: a function of the block's max|x| alone (monotone), looked up
 //     in s_byte[], which holds it for every bf16 max from amax down by 2559
-//     steps (about 20 binades; anything smaller has a zero byte);
+//     steps (about 20 binades; anything smaller has a zero byte, as has the
+//     last entry);
 //   code: with c = RN(1/gsa) * RN(1/s) (rounded) and c_lo/hi = c (1 -/+ 2^-20)
 //     (rounded), P_lo/hi = RN(x c_lo/hi) lie on both sides of the exact
 //     q = RN(RN(x / gsa) / s): each of them is within 5 ulp of x / (gsa s) and
@@ -155,21 +156,31 @@ __device__ __forceinline__ void quant_rows(const uint4 (&v)[kG], const QuantScal
 //     Where they differ (q within ~2^-20 of a rounding boundary, e.g. an exact
 //     tie), mism[i] != 0 and the row's codes must be recomputed exactly
 //     (quant_cell_exact).
+//   sign of zero: an element that rounds to zero gets code 0x0 whatever its
+//     sign (the conversion drops it; the standalone quantizer restores 0x8).
+//     A zero code adds +-0 to the tensor-core dot product, which changes
+//     nothing but the sign of an all-zero sum, and sigmoid(+0) = sigmoid(-0):
+//     the router's scores, ids and weights are the same.
 // s_cc[b] = (c_lo, c_hi) of scale byte b.
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t d;   // magnitude max(|a|, |b|) per half (the sign bit is the xor of the inputs')
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 template <int kG>
-__device__ __forceinline__ void quant_rows_bracket(const uint4 (&v)[kG], const uint8_t* s_byte, int byte_base,
+__device__ __forceinline__ void quant_rows_bracket(const uint4 (&v)[kG], const uint8_t* s_byte, uint32_t amax_b16,
                                                    const float2* s_cc, uint32_t (&codes)[kG],
                                                    uint32_t (&bytes)[kG], uint32_t (&mism)[kG]) {
 #pragma unroll
   for (int i = 0; i < kG; ++i) {
-    // the block's max |x| as bf16 bits: this lane's 8 values, then its partner's
-    uint32_t m0, m1, m;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(m0) : "r"(v[i].x & 0x7FFF7FFFu), "r"(v[i].y & 0x7FFF7FFFu));
-    asm("max.u16x2 %0, %1, %2;" : "=r"(m1) : "r"(v[i].z & 0x7FFF7FFFu), "r"(v[i].w & 0x7FFF7FFFu));
-    asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m0), "r"(m1));
-    asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(__shfl_xor_sync(0xFFFFFFFFu, m, 1)));
-    const int mb = static_cast<int>(max(m & 0xFFFFu, m >> 16));
-    bytes[i] = s_byte[min(max(mb - byte_base, 0), kFByteTab - 1)];
+    // the block's max |x| (bf16 magnitude bits): this lane's 8 values, then
+    // its partner's, then the two halves (finite inputs: mode 1)
+    uint32_t m = bf16x2_max_abs(bf16x2_max_abs(v[i].x, v[i].y), bf16x2_max_abs(v[i].z, v[i].w));
+    m = bf16x2_max_abs(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = bf16x2_max_abs(m, __byte_perm(m, 0u, 0x1032));
+    // s_byte[d] holds the byte of the block max with bf16 bits amax - d
+    bytes[i] = s_byte[min(amax_b16 - (m & 0x7FFFu), static_cast<uint32_t>(kFByteTab - 1))];
   }
 #pragma unroll
   for (int i = 0; i < kG; ++i) {
@@ -186,13 +197,14 @@ __device__ __forceinline__ void quant_rows_bracket(const uint4 (&v)[kG], const u
     }
     const uint32_t c = e2m1_pack8(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
     mism[i] = c ^ e2m1_pack8(b[0], b[1], b[2], b[3], b[4], b[5], b[6], b[7]);
-    codes[i] = bytes[i] ? c | bf16x8_sign_nibbles(v[i].x, v[i].y, v[i].z, v[i].w) : 0u;
+    codes[i] = bytes[i] ? c : 0u;
   }
 }
 
 // Exact mode-1 codes of one row's 8 values (half a block) with a known
 // nonzero scale byte: y = RN(x / gsa) and q = RN(y / s) by the division
-// shortcuts, as in quant_rows<1, 1>.
+// shortcuts, as in quant_rows<1, 1> (zero codes unsigned, as in
+// quant_rows_bracket).
 __device__ __forceinline__ uint32_t quant_cell_exact(const uint4 v, uint32_t byte, const QuantScale& qs,
                                                      const float2* s_scale) {
   const float2 sr = s_scale[byte];
@@ -207,7 +219,7 @@ __device__ __forceinline__ uint32_t quant_cell_exact(const uint4 v, uint32_t byt
     z[2 * j] = f2_lo(q);
     z[2 * j + 1] = f2_hi(q);
   }
-  return e2m1_pack8(z[0], z[1], z[2], z[3], z[4], z[5], z[6], z[7]) | bf16x8_sign_nibbles(v.x, v.y, v.z, v.w);
+  return e2m1_pack8(z[0], z[1], z[2], z[3], z[4], z[5], z[6], z[7]);
 }
 
 // Per-call quantizer constants and the shared-memory tables built from them.
@@ -216,7 +228,7 @@ struct QuantTables {
   const float2* s_scale;     // [128] (dec(b), RN(1/dec(b)))
   const float2* s_cc;        // [128] bracketing multipliers of byte b
   const uint8_t* s_byte;     // [kFByteTab] scale byte of a bf16 block max
-  int byte_base;             // bf16 bits of s_byte[0]
+  uint32_t amax_b16;         // bf16 bits of amax: s_byte[d] is for amax_b16 - d
 };
 
 // Stores of one 4-row group: each row's 4 code bytes into the A slot's
@@ -274,7 +286,7 @@ __device__ __forceinline__ void quant_box(const uint8_t* xb, uint8_t* ac, uint8_
     for (int i = 0; i < 4; ++i)
       v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
     uint32_t codes[4], bytes[4], mism[4];
-    quant_rows_bracket<4>(v, tb.s_byte, tb.byte_base, tb.s_cc, codes, bytes, mism);
+    quant_rows_bracket<4>(v, tb.s_byte, tb.amax_b16, tb.s_cc, codes, bytes, mism);
     // rows whose bracketing codes differ go to the exact pass:
     // entry = row pair (3 bits) | lane (5 bits) | scale byte << 8
 #pragma unroll
@@ -360,8 +372,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   const uint32_t tmem = *tmem_holder;
   // the amax kernel before us (programmatic launch) must have finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The next call's amax kernel may start streaming its input now: it
-  // publishes its results only after this grid has finished.
+  // The next kernel of the stream may launch now; it waits for this grid to
+  // complete before it reads anything.
   asm volatile("griddepcontrol.launch_dependents;");
   const uint64_t deadline = globaltimer_ns() + 1000000000ull;   // 1 s
 
@@ -471,12 +483,12 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     const int qw = warp - 2;
     // bracketing quantizer (mode 1): the scale byte of every bf16 block max
     // within ~20 binades below amax, and the bracketing multipliers per byte
-    const int byte_base = static_cast<int>(__float_as_uint(__ldg(p.qrec + 3)) >> 16) - (kFByteTab - 1);
+    const uint32_t amax_b16 = __float_as_uint(__ldg(p.qrec + 3)) >> 16;     // bf16 bits of amax
     if (qs.mode == 1) {
       const float r6 = 0.16666667163372039794921875f;       // RN(1/6)
       const int qt = static_cast<int>(threadIdx.x) - 64;   // 0..255 over the quantizer warps
       for (int i = qt; i < kFByteTab; i += 256) {
-        const int b16 = byte_base + i;
+        const int b16 = static_cast<int>(amax_b16) - i;
         const float mx = __uint_as_float(static_cast<uint32_t>(max(b16, 0)) << 16);
         s_byte[i] = static_cast<uint8_t>(e4m3_byte(div_rn_short(div_rn(mx, qs.gsa, qs.rgsa), 6.0f, r6)));
       }
@@ -494,7 +506,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     tb.s_scale = s_scale;
     tb.s_cc = s_cc;
     tb.s_byte = s_byte;
-    tb.byte_base = byte_base;
+    tb.amax_b16 = amax_b16;
     bool ok = true;
     for (int s = 0; s < my_st; ++s) {
       const int slot = s & 1;

@@ -90,12 +90,12 @@ amax_kernel(const void* __restrict__ x, int64_t n_vec16, uint32_t* __restrict__ 
 // which is what a pure HBM stream needs.  Waits on the ring are bounded
 // (about a second); a timeout is recorded in the status word.
 //
-// Overlap with the previous call: the kernel is launched with programmatic
-// dependent launch and reads nothing the previous kernels of the stream
-// write, so it may stream x while they finish.  Its last CTA waits for them
-// (griddepcontrol.wait) before it publishes gsa and the quantizer record:
-// the previous call's consumers have read theirs, and this grid completes
-// only after its predecessor, which keeps the next kernel's wait transitive.
+// Launched with programmatic dependent launch: the grid may become resident
+// while the previous kernel of the stream finishes, but it waits for it
+// (griddepcontrol.wait: completed, its writes visible) before it reads x --
+// the previous kernel may be the one that produced x -- or touches the
+// workspace.  Each CTA lets the next kernel launch once its share of x has
+// been read.
 constexpr int kAmaxChunk = 32 * 1024;
 constexpr int kAmaxStages = 4;
 
@@ -125,6 +125,10 @@ amax_bulk_kernel(const uint8_t* __restrict__ x, int64_t nbytes, uint32_t* __rest
   if (threadIdx.x == 0) {
     for (int st = 0; st < kAmaxStages; ++st) mbar_init(full + st, 1);
     fence_mbar_init();
+  }
+  // x and the workspace counters may be written by the previous kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) {
     for (int st = 0; st < kAmaxStages; ++st) grab_and_issue(st, fills);
   }
   __syncthreads();
@@ -186,8 +190,6 @@ amax_bulk_kernel(const uint8_t* __restrict__ x, int64_t nbytes, uint32_t* __rest
   for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = b;
   __syncthreads();
-  // the previous kernels of the stream have finished (see above)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
     uint32_t r = 0;
     for (int w = 0; w < kAmaxThreads / 32; ++w) r = max(r, red[w]);
