@@ -165,9 +165,9 @@ def job_throughput(world, tokens_per_rank, steps, max_ms):
 
 def kernel_names(path):
     """Launches of one router call: bf16 activations on a head of <= 256
-    experts run amax, then one kernel with the quantization, the GEMM and the
-    router epilogue; the decode path is one kernel."""
-    return ["amax", "gemm"] if path == "tc" else ["decode_router"]
+    experts whose token tiles all fit on the GPU at once run one kernel (max|x|,
+    quantization, GEMM and router epilogue); the decode path is one kernel."""
+    return ["fused"] if path == "tc" else ["decode_router"]
 
 
 def algorithmic(w, T, name):
@@ -181,7 +181,7 @@ def algorithmic(w, T, name):
         return x_bytes, 0
     if name == "quantize":
         return x_bytes + xq, 0
-    if name == "gemm":                     # quantizes x inside (reads bf16 x), routes, writes ids/weights
+    if name in ("gemm", "fused"):          # x (bf16) once from HBM, W, bias, ids/weights
         return x_bytes + wq + N * 4 + out, 2 * T * D * N
     if name == "epilogue":
         return T * N * 4 + N * 4 + out, 0                      # the logits read once, bias, outputs

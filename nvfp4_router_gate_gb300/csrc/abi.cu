@@ -221,11 +221,6 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   uint32_t* status = reinterpret_cast<uint32_t*>(w + kWsStatus);
   const bool stall = (flags & NVR_FLAG_TEST_STALL) != 0;
   ProfileScope prof(s);
-  prof.before();
-  cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
-                                   reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec, status, sms, s);
-  prof.after();
-  if (e != cudaSuccess) return cuda_status(e);
   // Up to 256 experts: K split over S CTAs with one tensor-core accumulator
   // for the whole row each; bf16 activations are quantized inside the GEMM
   // and routed in the same kernel, fp32 ones take the standalone quantizer,
@@ -245,12 +240,30 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
       if (c > split_k) continue;
       if (forced_split || fused_cluster_capacity(c) >= m_tiles) { S = c; break; }
     }
+    // the whole grid resident at once: the kernel computes max|x| itself (one
+    // launch, x's second pass from L2); else the amax kernel runs first
+    const bool one_launch = fused_cluster_capacity(S) >= m_tiles;
+    if (!one_launch) {
+      prof.before();
+      const cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
+                                             reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec, status,
+                                             sms, s);
+      prof.after();
+      if (e != cudaSuccess) return cuda_status(e);
+    }
     prof.before();
-    st = launch_fused_router(static_cast<const uint16_t*>(x), qrec, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k,
-                             routed_scaling, raw, out_ids, out_w, logits, partials, status, S, stall, s);
+    st = launch_fused_router(static_cast<const uint16_t*>(x), qrec, x_gsa,
+                             one_launch ? reinterpret_cast<uint32_t*>(w + kWsFusedAmax) : nullptr, T, D, W_fp4,
+                             W_sf, w_gsa, N, bias, k, routed_scaling, raw, out_ids, out_w, logits, partials, status,
+                             S, stall, s);
     prof.after();
     return st;
   }
+  prof.before();
+  cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
+                                   reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec, status, sms, s);
+  prof.after();
+  if (e != cudaSuccess) return cuda_status(e);
   prof.before();
   e = launch_quantize(x, bf16, T, D, true, qrec, xc, xsf, s);
   prof.after();

@@ -69,7 +69,10 @@ static_assert(8 * 8192 <= kFXRing, "store staging fits the x ring");
 struct FusedParams {
   CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
   CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 x (128 * n_half)
-  const float* qrec;           // quantizer record {gsa, 1/gsa, mode, amax} from the amax kernel
+  float* qrec;                 // quantizer record {gsa, 1/gsa, mode, amax}: from the amax kernel, or
+                               // published by this kernel's last CTA when amax_sync is set
+  uint32_t* amax_sync;         // in-kernel amax: 4 workspace words (grid_amax), or null
+  float* gsa_out;              // in-kernel amax: x's global scale (also x_gsa)
   const uint8_t* sfb;          // W scales, tile layout
   float* partials;             // [S][T][256] fp32 partial logits (workspace)
   int T, D, N, n_half, S;
@@ -91,6 +94,41 @@ __device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t v) {
 }
 __device__ __forceinline__ void st_shared_u8(uint8_t* p, uint32_t v) {
   asm volatile("st.shared.u8 [%0], %1;" :: "r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide max |x| bits, for one thread per CTA, over 4 workspace words:
+// sync[0..1] the max of calls of even / odd generation, sync[2] arrivals,
+// sync[3] the generation.  A CTA folds its max into its generation's slot and
+// arrives (release); the last to arrive (acquire) resets the arrivals and the
+// other generation's slot -- the next call's, untouched until this grid has
+// finished -- and opens the barrier by bumping the generation (release); the
+// others wait for it (acquire, bounded).  Every CTA then reads the complete
+// max.  All CTAs of the grid must be resident.
+__device__ bool grid_amax(uint32_t* sync, uint32_t cta_max, uint32_t n_ctas, uint32_t& amax_bits,
+                          uint64_t deadline, volatile int* abort_flag) {
+  const uint32_t gen = ld_acquire_gpu(sync + 3);
+  uint32_t* slot = sync + (gen & 1u);
+  uint32_t t;
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" :: "l"(slot), "r"(cta_max) : "memory");
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(sync + 2) : "memory");
+  if (t == n_ctas - 1) {
+    sync[(gen + 1u) & 1u] = 0u;
+    sync[2] = 0u;
+    st_release_gpu(sync + 3, gen + 1u);
+  } else {
+    while (ld_acquire_gpu(sync + 3) == gen)
+      if (*abort_flag || globaltimer_ns() > deadline) return false;
+  }
+  amax_bits = ld_acquire_gpu(slot);
+  return true;
 }
 
 // Quantize kG rows of one stage, 8 bf16 values (half of a 16-element block;
@@ -385,11 +423,16 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     int wst = 0;
     uint32_t wph = 0;
     bool ok = true;
+    int xi = 0;                                        // x boxes issued so far
+    // with the in-kernel amax the CTA's boxes stream twice: for the max, then
+    // (from L2) for the GEMM; the second pass follows the first without a
+    // pause, its loads overlapping the grid barrier
+    for (int pass = p.amax_sync ? 0 : 1; pass < 2 && ok; ++pass)
     for (int s = 0; s < my_st && ok; ++s) {
       const int ks = st0 + s;
       // the stage's two x boxes (a box past D or T reads zeros)
-      for (int hs = 0; hs < 2; ++hs) {
-        const int xi = 2 * s + hs, xs = xi % kFXSlots;
+      for (int hs = 0; hs < 2; ++hs, ++xi) {
+        const int xs = xi % kFXSlots;
         const uint32_t xph = (xi / kFXSlots) & 1;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_x + xs, xph ^ 1u, deadline, abort_flag))) {
           ok = false;
@@ -404,6 +447,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         bits_x = (bits_x & ~(1u << xs)) | (xph << xs);
       }
       if (!ok) break;
+      if (pass == 0) continue;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_w + wst, wph ^ 1u, deadline, abort_flag))) {
         ok = false;
         break;
@@ -475,29 +519,89 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   } else {
     // ---------------------------------------------------------- quantizers
     rt.init(p.bias, p.N, p.k, p.raw, p.routed_scaling, lane);       // for the epilogue
-    gscale = __fmul_rn(__ldg(p.x_gsa), __ldg(p.w_gsa));
-    QuantScale qs;
-    qs.gsa = __ldg(p.qrec);
-    qs.rgsa = __ldg(p.qrec + 1);
-    qs.mode = __float_as_int(__ldg(p.qrec + 2));
     const int qw = warp - 2;
+    bool ok = true;
+    int xi = 0;                                        // x boxes consumed so far
+    if (p.amax_sync) {
+      // ---- in-kernel amax: max |x| over this CTA's boxes (the same
+      // bit-pattern max as the amax kernel), then the grid-wide record
+      uint32_t m = 0;
+      const int sub = lane >> 4, l16 = lane & 15;
+      for (int s = 0; s < my_st && ok; ++s) {
+        for (int hs = 0; hs < 2; ++hs, ++xi) {
+          const int xs = xi % kFXSlots;
+          const uint32_t xph = (xi / kFXSlots) & 1;
+          const bool okx = __all_sync(0xFFFFFFFFu, mbar_wait(full_x + xs, xph, deadline, abort_flag));
+          ok = ok && okx;
+          if (okx) {
+            const uint8_t* xb = xring + xs * kFXBox + (qw * kFRowsPerWarp + sub) * 256 + 16 * l16;
+#pragma unroll
+            for (int i = 0; i < kFRowsPerWarp / 2; ++i)
+              m = max(m, absmax_bits16B<true>(ld_shared_v4(xb + 512 * i)));
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_x + xs);
+          if (!okx) break;
+        }
+      }
+      m = __reduce_max_sync(0xFFFFFFFFu, m);
+      uint32_t* s_wmax = reinterpret_cast<uint32_t*>(s_fixq);     // the queue is not in use yet
+      if (lane == 0) s_wmax[qw] = m;
+      ok = bar_and(3, 256, ok);
+      bool gok = true;
+      if (threadIdx.x == 64 && ok) {
+        uint32_t cm = 0;
+        for (int w = 0; w < 8; ++w) cm = max(cm, s_wmax[w]);
+        uint32_t bits = 0;
+        gok = grid_amax(p.amax_sync, cm, gridDim.x, bits, deadline, abort_flag);
+        s_wmax[8] = bits;
+        if (!gok) {
+          report_timeout(p.status);
+          *abort_flag = 1;
+        }
+      }
+      ok = bar_and(3, 256, ok && gok);                 // thread 64's outcome, for every warp
+    }
+    // the quantizer record: derived here from the grid's max (the amax
+    // kernel's arithmetic; CTA 0 also stores it), or the amax kernel's
+    QuantScale qs;
+    float amax;
+    if (p.amax_sync) {
+      amax = __uint_as_float(reinterpret_cast<const uint32_t*>(s_fixq)[8]);
+      qs = make_quant_scale(amax);
+      if (blockIdx.x == 0 && threadIdx.x == 64) {
+        p.qrec[0] = qs.gsa;
+        p.qrec[1] = qs.rgsa;
+        p.qrec[2] = __int_as_float(qs.mode);
+        p.qrec[3] = amax;
+        *p.gsa_out = qs.gsa;
+      }
+      gscale = __fmul_rn(qs.gsa, __ldg(p.w_gsa));
+    } else {
+      qs.gsa = __ldg(p.qrec);
+      qs.rgsa = __ldg(p.qrec + 1);
+      qs.mode = __float_as_int(__ldg(p.qrec + 2));
+      amax = __ldg(p.qrec + 3);
+      gscale = __fmul_rn(__ldg(p.x_gsa), __ldg(p.w_gsa));
+    }
     // bracketing quantizer (mode 1): the scale byte of every bf16 block max
     // within ~20 binades below amax, and the bracketing multipliers per byte
-    const uint32_t amax_b16 = __float_as_uint(__ldg(p.qrec + 3)) >> 16;     // bf16 bits of amax
+    const uint32_t amax_b16 = __float_as_uint(amax) >> 16;                  // bf16 bits of amax
     if (qs.mode == 1) {
       const float r6 = 0.16666667163372039794921875f;       // RN(1/6)
       const int qt = static_cast<int>(threadIdx.x) - 64;   // 0..255 over the quantizer warps
-      for (int i = qt; i < kFByteTab; i += 256) {
+      static_assert(kFByteTab % 256 == 0, "whole rounds of the table");
+#pragma unroll
+      for (int j = 0; j < kFByteTab / 256; ++j) {          // independent entries: their latencies overlap
+        const int i = qt + 256 * j;
         const int b16 = static_cast<int>(amax_b16) - i;
         const float mx = __uint_as_float(static_cast<uint32_t>(max(b16, 0)) << 16);
         s_byte[i] = static_cast<uint8_t>(e4m3_byte(div_rn_short(div_rn(mx, qs.gsa, qs.rgsa), 6.0f, r6)));
       }
       if (qt < 128) {
-        const int b = qt;
-        const bool ok = b >= 1 && b <= 126;
-        const float c = __fmul_rn(qs.rgsa, ok ? __frcp_rn(e4m3_value(b)) : 0.0f);
-        s_cc[b] = make_float2(__fmul_rn(c, 0.99999904632568359375f),     // 1 - 2^-20
-                              __fmul_rn(c, 1.00000095367431640625f));    // 1 + 2^-20
+        const float c = __fmul_rn(qs.rgsa, s_scale[qt].y);   // RN(1/dec(b)), 0 for bytes 0 and 127
+        s_cc[qt] = make_float2(__fmul_rn(c, 0.99999904632568359375f),     // 1 - 2^-20
+                               __fmul_rn(c, 1.00000095367431640625f));    // 1 + 2^-20
       }
     }
     bar_and(2, 256, true);
@@ -507,7 +611,6 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     tb.s_cc = s_cc;
     tb.s_byte = s_byte;
     tb.amax_b16 = amax_b16;
-    bool ok = true;
     for (int s = 0; s < my_st; ++s) {
       const int slot = s & 1;
       const uint32_t aph = (s >> 1) & 1;
@@ -519,8 +622,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       }
       uint8_t* ac = aring + slot * kFASlot;
       uint8_t* asf = ac + kFACodes;
-      for (int hs = 0; hs < 2; ++hs) {
-        const int xi = 2 * s + hs, xs = xi % kFXSlots;
+      for (int hs = 0; hs < 2; ++hs, ++xi) {
+        const int xs = xi % kFXSlots;
         const uint32_t xph = (xi / kFXSlots) & 1;
         const bool okx = __all_sync(0xFFFFFFFFu, mbar_wait(full_x + xs, xph, deadline, abort_flag));
         ok = ok && okx;
@@ -658,7 +761,7 @@ int fused_cluster_capacity(int S) {
   return n;
 }
 
-nvr_status launch_fused_router(const uint16_t* x, const float* qrec, const float* x_gsa, int64_t T, int64_t D,
+nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
@@ -675,6 +778,7 @@ nvr_status launch_fused_router(const uint16_t* x, const float* qrec, const float
   if (!encode_x(&g.tmap_x, x, T, D)) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes(&g.tmap_b, W_codes, N, D, 128u * n_half)) return NVR_ERR_UNSUPPORTED;
   g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
+  g.amax_sync = amax_sync; g.gsa_out = x_gsa;
   g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_half = n_half; g.S = S;
   g.x_gsa = x_gsa; g.w_gsa = w_gsa; g.bias = raw ? nullptr : bias;
   g.k = k; g.raw = raw ? 1 : 0; g.routed_scaling = routed_scaling;

@@ -93,12 +93,15 @@ int plan_splitk(int64_t T, int64_t D, int num_sms);
 nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64_t T, int64_t D,
                               const uint8_t* W_codes, const uint8_t* W_sf, int64_t N, float* partials,
                               uint32_t* status, int S, bool test_stall, cudaStream_t s);
-// The whole router after the amax kernel for bf16 activations and N <= 256:
-// quantization inside the K-split GEMM, partials through L2 and the epilogue
-// in the same kernel (cluster of S CTAs per 128-token tile, S in {1,2,4,8,16}).
+// The router for bf16 activations and N <= 256 in one kernel: quantization
+// inside the K-split GEMM, partials through L2 and the epilogue (cluster of S
+// CTAs per 128-token tile, S in {1,2,4,8,16}).  With amax_sync (4 zeroed
+// workspace words) the kernel also computes max|x| itself and publishes qrec
+// and x_gsa -- every CTA of the grid must then be resident at once; without
+// it, qrec and x_gsa come from the amax kernel launched before.
 // fused_cluster_capacity(S): clusters of S CTAs the device holds at once.
 int fused_cluster_capacity(int S);
-nvr_status launch_fused_router(const uint16_t* x, const float* qrec, const float* x_gsa, int64_t T, int64_t D,
+nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
