@@ -58,11 +58,13 @@ constexpr int kFWRing = kFStagesW * kFWStage;
 constexpr int kFXRing = kFXSlots * kFXBox;
 constexpr int kFARing = kFASlots * kFASlot;
 constexpr int kFByteTab = 2560;                     // scale bytes of bf16 block maxima (amax down ~20 binades)
-constexpr int kFFixQ = 256;                         // exact-pass queue entries per quantizer warp and box
+constexpr int kFFixQ = 256;                         // exact-pass queue entries per quantizer warp and box (>= 32 x groups)
 constexpr int kFTables = 1024 + 1024 + kFByteTab + 8 * kFFixQ * 2;   // s_scale, s_cc, s_byte, s_fixq
 constexpr int kFSmem = kFWRing + kFXRing + kFARing + kFTables + 512 /*barriers*/ + 1024 /*align*/;
 constexpr int kFThreads = 320;
 constexpr int kFRowsPerWarp = 16;
+constexpr int kFGroup = 8;                          // row pairs quantized together (their chains interleave)
+static_assert((kFRowsPerWarp / 2) % kFGroup == 0 && kFRowsPerWarp / 2 <= 8, "row pairs fit the 3-bit queue field");
 static_assert(kFWStage % 1024 == 0 && kFASlot % 1024 == 0 && kFXBox % 1024 == 0, "1024-byte aligned tiles");
 static_assert(8 * 8192 <= kFXRing, "store staging fits the x ring");
 
@@ -199,7 +201,7 @@ __device__ __forceinline__ void quant_rows(const uint4 (&v)[kG], const QuantScal
 //     A zero code adds +-0 to the tensor-core dot product, which changes
 //     nothing but the sign of an all-zero sum, and sigmoid(+0) = sigmoid(-0):
 //     the router's scores, ids and weights are the same.
-// s_cc[b] = (c_lo, c_hi) of scale byte b.
+// s_cc[b] = (c_lo, c_hi) of scale byte b (zero for byte 0).
 __device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
   uint32_t d;   // magnitude max(|a|, |b|) per half (the sign bit is the xor of the inputs')
   asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -233,9 +235,9 @@ __device__ __forceinline__ void quant_rows_bracket(const uint4 (&v)[kG], const u
       a[2 * j] = f2_lo(pl); a[2 * j + 1] = f2_hi(pl);
       b[2 * j] = f2_lo(ph); b[2 * j + 1] = f2_hi(ph);
     }
-    const uint32_t c = e2m1_pack8(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
-    mism[i] = c ^ e2m1_pack8(b[0], b[1], b[2], b[3], b[4], b[5], b[6], b[7]);
-    codes[i] = bytes[i] ? c : 0u;
+    // a zero scale byte has zero multipliers: its codes come out zero
+    codes[i] = e2m1_pack8(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+    mism[i] = codes[i] ^ e2m1_pack8(b[0], b[1], b[2], b[3], b[4], b[5], b[6], b[7]);
   }
 }
 
@@ -272,12 +274,13 @@ struct QuantTables {
 // Stores of one 4-row group: each row's 4 code bytes into the A slot's
 // 128-byte swizzled layout (the one TMA would produce; box hs fills chunks
 // 4hs..4hs+3 of a row) and each block's scale byte into the slot's scale atoms.
+template <int G>
 __device__ __forceinline__ void store_group(uint8_t* ac, uint8_t* asf, int hs, int row0, int sub, int l16,
-                                            const uint32_t (&codes)[4], const uint32_t (&bytes)[4]) {
+                                            const uint32_t (&codes)[G], const uint32_t (&bytes)[G]) {
   const int j = 4 * hs + (l16 >> 2);                     // 16-byte chunk of the code row
   const int c = 8 * hs + (l16 >> 1);                     // 16-element block of the stage
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < G; ++i) {
     const int r = row0 + 2 * i + sub;
     // codes: 4 bytes at chunk j ^ (r % 8), offset 4 * (l16 % 4)
     st_shared_u32(ac + r * 128 + (((j ^ (r & 7)) << 4) | ((l16 & 3) << 2)), codes[i]);
@@ -309,46 +312,56 @@ __device__ __forceinline__ void quant_box(const uint8_t* xb, uint8_t* ac, uint8_
         v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
       uint32_t codes[4] = {0u, 0u, 0u, 0u}, bytes[4] = {0u, 0u, 0u, 0u};
       if (qs.mode == 2) quant_rows<2, 4>(v, qs, tb.s_scale, codes, bytes);
-      store_group(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
+      store_group<4>(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
     }
     return;
   }
   uint32_t n_fix = 0;                                      // queued rows (warp-uniform)
 #pragma unroll
-  for (int g = 0; g < kFRowsPerWarp / 2; g += 4) {
+  for (int g = 0; g < kFRowsPerWarp / 2; g += kFGroup) {
     // rows past T only feed accumulator rows that are never stored: a group
     // that starts past T is skipped (warp-uniform)
     if (qw * kFRowsPerWarp + 2 * g >= row_end) break;
-    uint4 v[4];
+    uint4 v[kFGroup];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kFGroup; ++i)
       v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
-    uint32_t codes[4], bytes[4], mism[4];
-    quant_rows_bracket<4>(v, tb.s_byte, tb.amax_b16, tb.s_cc, codes, bytes, mism);
-    // rows whose bracketing codes differ go to the exact pass:
-    // entry = row pair (3 bits) | lane (5 bits) | scale byte << 8
+    uint32_t codes[kFGroup], bytes[kFGroup], mism[kFGroup];
+    quant_rows_bracket<kFGroup>(v, tb.s_byte, tb.amax_b16, tb.s_cc, codes, bytes, mism);
+    // lanes with rows whose bracketing codes differ go to the exact pass:
+    // entry = lane (5 bits) | first row pair of the group (3 bits) << 5 |
+    // mask of the group's rows to redo << 8
+    uint32_t redo = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const bool need = mism[i] != 0u;
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, need);
-      if (need)
-        fixq[n_fix + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>((g + i) | (lane << 3) | (bytes[i] << 8));
-      n_fix += __popc(bal);
-    }
-    store_group(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
+    for (int i = 0; i < kFGroup; ++i) redo |= (mism[i] != 0u ? 1u : 0u) << i;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, redo != 0u);
+    if (redo) fixq[n_fix + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(lane | (g << 5) | (redo << 8));
+    n_fix += __popc(bal);
+    store_group<kFGroup>(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
   }
   if (n_fix) {
-    // exact pass over the queued rows, one lane per row; the box is still in
-    // shared memory (the caller releases it afterwards)
+    // exact pass over the queued lanes, one lane per entry: every flagged row
+    // of the entry's group, its block's scale byte found again from both
+    // halves of the block; the box is still in shared memory (the caller
+    // releases it afterwards)
     __syncwarp();
     for (uint32_t e0 = 0; e0 < n_fix; e0 += 32) {
       if (e0 + lane < n_fix) {
         const uint32_t ent = fixq[e0 + lane];
-        const int ln = (ent >> 3) & 31, l = ln & 15;
-        const int r = qw * kFRowsPerWarp + 2 * static_cast<int>(ent & 7u) + (ln >> 4);
-        const uint32_t code = quant_cell_exact(ld_shared_v4(xb + r * 256 + 16 * l), ent >> 8, qs, tb.s_scale);
-        const int j = 4 * hs + (l >> 2);
-        st_shared_u32(ac + r * 128 + (((j ^ (r & 7)) << 4) | ((l & 3) << 2)), code);
+        const int ln = ent & 31, l = ln & 15;
+        const int row_pair0 = static_cast<int>((ent >> 5) & 7u);
+        for (uint32_t redo = ent >> 8; redo; redo &= redo - 1u) {
+          const int r = qw * kFRowsPerWarp + 2 * (row_pair0 + __ffs(redo) - 1) + (ln >> 4);
+          const uint4 v = ld_shared_v4(xb + r * 256 + 16 * l);
+          const uint4 w = ld_shared_v4(xb + r * 256 + 16 * (l ^ 1));
+          uint32_t m = bf16x2_max_abs(bf16x2_max_abs(bf16x2_max_abs(v.x, v.y), bf16x2_max_abs(v.z, v.w)),
+                                      bf16x2_max_abs(bf16x2_max_abs(w.x, w.y), bf16x2_max_abs(w.z, w.w)));
+          m = bf16x2_max_abs(m, __byte_perm(m, 0u, 0x1032));
+          const uint32_t byte = tb.s_byte[min(tb.amax_b16 - (m & 0x7FFFu), static_cast<uint32_t>(kFByteTab - 1))];
+          const int j = 4 * hs + (l >> 2);
+          st_shared_u32(ac + r * 128 + (((j ^ (r & 7)) << 4) | ((l & 3) << 2)),
+                        quant_cell_exact(v, byte, qs, tb.s_scale));
+        }
       }
     }
   }
@@ -622,6 +635,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       }
       uint8_t* ac = aring + slot * kFASlot;
       uint8_t* asf = ac + kFACodes;
+#pragma unroll 1
       for (int hs = 0; hs < 2; ++hs, ++xi) {
         const int xs = xi % kFXSlots;
         const uint32_t xph = (xi / kFXSlots) & 1;

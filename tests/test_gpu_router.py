@@ -340,6 +340,48 @@ def test_split_k_flag_rejects_wide_heads():
         R.router_gate_topk(big, wf, wsf, g, None, k=8, flags=K4)
 
 
+# One launch or two: when every token tile's cluster fits on the GPU at once,
+# the fused kernel computes max|x| itself (a grid barrier in the workspace);
+# otherwise the amax kernel runs first.  With S = 8 forced, 20 tiles need 20
+# clusters of 8 CTAs, more than a 152-SM GB300 holds (19): the two-launch path.
+
+@pytest.mark.parametrize("flags", [0, K8])
+def test_prefill_one_launch_and_two_launch_paths(flags):
+    case = Case(WL.WORKLOADS["prefill"].with_T(2560))
+    ids, w = case.run(flags)
+    rows = np.concatenate([np.arange(0, 2560, 23), [2559]])
+    res = case.check(ids, w, rows)
+    assert compare.topk_ok(res), res
+
+
+def test_prefill_one_launch_back_to_back_calls_on_one_workspace():
+    """Five calls queued back to back on one workspace, on inputs whose
+    magnitudes differ by up to 2^14: each call must quantize with its own
+    max|x| (the barrier's maximum slot alternates between calls and the next
+    call's slot is reset by the last CTA to arrive)."""
+    import nvfp4_router_gate_gb300 as R
+    w = WL.WORKLOADS["prefill"].with_T(1024)
+    case = Case(w)
+    ws = R.new_workspace(R.router_gate_workspace_size(w.T, w.D, w.N, w.k))
+    rows = np.arange(0, w.T, 37)
+    outs = []
+    for scale in (1.0, 64.0, 2.0 ** -8, 3.0, 1.0):
+        bits = WL.float32_to_bf16_bits((case.x32 * np.float32(scale)).astype(np.float32))
+        ids, wts = R.router_gate_topk(to_device(bits, "bf16"), case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev,
+                                      w.k, w.routed_scaling, w.raw, workspace=ws)
+        outs.append((scale, bits, ids, wts))
+    torch.cuda.synchronize()
+    for scale, bits, ids, wts in outs:
+        x32 = WL.bf16_bits_to_float32(bits)
+        gsa = Q.global_scale(x32)
+        xq, xs, _ = Q.quantize(x32[rows], gsa=gsa)
+        L, B = gemm.logits(xq, xs, gsa, case.wq, case.ws, case.wg)
+        keys = router.selection_keys(L, case.bias, w.raw)
+        res = compare.check_topk(ids.cpu().numpy()[rows], wts.cpu().numpy()[rows], L, B, keys, case.bias,
+                                 w.routed_scaling, w.raw)
+        assert compare.topk_ok(res), (scale, res)
+
+
 # ------------------------------------------------ quantization inside the GEMM
 # bf16 activations on heads of up to 256 experts are quantized inside the GEMM
 # kernel; the codes never reach memory.  A one-hot gate weight makes every
