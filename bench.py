@@ -392,27 +392,46 @@ def ctypes_array(events):
 
 
 def run_reference(args, rank):
-    """The CPU oracle, as it stands, on the host cores (rank 0 only)."""
+    """The CPU oracle, as it stands, on the host cores (rank 0 only).  Each of
+    the K timed steps routes n consecutive tokens of the T=4096 prefill batch
+    (with the whole batch's gsa), n sized from one calibration slice so that
+    the W + K steps take about a minute in all; consecutive steps' tokens go
+    through the oracle in slices of up to 64 rows (its per-call cost)."""
     if rank != 0:
         return None
-    from oracle import pipeline
+    from oracle import pipeline, quantize as Q, gemm, router
     w = WL.WORKLOADS["prefill"]
     x32 = WL.bf16_bits_to_float32(WL.make_x(w))
     W_np = WL.make_w(w)
     bias = WL.make_bias(w)
-    packed = pipeline.pack_weight(WL.bf16_bits_to_float32(W_np))
-    budget = min(15.0, max(1.0, 60.0 / max(1, args.steps + args.warmup)))   # ~1 minute in all
-    for _ in range(args.warmup):
-        oracle_tokens_per_s(w, x32, packed, bias, budget_s=0.5)
-    vals, done, el = [], 0, 0.0
-    for _ in range(args.steps):
-        v, d, e = oracle_tokens_per_s(w, x32, packed, bias, budget_s=budget)
-        vals.append(v)
-        done += d
-        el += e
+    wq, wsc, wg = pipeline.pack_weight(WL.bf16_bits_to_float32(W_np))
+    gsa = Q.global_scale(x32)
+
+    def route_tokens(total, r0):
+        """Route `total` tokens from row r0 on (wrapping), 64 rows per call."""
+        done = 0
+        while done < total:
+            n = min(64, total - done, w.T - r0)
+            rows = x32[r0:r0 + n]
+            xq, xs, _ = Q.quantize(rows, gsa=gsa)
+            L, _ = gemm.logits(xq, xs, gsa, wq, wsc, wg)
+            router.route(L, bias, w.k, w.routed_scaling, w.raw)
+            done += n
+            r0 = (r0 + n) % w.T
+        return r0
+
+    t0 = time.perf_counter()
+    route_tokens(64, 0)                                   # calibration slice
+    rate = 64.0 / (time.perf_counter() - t0)
+    n = int(min(64, max(1, round(rate * 60.0 / (args.steps + args.warmup)))))
+    r0 = route_tokens(args.warmup * n, 0)
+    t0 = time.perf_counter()
+    route_tokens(args.steps * n, r0)
+    el = time.perf_counter() - t0
+    done = args.steps * n
     value = done / el
-    sample = ("%d steps, each ~%.1f s of 64-token slices of the T=4096 prefill batch (batch gsa); "
-              "NumPy quantize + float64 GEMM + epilogue" % (args.steps, budget))
+    sample = ("%d steps of %d tokens of the T=4096 prefill batch (batch gsa), routed in slices of up to "
+              "64 rows: NumPy quantize + float64 GEMM + epilogue" % (args.steps, n))
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
