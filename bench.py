@@ -343,21 +343,26 @@ def run_gpu(args, rank, world, local_rank):
                 for _ in range(3):
                     gate(xd)
             torch.cuda.current_stream().wait_stream(s2)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                gate(xd)
-            for _ in range(50):
-                g.replay()
-            torch.cuda.synchronize()
-            reps = 1000
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / reps
-            decode["T%d_us_per_call" % Td] = us
+            # the router calls of consecutive layers, captured in one graph as
+            # a decode step would capture them; and a graph of one call (its
+            # replay overhead is paid by every call)
+            for calls, key in ((16, "T%d_us_per_call"), (1, "T%d_us_per_call_one_call_graph")):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for _ in range(calls):
+                        gate(xd)
+                for _ in range(20):
+                    g.replay()
+                torch.cuda.synchronize()
+                reps = 2000 // calls
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                decode[key % Td] = e0.elapsed_time(e1) * 1e3 / (reps * calls)
         decode["launches_T1"] = 1
+        decode["graph"] = "per call: 16 calls captured in one CUDA graph (the layers of a decode step)"
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:

@@ -236,7 +236,7 @@ decode_router_kernel(const DecodeParams p) {
     Block16 blk;
     load_block16_shared<kBF16>(xraw, static_cast<size_t>(t) * D + static_cast<size_t>(c) * kBlock, blk);
     uint32_t lo, hi;
-    const uint32_t byte = quant_block16(blk, qs, lo, hi);
+    const uint32_t byte = quant_block16_bracket(blk, qs, lo, hi);
     uint4 q;
     q.x = e2m1x4_to_s8x4(lo & 0xFFFFu);
     q.y = e2m1x4_to_s8x4(lo >> 16);

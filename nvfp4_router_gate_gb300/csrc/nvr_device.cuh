@@ -249,6 +249,51 @@ __device__ __forceinline__ uint32_t quant_block16(const Block16& blk, const Quan
   return byte;
 }
 
+// quant_block16 at a fraction of its multiply-adds, same scale byte and
+// codes.  Mode 1 only (else quant_block16 itself).
+//   byte: RN(max|x| / gsa) = max RN(|x_i| / gsa) (correctly rounded division
+//     is monotone), then the same chain as quant_block16;
+//   codes: with c = RN(RN(1/gsa) * RN(1/s)) and c_lo/hi = RN(c (1 -/+ 2^-20)),
+//     the products P_lo/hi = RN(x c_lo/hi) lie within 5 ulp of x / (gsa s),
+//     the exact q = RN(RN(x / gsa) / s) within 2, and the margin is 16 ulp:
+//     P_lo <= q <= P_hi in magnitude.  E2M1 rounding is monotone, so where
+//     the two code words agree they are the exact codes; otherwise (some q
+//     within ~2^-20 of a rounding boundary, e.g. an exact tie) the block is
+//     quantized again by quant_block16.  Elements too small for the error
+//     bounds (subnormal products) give zero codes on both sides.
+__device__ __forceinline__ uint32_t quant_block16_bracket(const Block16& blk, const QuantScale& qs,
+                                                          uint32_t& codes_lo, uint32_t& codes_hi,
+                                                          const float* rcp_tab = nullptr) {
+  if (qs.mode != 1) return quant_block16(blk, qs, codes_lo, codes_hi, rcp_tab);
+  const float (&x)[16] = blk.v;
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(x[i]));
+  const float r6 = 0.16666667163372039794921875f;       // RN(1/6)
+  const uint32_t byte = e4m3_byte(div_rn_short(div_rn(m, qs.gsa, qs.rgsa), 6.0f, r6));
+  if (byte == 0) { codes_lo = codes_hi = 0; return 0; }
+  const float c = __fmul_rn(qs.rgsa, rcp_tab ? rcp_tab[byte] : __frcp_rn(e4m3_value(byte)));
+  const float c_lo = __fmul_rn(c, 0.99999904632568359375f);    // 1 - 2^-20
+  const float c_hi = __fmul_rn(c, 1.00000095367431640625f);    // 1 + 2^-20
+  const uint64_t lo2 = f2_pack(c_lo, c_lo), hi2 = f2_pack(c_hi, c_hi);
+  float a[16], b[16];
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const uint64_t xp = f2_pack(x[i], x[i + 1]);
+    const uint64_t pl = f2_mul(xp, lo2), ph = f2_mul(xp, hi2);
+    a[i] = f2_lo(pl); a[i + 1] = f2_hi(pl);
+    b[i] = f2_lo(ph); b[i + 1] = f2_hi(ph);
+  }
+  const uint32_t l0 = e2m1_pack8(a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7]);
+  const uint32_t l1 = e2m1_pack8(a[8], a[9], a[10], a[11], a[12], a[13], a[14], a[15]);
+  const uint32_t h0 = e2m1_pack8(b[0], b[1], b[2], b[3], b[4], b[5], b[6], b[7]);
+  const uint32_t h1 = e2m1_pack8(b[8], b[9], b[10], b[11], b[12], b[13], b[14], b[15]);
+  if ((l0 ^ h0) | (l1 ^ h1)) return quant_block16(blk, qs, codes_lo, codes_hi, rcp_tab);
+  codes_lo = l0 | blk.neg_lo;
+  codes_hi = l1 | blk.neg_hi;
+  return byte;
+}
+
 // Widen 8 bf16 (one uint4) to fp32 (exact).
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float* out) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};

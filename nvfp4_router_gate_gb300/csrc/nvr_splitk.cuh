@@ -174,8 +174,10 @@ struct TokenRouter {
   int N, k, raw;
   float routed_scaling;
 
-  // The bias is a caller input that no kernel of the call writes: it may be
-  // read before the grid-dependency wait.
+  // The bias is a caller input that no kernel of the call writes; the call's
+  // first kernel has already waited for the caller's previous kernel (which
+  // may have written it), so a later kernel of the call may read it before
+  // its own grid-dependency wait.
   __device__ __forceinline__ void init(const float* bias, int N_, int k_, int raw_, float rs, int lane) {
     N = N_; k = k_; raw = raw_; routed_scaling = rs;
 #pragma unroll

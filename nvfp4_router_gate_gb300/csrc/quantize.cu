@@ -236,9 +236,9 @@ quantize_kernel(const void* __restrict__ x, uint32_t rows, uint32_t rows_pad, ui
     Block16 blk;
     const size_t e0 = static_cast<size_t>(r) * D + static_cast<size_t>(c) * kBlock;
     load_block16<kBF16>(x, e0, blk);
-    b0 = quant_block16(blk, qs, q.x, q.y, s_rcp);
+    b0 = quant_block16_bracket(blk, qs, q.x, q.y, s_rcp);
     load_block16<kBF16>(x, e0 + kBlock, blk);
-    b1 = quant_block16(blk, qs, q.z, q.w, s_rcp);
+    b1 = quant_block16_bracket(blk, qs, q.z, q.w, s_rcp);
     *reinterpret_cast<uint4*>(codes + static_cast<size_t>(r) * (D / 2) + static_cast<size_t>(c) * 8) = q;
   }
   if (kTiled) {
