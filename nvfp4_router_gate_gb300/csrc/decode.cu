@@ -45,6 +45,14 @@ struct DecodeParams {
   float* ws_keys;
   float* ws_scores;
   uint32_t* ticket;
+  // shared quantization (several tokens, the whole grid resident): each CTA
+  // quantizes 1/grid of x into these workspace buffers, the grid meets at a
+  // barrier (bar: arrivals, generation) and every CTA loads the rest; null:
+  // every CTA quantizes all of x itself
+  int8_t* ws_xv;
+  float* ws_xs;
+  uint32_t* bar;
+  uint32_t* status;
 };
 
 // Four E2M1 codes (16 bits, element i in nibble i) -> four signed bytes
@@ -171,6 +179,28 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
                "l"(reinterpret_cast<uint64_t>(gmem_src)) : "memory");
 }
 
+// Grid barrier for one thread per CTA over two workspace words (bar[0]
+// arrivals, bar[1] generation): arrive (release), the last CTA to arrive
+// resets the arrivals and bumps the generation (release), the others wait for
+// it (acquire).  The caller fences its CTA's writes before.  All CTAs of the
+// grid must be resident; false when the wait times out.
+__device__ bool grid_barrier(uint32_t* bar, uint32_t n_ctas, uint64_t deadline) {
+  uint32_t gen, t;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(bar + 1) : "memory");
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(bar) : "memory");
+  if (t == n_ctas - 1) {
+    bar[0] = 0u;
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(bar + 1), "r"(gen + 1u) : "memory");
+    return true;
+  }
+  for (;;) {
+    uint32_t g;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(bar + 1) : "memory");
+    if (g != gen) return true;
+    if (globaltimer_ns() > deadline) return false;
+  }
+}
+
 template <bool kBF16>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_router_kernel(const DecodeParams p) {
@@ -230,8 +260,18 @@ decode_router_kernel(const DecodeParams p) {
   const QuantScale qs = make_quant_scale(__uint_as_float(mb));
 
   // 2. quantize x (shared -> shared) with the block quantizer shared with the
-  //    quantize kernel: identical codes and scales
-  for (int b = tid; b < T * KB; b += kDecodeThreads) {
+  //    quantize kernel: identical codes and scales.  Block b = t * KB + c
+  //    keeps its 16 signed bytes at xv + 16 b and its scale at xs[b].  With
+  //    shared quantization this CTA does blocks [b_lo, b_hi) only.
+  const int nblk = T * KB;
+  const bool shared_q = p.ws_xv != nullptr;
+  int b_lo = 0, b_hi = nblk;
+  if (shared_q) {
+    const int per = (nblk + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    b_lo = min(nblk, static_cast<int>(blockIdx.x) * per);
+    b_hi = min(nblk, b_lo + per);
+  }
+  for (int b = b_lo + tid; b < b_hi; b += kDecodeThreads) {
     const int t = b / KB, c = b - t * KB;
     Block16 blk;
     load_block16_shared<kBF16>(xraw, static_cast<size_t>(t) * D + static_cast<size_t>(c) * kBlock, blk);
@@ -242,8 +282,30 @@ decode_router_kernel(const DecodeParams p) {
     q.y = e2m1x4_to_s8x4(lo >> 16);
     q.z = e2m1x4_to_s8x4(hi & 0xFFFFu);
     q.w = e2m1x4_to_s8x4(hi >> 16);
-    *reinterpret_cast<uint4*>(xv + static_cast<size_t>(t) * D + c * kBlock) = q;
-    xs[t * KB + c] = e4m3_value(byte);
+    const float sc = e4m3_value(byte);
+    *reinterpret_cast<uint4*>(xv + 16 * static_cast<size_t>(b)) = q;
+    xs[b] = sc;
+    if (shared_q) {
+      *reinterpret_cast<uint4*>(p.ws_xv + 16 * static_cast<size_t>(b)) = q;
+      p.ws_xs[b] = sc;
+    }
+  }
+  if (shared_q) {
+    // publish this CTA's blocks, wait for every CTA's (bounded), load them
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = grid_barrier(p.bar, gridDim.x, globaltimer_ns() + 1000000000ull) ? 1 : 0;
+    __syncthreads();
+    if (!s_last) {
+      if (tid == 0) report_timeout(p.status);
+      return;
+    }
+    for (int b = tid; b < nblk; b += kDecodeThreads) {
+      if (b >= b_lo && b < b_hi) continue;
+      cp_async16(xv + 16 * static_cast<size_t>(b), p.ws_xv + 16 * static_cast<size_t>(b));
+      xs[b] = __ldcg(p.ws_xs + b);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   }
   __syncthreads();
 
@@ -264,27 +326,58 @@ decode_router_kernel(const DecodeParams p) {
   // 3. logits of this CTA's experts: integer dot products of each 16-element
   //    block (exact), scaled by the two block scales (exact product), fp32 sum.
   //    The weight blocks are decoded once; the token loop stays rolled.
-#pragma unroll 1
-  for (int t = 0; t < T; ++t) {
+  // Four tokens at a time (one for a single token): their block loops and
+  // warp reductions interleave; a token's own sums keep the block order, so
+  // results do not depend on T.
+  if (T == 1) {
     float acc = 0.0f;
 #pragma unroll
     for (int i = 0; i < kMaxBlocksPerThread; ++i) {
       const int c = j + i * gs;
       if (i >= nb) break;
       if (e < N && c < KB) {
-        const uint4 xq = *reinterpret_cast<const uint4*>(xv + static_cast<size_t>(t) * D + c * kBlock);
+        const uint4 xq = *reinterpret_cast<const uint4*>(xv + c * kBlock);
         int sdot = __dp4a(static_cast<int>(xq.x), static_cast<int>(wv[i][0]), 0);
         sdot = __dp4a(static_cast<int>(xq.y), static_cast<int>(wv[i][1]), sdot);
         sdot = __dp4a(static_cast<int>(xq.z), static_cast<int>(wv[i][2]), sdot);
         sdot = __dp4a(static_cast<int>(xq.w), static_cast<int>(wv[i][3]), sdot);
-        // |sdot| <= 16 * 144 and both scales have 4 significant bits: the
-        // product is exact, only the accumulation rounds
-        acc = __fmaf_rn(static_cast<float>(sdot), __fmul_rn(xs[t * KB + c], swv[i]), acc);
+        acc = __fmaf_rn(static_cast<float>(sdot), __fmul_rn(xs[c], swv[i]), acc);
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-    if (lane == 0) red[warp * kMaxT + t] = acc;
+    if (lane == 0) red[warp * kMaxT] = acc;
+  }
+#pragma unroll 1
+  for (int t0 = 0; t0 < (T > 1 ? T : 0); t0 += 4) {
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < kMaxBlocksPerThread; ++i) {
+      const int c = j + i * gs;
+      if (i >= nb) break;
+      if (e < N && c < KB) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int t = min(t0 + u, T - 1);               // a repeated token past T is discarded
+          const uint4 xq = *reinterpret_cast<const uint4*>(xv + static_cast<size_t>(t) * D + c * kBlock);
+          int sdot = __dp4a(static_cast<int>(xq.x), static_cast<int>(wv[i][0]), 0);
+          sdot = __dp4a(static_cast<int>(xq.y), static_cast<int>(wv[i][1]), sdot);
+          sdot = __dp4a(static_cast<int>(xq.z), static_cast<int>(wv[i][2]), sdot);
+          sdot = __dp4a(static_cast<int>(xq.w), static_cast<int>(wv[i][3]), sdot);
+          // |sdot| <= 16 * 144 and both scales have 4 significant bits: the
+          // product is exact, only the accumulation rounds
+          acc[u] = __fmaf_rn(static_cast<float>(sdot), __fmul_rn(xs[t * KB + c], swv[i]), acc[u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[u] += __shfl_xor_sync(0xFFFFFFFFu, acc[u], o);
+    if (lane == 0)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (t0 + u < T) red[warp * kMaxT + t0 + u] = acc[u];
   }
   __syncthreads();
 
@@ -471,8 +564,10 @@ cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const 
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,
                           int k, float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                           float* logits, float* ws_keys, float* ws_scores, uint32_t* ticket,
+                          int8_t* ws_xv, float* ws_xs, uint32_t* bar, uint32_t* status,
                           const DecodePlan& plan, cudaStream_t s) {
   DecodeParams p;
+  p.ws_xv = ws_xv; p.ws_xs = ws_xs; p.bar = bar; p.status = status;
   p.x = x; p.T = static_cast<int>(T); p.D = static_cast<int>(D);
   p.W_codes = W_codes; p.W_sf = W_sf; p.w_gsa = w_gsa; p.N = static_cast<int>(N);
   p.bias = raw ? nullptr : bias; p.k = k; p.routed_scaling = routed_scaling;

@@ -26,6 +26,7 @@ constexpr int kWsAmaxTicket = 4;
 constexpr int kWsDecodeTicket = 8;
 constexpr int kWsAmaxChunk = 12;           // amax: next chunk to claim
 constexpr int kWsFusedAmax = 16;           // fused router's in-kernel amax: 4 words (2 maxima, arrivals, generation)
+constexpr int kWsDecodeBar = 32;           // decode kernel's grid barrier: 2 words (arrivals, generation)
 constexpr uint32_t kStatusTimeout = 6;     // == NVR_ERR_TIMEOUT
 
 // ------------------------------------------------------------------ small PTX
@@ -388,9 +389,13 @@ __device__ __forceinline__ bool topk_better(float ka, int ia, float kb, int ib) 
 // approximation (__fdividef, within 2 ulp, 0 for a denominator above 2^126).
 // The result is within a few ulp of the correctly rounded sigmoid for every
 // float32 logit, exact at l = 0 (0.5) and equal to 1 once exp(-l) < 2^-25.
+// Below -87 the result is 0 (the true sigmoid is below 2^-125; an infinite
+// 2^t_hi would otherwise turn the correction into inf - inf = NaN).
 // (W. J. Cody, W. Waite, Software Manual for the Elementary Functions, 1980:
 // argument reduction with a split constant.)
 __device__ __forceinline__ float sigmoid_f32(float l) {
+  const bool tiny = l < -87.0f;
+  l = tiny ? -87.0f : l;
   const float kLog2eHi = 1.44269502162933349609375f;      // RN(log2 e)
   const float kLog2eLo = 1.925963033500011079e-8f;        // log2 e - kLog2eHi
   const float t = __fmul_rn(-l, kLog2eHi);
@@ -398,7 +403,7 @@ __device__ __forceinline__ float sigmoid_f32(float l) {
   float e;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
   e = __fmaf_rn(__fmul_rn(e, 0.693147180559945309f), t_lo, e);
-  return __fdividef(1.0f, __fadd_rn(1.0f, e));
+  return tiny ? 0.0f : __fdividef(1.0f, __fadd_rn(1.0f, e));
 }
 
 // ------------------------------------------------- sorting-network helpers

@@ -40,6 +40,9 @@ struct GemmPlan {
 GemmPlan plan_gemm(int64_t T, int64_t N, int num_sms);
 
 // Decode (single-launch) path limits and plan.
+// Decode calls of at least this many tokens share the quantization of x
+// across the grid (each CTA quantizes a slice; a grid barrier in between).
+constexpr int kDecodeSharedQuantMinT = 3;
 struct DecodePlan {
   bool ok = false;
   int tmax = 0;        // template bucket >= T
@@ -114,6 +117,7 @@ cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const 
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,
                           int k, float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                           float* logits, float* ws_keys, float* ws_scores, uint32_t* ticket,
+                          int8_t* ws_xv, float* ws_xs, uint32_t* bar, uint32_t* status,
                           const DecodePlan& plan, cudaStream_t s);
 
 }  // namespace nvr

@@ -382,6 +382,65 @@ def test_prefill_one_launch_back_to_back_calls_on_one_workspace():
         assert compare.topk_ok(res), (scale, res)
 
 
+@pytest.mark.parametrize("flags", [DEC, TC])
+def test_huge_logits_saturate_without_nan(flags):
+    """x scaled by 2^10: logits reach +-3e4, every sigmoid saturates to 0 or 1
+    (exp(-l) overflows for very negative logits; the scores must stay 0, not
+    NaN) and the bias alone orders the saturated experts."""
+    w = WL.WORKLOADS["decode"].with_T(8)
+    case = Case(w)
+    bits = WL.float32_to_bf16_bits((case.x32 * np.float32(1024.0)).astype(np.float32))
+    import nvfp4_router_gate_gb300 as R
+    ids, wts = R.router_gate_topk(to_device(bits, "bf16"), case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev,
+                                  w.k, w.routed_scaling, w.raw, flags=flags)
+    torch.cuda.synchronize()
+    ids, wts = ids.cpu().numpy(), wts.cpu().numpy()
+    assert np.all(np.isfinite(wts))
+    x32 = WL.bf16_bits_to_float32(bits)
+    gsa = Q.global_scale(x32)
+    xq, xs, _ = Q.quantize(x32, gsa=gsa)
+    L, B = gemm.logits(xq, xs, gsa, case.wq, case.ws, case.wg)
+    keys = router.selection_keys(L, case.bias, w.raw)
+    res = compare.check_topk(ids, wts, L, B, keys, case.bias, w.routed_scaling, w.raw)
+    assert compare.topk_ok(res), res
+
+
+# Decode calls of 3 or more tokens share the quantization of x across the
+# grid (a barrier in the workspace between quantizing a slice and loading
+# the rest); calls back to back on one workspace reuse the barrier.
+
+@pytest.mark.parametrize("T", [3, 5, 7])
+def test_decode_shared_quantization_ragged_token_counts(T):
+    case = Case(WL.WORKLOADS["decode"].with_T(T))
+    ids, w = case.run(DEC)
+    res = case.check(ids, w, np.arange(T))
+    assert compare.topk_ok(res), res
+
+
+def test_decode_shared_quantization_back_to_back_on_one_workspace():
+    import nvfp4_router_gate_gb300 as R
+    w = WL.WORKLOADS["decode"].with_T(8)
+    case = Case(w)
+    ws = R.new_workspace(R.router_gate_workspace_size(w.T, w.D, w.N, w.k))
+    outs = []
+    for scale in (1.0, 2.0 ** 10, 2.0 ** -12, 3.0, 1.0):
+        bits = WL.float32_to_bf16_bits((case.x32 * np.float32(scale)).astype(np.float32))
+        ids, wts = R.router_gate_topk(to_device(bits, "bf16"), case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev,
+                                      w.k, w.routed_scaling, w.raw, workspace=ws, flags=DEC)
+        outs.append((scale, bits, ids, wts))
+    torch.cuda.synchronize()
+    rows = np.arange(w.T)
+    for scale, bits, ids, wts in outs:
+        x32 = WL.bf16_bits_to_float32(bits)
+        gsa = Q.global_scale(x32)
+        xq, xs, _ = Q.quantize(x32, gsa=gsa)
+        L, B = gemm.logits(xq, xs, gsa, case.wq, case.ws, case.wg)
+        keys = router.selection_keys(L, case.bias, w.raw)
+        res = compare.check_topk(ids.cpu().numpy(), wts.cpu().numpy(), L, B, keys, case.bias,
+                                 w.routed_scaling, w.raw)
+        assert compare.topk_ok(res), (scale, res)
+
+
 # ------------------------------------------------ quantization inside the GEMM
 # bf16 activations on heads of up to 256 experts are quantized inside the GEMM
 # kernel; the codes never reach memory.  A one-hot gate weight makes every
