@@ -208,16 +208,9 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     float* scores = keys + T * N;
     ProfileScope prof(s);
     prof.before();
-    // several tokens and the whole grid resident (one CTA per SM always
-    // fits): the CTAs share the quantization of x through the workspace
-    const bool shared_q = T >= kDecodeSharedQuantMinT && dp.grid <= sms;
     cudaError_t e = launch_decode(x, bf16, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
                                   out_ids, out_w, logits, keys, scores,
-                                  reinterpret_cast<uint32_t*>(w + kWsDecodeTicket),
-                                  shared_q ? reinterpret_cast<int8_t*>(w + L.x_codes) : nullptr,
-                                  shared_q ? reinterpret_cast<float*>(w + L.x_sf) : nullptr,
-                                  shared_q ? reinterpret_cast<uint32_t*>(w + kWsDecodeBar) : nullptr,
-                                  reinterpret_cast<uint32_t*>(w + kWsStatus), dp, s);
+                                  reinterpret_cast<uint32_t*>(w + kWsDecodeTicket), dp, s);
     prof.after();
     return cuda_status(e);
   }

@@ -8,11 +8,14 @@
 // For T <= 16 tokens the gate GEMM is a skinny GEMV that streams the 1 MB
 // weight once; tensor cores buy nothing at this size, latency is everything.
 // Every CTA:
-//   1. reduces max|x| over the whole (small) x itself -- the same exact
-//      maximum the grid-wide amax kernel finds, so gsa has identical bits;
+//   1. reduces max|x| over the whole (small) x -- the same exact maximum the
+//      grid-wide amax kernel finds, so gsa has identical bits;
 //   2. quantizes all of x into shared memory with the block quantizer shared
 //      with the quantize kernel (identical codes and scales), keeping each
 //      block as 16 signed bytes 2*e2m1(code) and its fp32 scale;
+//   (for several tokens the CTAs form clusters of 4 that split steps 1-2:
+//   each stages, reduces and quantizes a quarter of x and stores its blocks
+//   into the other CTAs' shared memory; one token: every CTA does all of it)
 //   3. computes the logits of its `epc` experts: integer dot products of each
 //      16-element block (dp4a on 2*e2m1 values, exact) scaled by the two block
 //      scales (exact product) and accumulated in fp32, then x gsa_x * gsa_w;
@@ -21,10 +24,15 @@
 // keys (key descending, lower id first), renormalises the k selected scores
 // and writes ids and weights, then resets the ticket.
 #include "nvr_internal.h"
+#include "nvr_tcgen05.cuh"
 
 namespace nvr {
 
 constexpr int kDecodeThreads = 256;
+// Several tokens: clusters of 4 CTAs share the staging and quantization of x.
+// (Measured on GB300: clusters of 8 were launched in waves, several µs apart;
+// for a single token the cluster barriers cost more than the sharing saves.)
+constexpr int kMaxDecodeCluster = 4;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kDecodeMaxSmem = 200 * 1024;
 
@@ -45,14 +53,10 @@ struct DecodeParams {
   float* ws_keys;
   float* ws_scores;
   uint32_t* ticket;
-  // shared quantization (several tokens, the whole grid resident): each CTA
-  // quantizes 1/grid of x into these workspace buffers, the grid meets at a
-  // barrier (bar: arrivals, generation) and every CTA loads the rest; null:
-  // every CTA quantizes all of x itself
-  int8_t* ws_xv;
-  float* ws_xs;
-  uint32_t* bar;
-  uint32_t* status;
+  // CTAs per thread-block cluster (1: every CTA stages, reduces and
+  // quantizes all of x itself; C > 1: the C CTAs of a cluster split these
+  // and exchange the results through distributed shared memory)
+  int cluster;
 };
 
 // Four E2M1 codes (16 bits, element i in nibble i) -> four signed bytes
@@ -179,26 +183,19 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
                "l"(reinterpret_cast<uint64_t>(gmem_src)) : "memory");
 }
 
-// Grid barrier for one thread per CTA over two workspace words (bar[0]
-// arrivals, bar[1] generation): arrive (release), the last CTA to arrive
-// resets the arrivals and bumps the generation (release), the others wait for
-// it (acquire).  The caller fences its CTA's writes before.  All CTAs of the
-// grid must be resident; false when the wait times out.
-__device__ bool grid_barrier(uint32_t* bar, uint32_t n_ctas, uint64_t deadline) {
-  uint32_t gen, t;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(gen) : "l"(bar + 1) : "memory");
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(bar) : "memory");
-  if (t == n_ctas - 1) {
-    bar[0] = 0u;
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(bar + 1), "r"(gen + 1u) : "memory");
-    return true;
-  }
-  for (;;) {
-    uint32_t g;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(bar + 1) : "memory");
-    if (g != gen) return true;
-    if (globaltimer_ns() > deadline) return false;
-  }
+// Distributed shared memory: the address of a local shared-memory location in
+// CTA `rank` of the cluster, and stores to it.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, const uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
 
 template <bool kBF16>
@@ -212,6 +209,7 @@ decode_router_kernel(const DecodeParams p) {
   float* xs = reinterpret_cast<float*>(sm + L.xs);
   float* red = reinterpret_cast<float*>(sm + L.red);          // [warps][kMaxT]
   __shared__ uint32_t s_red[kDecodeWarps];
+  __shared__ uint32_t s_cmax[kMaxDecodeCluster];
   __shared__ int s_last;
   __shared__ int s_sel[kMaxT * 16];
 
@@ -241,15 +239,36 @@ decode_router_kernel(const DecodeParams p) {
       wsb[i] = 0;
     }
   }
-  const int64_t nvec = static_cast<int64_t>(T) * D * (kBF16 ? 2 : 4) / 16;
-  for (int64_t v = tid; v < nvec; v += kDecodeThreads)
-    cp_async16(xraw + 16 * v, static_cast<const uint8_t*>(p.x) + 16 * v);
+  // The blocks of x (block b = t * KB + c: 16 elements of token t) this CTA
+  // stages, reduces and quantizes: all of them, or in a cluster of C CTAs
+  // the slice [b_lo, b_hi) of its rank.
+  const int C = p.cluster;
+  uint32_t crank = 0;
+  if (C > 1) {
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+    // distributed shared memory may be accessed once every CTA of the
+    // cluster runs: arrive now, wait before the first remote store
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  }
+  const int nblk = T * KB;
+  int b_lo = 0, b_hi = nblk;
+  if (C > 1) {
+    const int per = (nblk + C - 1) / C;
+    b_lo = min(nblk, static_cast<int>(crank) * per);
+    b_hi = min(nblk, b_lo + per);
+  }
+  constexpr int kVecPerBlock = kBlock * (kBF16 ? 2 : 4) / 16;     // 16-byte vectors per block
+  for (int v = b_lo * kVecPerBlock + tid; v < b_hi * kVecPerBlock; v += kDecodeThreads)
+    cp_async16(xraw + 16 * static_cast<size_t>(v), static_cast<const uint8_t*>(p.x) + 16 * static_cast<size_t>(v));
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncthreads();
-  // 1. max |x| over the whole batch (from shared memory)
+  // 1. max |x| over the staged blocks; in a cluster, every CTA's maximum goes
+  //    to every CTA (thread i writes CTA i's slot), so each one finds the
+  //    maximum of the whole batch -- the same exact value in every CTA
   const uint4* x4 = reinterpret_cast<const uint4*>(xraw);
   uint32_t m = 0;
-  for (int64_t v = tid; v < nvec; v += kDecodeThreads) m = max(m, absmax_bits16B<kBF16>(x4[v]));
+  for (int v = b_lo * kVecPerBlock + tid; v < b_hi * kVecPerBlock; v += kDecodeThreads)
+    m = max(m, absmax_bits16B<kBF16>(x4[v]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if (lane == 0) s_red[warp] = m;
@@ -257,20 +276,19 @@ decode_router_kernel(const DecodeParams p) {
   uint32_t mb = 0;
 #pragma unroll
   for (int w = 0; w < kDecodeWarps; ++w) mb = max(mb, s_red[w]);
+  if (C > 1) {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (tid < C) st_cluster_u32(cluster_addr(s_cmax + crank, tid), mb);
+    cluster_sync_all();
+    mb = 0;
+    for (int r = 0; r < C; ++r) mb = max(mb, s_cmax[r]);
+  }
   const QuantScale qs = make_quant_scale(__uint_as_float(mb));
 
-  // 2. quantize x (shared -> shared) with the block quantizer shared with the
-  //    quantize kernel: identical codes and scales.  Block b = t * KB + c
-  //    keeps its 16 signed bytes at xv + 16 b and its scale at xs[b].  With
-  //    shared quantization this CTA does blocks [b_lo, b_hi) only.
-  const int nblk = T * KB;
-  const bool shared_q = p.ws_xv != nullptr;
-  int b_lo = 0, b_hi = nblk;
-  if (shared_q) {
-    const int per = (nblk + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-    b_lo = min(nblk, static_cast<int>(blockIdx.x) * per);
-    b_hi = min(nblk, b_lo + per);
-  }
+  // 2. quantize the blocks (shared -> shared) with the block quantizer shared
+  //    with the quantize kernel: identical codes and scales.  Block b keeps
+  //    its 16 signed bytes at xv + 16 b and its scale at xs[b]; in a cluster
+  //    each CTA also stores its blocks into every other CTA's copy.
   for (int b = b_lo + tid; b < b_hi; b += kDecodeThreads) {
     const int t = b / KB, c = b - t * KB;
     Block16 blk;
@@ -285,29 +303,15 @@ decode_router_kernel(const DecodeParams p) {
     const float sc = e4m3_value(byte);
     *reinterpret_cast<uint4*>(xv + 16 * static_cast<size_t>(b)) = q;
     xs[b] = sc;
-    if (shared_q) {
-      *reinterpret_cast<uint4*>(p.ws_xv + 16 * static_cast<size_t>(b)) = q;
-      p.ws_xs[b] = sc;
+    for (int r = 1; r < C; ++r) {
+      const uint32_t peer = (crank + r) % C;                     // a different peer per step
+      st_cluster_v4(cluster_addr(xv + 16 * static_cast<size_t>(b), peer), q);
+      st_cluster_u32(cluster_addr(xs + b, peer), __float_as_uint(sc));
     }
   }
-  if (shared_q) {
-    // publish this CTA's blocks, wait for every CTA's (bounded), load them
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = grid_barrier(p.bar, gridDim.x, globaltimer_ns() + 1000000000ull) ? 1 : 0;
-    __syncthreads();
-    if (!s_last) {
-      if (tid == 0) report_timeout(p.status);
-      return;
-    }
-    for (int b = tid; b < nblk; b += kDecodeThreads) {
-      if (b >= b_lo && b < b_hi) continue;
-      cp_async16(xv + 16 * static_cast<size_t>(b), p.ws_xv + 16 * static_cast<size_t>(b));
-      xs[b] = __ldcg(p.ws_xs + b);
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-  }
-  __syncthreads();
+  // every block in every CTA of the cluster (and no remote access after)
+  if (C > 1) cluster_sync_all();
+  else __syncthreads();
 
   // decode this thread's weight blocks: their loads were issued first and have
   // long landed; decoding them only now keeps them off the path to gsa
@@ -539,6 +543,12 @@ DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms, bool bf16) 
   if (d.smem > kDecodeMaxSmem) return d;
   d.epc = epc;
   d.grid = static_cast<int>((N + epc - 1) / epc);
+  // several tokens: clusters of CTAs share the staging and quantization of x
+  // (the grid is padded to whole clusters; the extra CTAs have no experts)
+  if (T >= 2 && d.grid >= kMaxDecodeCluster) {
+    d.cluster = kMaxDecodeCluster;
+    d.grid = (d.grid + kMaxDecodeCluster - 1) / kMaxDecodeCluster * kMaxDecodeCluster;
+  }
   d.ok = true;
   return d;
 }
@@ -556,18 +566,32 @@ static cudaError_t launch_t(const DecodeParams& p, const DecodePlan& plan, cudaS
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  decode_router_kernel<kBF16><<<plan.grid, kDecodeThreads, plan.smem, s>>>(p);
-  return cudaGetLastError();
+  if (plan.cluster <= 1) {
+    decode_router_kernel<kBF16><<<plan.grid, kDecodeThreads, plan.smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = plan.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_router_kernel<kBF16>, p);
 }
 
 cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const uint8_t* W_codes,
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,
                           int k, float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                           float* logits, float* ws_keys, float* ws_scores, uint32_t* ticket,
-                          int8_t* ws_xv, float* ws_xs, uint32_t* bar, uint32_t* status,
                           const DecodePlan& plan, cudaStream_t s) {
   DecodeParams p;
-  p.ws_xv = ws_xv; p.ws_xs = ws_xs; p.bar = bar; p.status = status;
+  p.cluster = plan.cluster;
   p.x = x; p.T = static_cast<int>(T); p.D = static_cast<int>(D);
   p.W_codes = W_codes; p.W_sf = W_sf; p.w_gsa = w_gsa; p.N = static_cast<int>(N);
   p.bias = raw ? nullptr : bias; p.k = k; p.routed_scaling = routed_scaling;

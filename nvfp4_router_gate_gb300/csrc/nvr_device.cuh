@@ -26,7 +26,6 @@ constexpr int kWsAmaxTicket = 4;
 constexpr int kWsDecodeTicket = 8;
 constexpr int kWsAmaxChunk = 12;           // amax: next chunk to claim
 constexpr int kWsFusedAmax = 16;           // fused router's in-kernel amax: 4 words (2 maxima, arrivals, generation)
-constexpr int kWsDecodeBar = 32;           // decode kernel's grid barrier: 2 words (arrivals, generation)
 constexpr uint32_t kStatusTimeout = 6;     // == NVR_ERR_TIMEOUT
 
 // ------------------------------------------------------------------ small PTX

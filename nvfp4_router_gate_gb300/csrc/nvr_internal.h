@@ -40,14 +40,12 @@ struct GemmPlan {
 GemmPlan plan_gemm(int64_t T, int64_t N, int num_sms);
 
 // Decode (single-launch) path limits and plan.
-// Decode calls of at least this many tokens share the quantization of x
-// across the grid (each CTA quantizes a slice; a grid barrier in between).
-constexpr int kDecodeSharedQuantMinT = 3;
 struct DecodePlan {
   bool ok = false;
   int tmax = 0;        // template bucket >= T
   int epc = 0;         // experts per CTA
   int grid = 0;
+  int cluster = 1;     // CTAs per cluster sharing the staging and quantization of x
   size_t smem = 0;
 };
 DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms, bool bf16);
@@ -117,7 +115,6 @@ cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const 
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,
                           int k, float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                           float* logits, float* ws_keys, float* ws_scores, uint32_t* ticket,
-                          int8_t* ws_xv, float* ws_xs, uint32_t* bar, uint32_t* status,
                           const DecodePlan& plan, cudaStream_t s);
 
 }  // namespace nvr
