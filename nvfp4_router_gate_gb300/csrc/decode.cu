@@ -34,7 +34,7 @@ constexpr int kDecodeThreads = 256;
 // for a single token the cluster barriers cost more than the sharing saves.)
 constexpr int kMaxDecodeCluster = 4;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
-constexpr int kDecodeMaxSmem = 200 * 1024;
+constexpr int kDecodeMaxSmem = 224 * 1024;
 
 struct DecodeParams {
   const void* x;
@@ -162,11 +162,14 @@ constexpr int kMaxT = 16;                 // tokens of one decode call
 struct DecodeSmem {
   size_t raw, xv, xs, red, total;
 };
-__host__ __device__ inline DecodeSmem decode_smem_layout(int T, int D, int N, int elt) {
+__host__ __device__ inline DecodeSmem decode_smem_layout(int T, int D, int N, int elt, int C) {
   const int KB = D / kBlock;
   DecodeSmem L;
   L.raw = 0;
-  const size_t raw_bytes = static_cast<size_t>(T) * D * elt;
+  // the raw activations of this CTA's blocks only: all of x, or a cluster
+  // rank's slice
+  const size_t slice = (static_cast<size_t>(T) * KB + C - 1) / C;
+  const size_t raw_bytes = slice * kBlock * elt;
   const size_t kv_bytes = static_cast<size_t>(T) * N * 8;
   L.xv = align_up(raw_bytes > kv_bytes ? raw_bytes : kv_bytes, 16);
   L.xs = align_up(L.xv + static_cast<size_t>(T) * D, 16);
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 decode_router_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int T = p.T, D = p.D, N = p.N, KB = D / kBlock;
-  const DecodeSmem L = decode_smem_layout(T, D, N, kBF16 ? 2 : 4);
+  const DecodeSmem L = decode_smem_layout(T, D, N, kBF16 ? 2 : 4, p.cluster);
   uint8_t* xraw = sm + L.raw;
   int8_t* xv = reinterpret_cast<int8_t*>(sm + L.xv);
   float* xs = reinterpret_cast<float*>(sm + L.xs);
@@ -259,7 +262,8 @@ decode_router_kernel(const DecodeParams p) {
   }
   constexpr int kVecPerBlock = kBlock * (kBF16 ? 2 : 4) / 16;     // 16-byte vectors per block
   for (int v = b_lo * kVecPerBlock + tid; v < b_hi * kVecPerBlock; v += kDecodeThreads)
-    cp_async16(xraw + 16 * static_cast<size_t>(v), static_cast<const uint8_t*>(p.x) + 16 * static_cast<size_t>(v));
+    cp_async16(xraw + 16 * static_cast<size_t>(v - b_lo * kVecPerBlock),
+               static_cast<const uint8_t*>(p.x) + 16 * static_cast<size_t>(v));
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncthreads();
   // 1. max |x| over the staged blocks; in a cluster, every CTA's maximum goes
@@ -267,8 +271,7 @@ decode_router_kernel(const DecodeParams p) {
   //    maximum of the whole batch -- the same exact value in every CTA
   const uint4* x4 = reinterpret_cast<const uint4*>(xraw);
   uint32_t m = 0;
-  for (int v = b_lo * kVecPerBlock + tid; v < b_hi * kVecPerBlock; v += kDecodeThreads)
-    m = max(m, absmax_bits16B<kBF16>(x4[v]));
+  for (int v = tid; v < (b_hi - b_lo) * kVecPerBlock; v += kDecodeThreads) m = max(m, absmax_bits16B<kBF16>(x4[v]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if (lane == 0) s_red[warp] = m;
@@ -290,9 +293,8 @@ decode_router_kernel(const DecodeParams p) {
   //    its 16 signed bytes at xv + 16 b and its scale at xs[b]; in a cluster
   //    each CTA also stores its blocks into every other CTA's copy.
   for (int b = b_lo + tid; b < b_hi; b += kDecodeThreads) {
-    const int t = b / KB, c = b - t * KB;
     Block16 blk;
-    load_block16_shared<kBF16>(xraw, static_cast<size_t>(t) * D + static_cast<size_t>(c) * kBlock, blk);
+    load_block16_shared<kBF16>(xraw, static_cast<size_t>(b - b_lo) * kBlock, blk);   // xraw holds [b_lo, b_hi)
     uint32_t lo, hi;
     const uint32_t byte = quant_block16_bracket(blk, qs, lo, hi);
     uint4 q;
@@ -538,9 +540,6 @@ DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms, bool bf16) 
   // every thread prefetches at most kMaxBlocksPerThread weight blocks
   const int64_t gs = kDecodeThreads / epc;
   if ((D / kBlock + gs - 1) / gs > kMaxBlocksPerThread) return d;
-  d.smem = decode_smem_layout(static_cast<int>(T), static_cast<int>(D), static_cast<int>(N),
-                              bf16 ? 2 : 4).total;
-  if (d.smem > kDecodeMaxSmem) return d;
   d.epc = epc;
   d.grid = static_cast<int>((N + epc - 1) / epc);
   // several tokens: clusters of CTAs share the staging and quantization of x
@@ -549,6 +548,9 @@ DecodePlan plan_decode(int64_t T, int64_t D, int64_t N, int num_sms, bool bf16) 
     d.cluster = kMaxDecodeCluster;
     d.grid = (d.grid + kMaxDecodeCluster - 1) / kMaxDecodeCluster * kMaxDecodeCluster;
   }
+  d.smem = decode_smem_layout(static_cast<int>(T), static_cast<int>(D), static_cast<int>(N), bf16 ? 2 : 4,
+                              d.cluster).total;
+  if (d.smem > kDecodeMaxSmem) return d;
   d.ok = true;
   return d;
 }

@@ -409,7 +409,7 @@ def test_huge_logits_saturate_without_nan(flags):
 # grid (a barrier in the workspace between quantizing a slice and loading
 # the rest); calls back to back on one workspace reuse the barrier.
 
-@pytest.mark.parametrize("T", [3, 5, 7])
+@pytest.mark.parametrize("T", [3, 5, 7, 12, 16])
 def test_decode_shared_quantization_ragged_token_counts(T):
     case = Case(WL.WORKLOADS["decode"].with_T(T))
     ids, w = case.run(DEC)
