@@ -385,7 +385,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   uint64_t* a_empty = empty_x + kFXSlots;
   uint64_t* q_done = a_empty + kFASlots;                               // [kFASlots]
   uint64_t* acc_full = q_done + kFASlots;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* amax_mbar = acc_full + 1;           // one-cluster grids: the S CTAs' maxima have landed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(amax_mbar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   // producer: ring slots with a fill in flight and the parity of their latest fill
@@ -406,6 +407,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       mbar_init(q_done + a, 8);
     }
     mbar_init(acc_full, 1);
+    mbar_init(amax_mbar, p.S);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_map(&p.tmap_x);
@@ -421,6 +423,10 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // A grid of one cluster exchanges the CTAs' maxima through distributed
+  // shared memory: every CTA must run, its mbarrier initialised, first.
+  const bool one_cluster = p.amax_sync && gridDim.x == static_cast<unsigned>(p.S) && p.S > 1;
+  if (one_cluster) cluster_sync_all();
   // the amax kernel before us (programmatic launch) must have finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // The next kernel of the stream may launch now; it waits for this grid to
@@ -566,7 +572,31 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         uint32_t cm = 0;
         for (int w = 0; w < 8; ++w) cm = max(cm, s_wmax[w]);
         uint32_t bits = 0;
-        gok = grid_amax(p.amax_sync, cm, gridDim.x, bits, deadline, abort_flag);
+        if (one_cluster) {
+          // my maximum into slot `rank` of every CTA, then an arrival on its
+          // mbarrier (release: the store is visible first); wait for all S
+          uint32_t* s_cmax = reinterpret_cast<uint32_t*>(s_fixq) + 16;
+          for (int r = 0; r < p.S; ++r) {
+            uint32_t slot, bar;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(slot) : "r"(smem_u32(s_cmax + rank)), "r"(r));
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(smem_u32(amax_mbar)), "r"(r));
+            asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(slot), "r"(cm) : "memory");
+            asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar) : "memory");
+          }
+          gok = false;
+          for (uint32_t it = 0;; ++it) {
+            uint32_t done;
+            asm volatile("{\n\t.reg .pred q;\n\t"
+                         "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 q, [%1], 0;\n\t"
+                         "selp.u32 %0, 1, 0, q;\n\t}"
+                         : "=r"(done) : "r"(smem_u32(amax_mbar)) : "memory");
+            if (done) { gok = true; break; }
+            if ((it & 63) == 63 && (*abort_flag || globaltimer_ns() > deadline)) break;
+          }
+          for (int r = 0; r < p.S; ++r) bits = max(bits, s_cmax[r]);
+        } else {
+          gok = grid_amax(p.amax_sync, cm, gridDim.x, bits, deadline, abort_flag);
+        }
         s_wmax[8] = bits;
         if (!gok) {
           report_timeout(p.status);
@@ -685,6 +715,12 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     // takes tokens w-2, w+6, ... (up to four at once, their latencies
     // overlapping; the A ring holds each warp's copies of its rows)
     float4* s_row = reinterpret_cast<float4*>(aring) + (warp - 2) * 256;
+    // with 8 or more partial planes the W and x rings (contiguous, idle now)
+    // stage each warp's partial rows, all copied at once (measured: fewer
+    // planes are faster loaded directly): 16 KB per warp -- a valid slot n of
+    // a route call has 8 n < 128 / S, so its rows n * S + s stay below 16
+    float4* stage = p.S >= 8 ? reinterpret_cast<float4*>(wring) + (warp - 2) * 1024 : nullptr;
+    static_assert(8 * 16384 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
     const int per = 128 / p.S;
     const int64_t t0 = static_cast<int64_t>(m_tile) * 128 + static_cast<int64_t>(rank) * per;
     for (int i = warp - 2; i < per; i += 32) {
@@ -695,7 +731,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         tt[n] = (i + 8 * n < per && t < p.T) ? t : -1;
       }
       rt.route<4>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row, lane, p.out_ids, p.out_w,
-                  p.logits);
+                  p.logits, stage);
     }
   }
 

@@ -189,24 +189,57 @@ struct TokenRouter {
 
   // Routes NT tokens at once (independent dependency chains interleave);
   // t[i] < 0 marks an unused slot.  s_row: NT rows of 64 float4 for the warp.
+  // stage: null, or shared memory for the warp's partial rows (row n * S + s:
+  // 64 float4 of token slot n, plane s; only the rows of valid slots are
+  // touched) -- then every partial row is copied in at once (asynchronous
+  // copies, one round trip to L2 whatever S) before the sums.
   template <int NT>
   __device__ __forceinline__ void route(const float* partials, size_t plane, int S, const int64_t (&t)[NT],
                                         float gscale, float4* s_row, int lane, int32_t* out_ids, float* out_w,
-                                        float* logits) const {
+                                        float* logits, float4* stage = nullptr) const {
     float4 a0[NT], a1[NT];
+    if (stage) {
+      for (int s = 0; s < S; ++s)
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const float* row = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * 256;
-      a0[n] = __ldcg(reinterpret_cast<const float4*>(row + 4 * lane));
-      a1[n] = __ldcg(reinterpret_cast<const float4*>(row + 128 + 4 * lane));
-    }
-#pragma unroll 2
-    for (int s = 1; s < S; ++s) {                      // partials in rank order
+        for (int n = 0; n < NT; ++n) {
+          if (t[n] < 0) continue;
+          const float* r = partials + static_cast<size_t>(t[n]) * 256 + s * plane;
+          float4* d = stage + 64 * (n * S + s);
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(d + lane)),
+                       "l"(reinterpret_cast<uint64_t>(r + 4 * lane)) : "memory");
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(d + 32 + lane)),
+                       "l"(reinterpret_cast<uint64_t>(r + 128 + 4 * lane)) : "memory");
+        }
+      asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+      // each lane reads back only what it copied itself: no warp barrier needed
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        const float* r = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * 256 + s * plane;
-        a0[n] = add4(a0[n], __ldcg(reinterpret_cast<const float4*>(r + 4 * lane)));
-        a1[n] = add4(a1[n], __ldcg(reinterpret_cast<const float4*>(r + 128 + 4 * lane)));
+        const bool ok = t[n] >= 0;
+        a0[n] = ok ? stage[64 * (n * S) + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        a1[n] = ok ? stage[64 * (n * S) + 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int s = 1; s < S; ++s)                        // partials in rank order
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          if (t[n] < 0) continue;
+          a0[n] = add4(a0[n], stage[64 * (n * S + s) + lane]);
+          a1[n] = add4(a1[n], stage[64 * (n * S + s) + 32 + lane]);
+        }
+    } else {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const float* row = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * 256;
+        a0[n] = __ldcg(reinterpret_cast<const float4*>(row + 4 * lane));
+        a1[n] = __ldcg(reinterpret_cast<const float4*>(row + 128 + 4 * lane));
+      }
+#pragma unroll 2
+      for (int s = 1; s < S; ++s) {                      // partials in rank order
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const float* r = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * 256 + s * plane;
+          a0[n] = add4(a0[n], __ldcg(reinterpret_cast<const float4*>(r + 4 * lane)));
+          a1[n] = add4(a1[n], __ldcg(reinterpret_cast<const float4*>(r + 128 + 4 * lane)));
+        }
       }
     }
     int col[8];
