@@ -231,18 +231,34 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
                                                               : plan_splitk(T, D, sms);
   float* partials = reinterpret_cast<float*>(w + L.partials);
   if (split_k > 0 && bf16) {
-    // one cluster of S CTAs per token tile: a power of two (each CTA routes
-    // 128/S tokens), no larger than the plan and small enough that every
-    // tile's cluster is resident at once (else the smallest size)
-    const int64_t m_tiles = (T + 127) / 128;
-    int S = 1;
-    for (int c = 16; c >= 2; c >>= 1) {
-      if (c > split_k) continue;
-      if (forced_split || fused_cluster_capacity(c) >= m_tiles) { S = c; break; }
+    // Token tiles of 128 or 112 rows, one cluster of S CTAs per tile: S a
+    // power of two (each CTA routes rows/S tokens), no larger than the plan
+    // and small enough that every tile's cluster is resident at once (else
+    // the smallest size).  The tile height with the least work per CTA (rows
+    // x K stages per CTA) among the grids resident at once wins: 112-row
+    // tiles put 148 CTAs on T = 4096 where 128-row ones leave 24 SMs idle.
+    // Forced split factors keep 128-row tiles.
+    const int n_st = static_cast<int>((D / kBlock + 15) / 16);
+    int tile_rows = 128, S = 1;
+    bool one_launch = false;
+    int64_t best = -1;
+    for (int rows : {128, 112}) {
+      if (forced_split && rows != 128) continue;
+      const int64_t m_tiles = (T + rows - 1) / rows;
+      int c_best = 1;
+      for (int c = 16; c >= 2; c >>= 1) {
+        if (c > split_k) continue;
+        if (forced_split || fused_cluster_capacity(c) >= m_tiles) { c_best = c; break; }
+      }
+      const bool resident = fused_cluster_capacity(c_best) >= m_tiles;
+      const int64_t cost = static_cast<int64_t>(rows) * ((n_st + c_best - 1) / c_best);
+      if (best < 0 || (resident && !one_launch) || (resident == one_launch && cost < best)) {
+        best = cost;
+        tile_rows = rows;
+        S = c_best;
+        one_launch = resident;
+      }
     }
-    // the whole grid resident at once: the kernel computes max|x| itself (one
-    // launch, x's second pass from L2); else the amax kernel runs first
-    const bool one_launch = fused_cluster_capacity(S) >= m_tiles;
     if (!one_launch) {
       prof.before();
       const cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
@@ -255,7 +271,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     st = launch_fused_router(static_cast<const uint16_t*>(x), qrec, x_gsa,
                              one_launch ? reinterpret_cast<uint32_t*>(w + kWsFusedAmax) : nullptr, T, D, W_fp4,
                              W_sf, w_gsa, N, bias, k, routed_scaling, raw, out_ids, out_w, logits, partials, status,
-                             S, stall, s);
+                             S, tile_rows, stall, s);
     prof.after();
     return st;
   }

@@ -62,9 +62,10 @@ constexpr int kFFixQ = 256;                         // exact-pass queue entries 
 constexpr int kFTables = 1024 + 1024 + kFByteTab + 8 * kFFixQ * 2;   // s_scale, s_cc, s_byte, s_fixq
 constexpr int kFSmem = kFWRing + kFXRing + kFARing + kFTables + 512 /*barriers*/ + 1024 /*align*/;
 constexpr int kFThreads = 320;
-constexpr int kFRowsPerWarp = 16;
-constexpr int kFGroup = 8;                          // row pairs quantized together (their chains interleave)
-static_assert((kFRowsPerWarp / 2) % kFGroup == 0 && kFRowsPerWarp / 2 <= 8, "row pairs fit the 3-bit queue field");
+// A token tile has kRows = 128 or 112 rows (the kernel is instantiated for
+// both): each of the eight quantizer warps takes kRows / 8 rows, that is
+// kRows / 16 row pairs, quantized as one group (their chains interleave).
+// With 112 the MMA's last 16 accumulator rows are junk and never stored.
 static_assert(kFWStage % 1024 == 0 && kFASlot % 1024 == 0 && kFXBox % 1024 == 0, "1024-byte aligned tiles");
 static_assert(8 * 8192 <= kFXRing, "store staging fits the x ring");
 
@@ -298,21 +299,22 @@ __device__ __forceinline__ void store_group(uint8_t* ac, uint8_t* asf, int hs, i
 // and then the exact pass over the queued rows; the other modes (IEEE
 // division, or gsa == 0: all codes zero) run in a loop of their own, so that
 // the hot loop holds no other code.
+template <int kRows>
 __device__ __forceinline__ void quant_box(const uint8_t* xb, uint8_t* ac, uint8_t* asf, int hs, int qw, int lane,
                                           int row_end, const QuantTables& tb, uint16_t* fixq) {
+  constexpr int kFRowsPerWarp = kRows / 8, kFGroup = kRows / 16;
+  static_assert(kFGroup <= 8, "row pairs fit the 3-bit queue field");
   const QuantScale& qs = tb.qs;
   const int sub = lane >> 4, l16 = lane & 15;
   if (qs.mode != 1) {
 #pragma unroll 1
-    for (int g = 0; g < kFRowsPerWarp / 2; g += 4) {
+    for (int g = 0; g < kFRowsPerWarp / 2; ++g) {
       if (qw * kFRowsPerWarp + 2 * g >= row_end) break;
-      uint4 v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        v[i] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * (g + i) + sub) * 256 + 16 * l16);
-      uint32_t codes[4] = {0u, 0u, 0u, 0u}, bytes[4] = {0u, 0u, 0u, 0u};
-      if (qs.mode == 2) quant_rows<2, 4>(v, qs, tb.s_scale, codes, bytes);
-      store_group<4>(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
+      uint4 v[1];
+      v[0] = ld_shared_v4(xb + (qw * kFRowsPerWarp + 2 * g + sub) * 256 + 16 * l16);
+      uint32_t codes[1] = {0u}, bytes[1] = {0u};
+      if (qs.mode == 2) quant_rows<2, 1>(v, qs, tb.s_scale, codes, bytes);
+      store_group<1>(ac, asf, hs, qw * kFRowsPerWarp + 2 * g, sub, l16, codes, bytes);
     }
     return;
   }
@@ -367,8 +369,11 @@ __device__ __forceinline__ void quant_box(const uint8_t* xb, uint8_t* ac, uint8_
   }
 }
 
+template <int kRows>
 __global__ void __launch_bounds__(kFThreads, 1)
 fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
+  constexpr int kFRowsPerWarp = kRows / 8;
+  constexpr uint32_t kBoxBytes = 128u * kRows * 2u;  // one bf16 x box: kRows rows x 128 elements
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wring = smem;
@@ -458,8 +463,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
           break;
         }
         if (elect_one()) {
-          mbar_arrive_expect_tx(full_x + xs, kFXBox);
-          tma_load_2d(xring + xs * kFXBox, &p.tmap_x, ks * 256 + hs * 128, m_tile * 128, full_x + xs);
+          mbar_arrive_expect_tx(full_x + xs, kBoxBytes);
+          tma_load_2d(xring + xs * kFXBox, &p.tmap_x, ks * 256 + hs * 128, m_tile * kRows, full_x + xs);
         }
         __syncwarp();
         filled_x |= 1u << xs;
@@ -538,6 +543,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   } else {
     // ---------------------------------------------------------- quantizers
     rt.init(p.bias, p.N, p.k, p.raw, p.routed_scaling, lane);       // for the epilogue
+    const float w_gsa = __ldg(p.w_gsa);                               // off the path after the barrier
     const int qw = warp - 2;
     bool ok = true;
     int xi = 0;                                        // x boxes consumed so far
@@ -619,13 +625,13 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         p.qrec[3] = amax;
         *p.gsa_out = qs.gsa;
       }
-      gscale = __fmul_rn(qs.gsa, __ldg(p.w_gsa));
+      gscale = __fmul_rn(qs.gsa, w_gsa);
     } else {
       qs.gsa = __ldg(p.qrec);
       qs.rgsa = __ldg(p.qrec + 1);
       qs.mode = __float_as_int(__ldg(p.qrec + 2));
       amax = __ldg(p.qrec + 3);
-      gscale = __fmul_rn(__ldg(p.x_gsa), __ldg(p.w_gsa));
+      gscale = __fmul_rn(__ldg(p.x_gsa), w_gsa);
     }
     // bracketing quantizer (mode 1): the scale byte of every bf16 block max
     // within ~20 binades below amax, and the bracketing multipliers per byte
@@ -672,7 +678,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         const bool okx = __all_sync(0xFFFFFFFFu, mbar_wait(full_x + xs, xph, deadline, abort_flag));
         ok = ok && okx;
         if (okx) {
-          quant_box(xring + xs * kFXBox, ac, asf, hs, qw, lane, p.T - m_tile * 128, tb, s_fixq + qw * kFFixQ);
+          quant_box<kRows>(xring + xs * kFXBox, ac, asf, hs, qw, lane, p.T - m_tile * kRows, tb, s_fixq + qw * kFFixQ);
         }
         // this warp has read its rows of the box
         __syncwarp();
@@ -698,8 +704,9 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     tc_fence_after();
     // every x box has been read (the last MMA needed them all): the x ring
     // stages the stores
-    store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * 256, xring, tmem, warp, lane, m_tile,
-                       p.n_half, p.T, my_st > 0 && acc_ok);
+    store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * 256, xring, tmem, warp, lane,
+                       static_cast<int64_t>(m_tile) * kRows, min(kRows, p.T - m_tile * kRows), p.n_half,
+                       my_st > 0 && acc_ok);
   }
 
   // The S CTAs of this token tile form the cluster: after the barrier every
@@ -721,8 +728,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     // a route call has 8 n < 128 / S, so its rows n * S + s stay below 16
     float4* stage = p.S >= 8 ? reinterpret_cast<float4*>(wring) + (warp - 2) * 1024 : nullptr;
     static_assert(8 * 16384 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
-    const int per = 128 / p.S;
-    const int64_t t0 = static_cast<int64_t>(m_tile) * 128 + static_cast<int64_t>(rank) * per;
+    const int per = kRows / p.S;
+    const int64_t t0 = static_cast<int64_t>(m_tile) * kRows + static_cast<int64_t>(rank) * per;
     for (int i = warp - 2; i < per; i += 32) {
       int64_t tt[4];
 #pragma unroll
@@ -753,13 +760,14 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// bf16 activations [T, D]: 128 x 128 boxes, no swizzle, zeros outside.
-bool encode_x(CUtensorMap* map, const uint16_t* ptr, int64_t T, int64_t D) {
+// bf16 activations [T, D]: boxes of box_rows rows x 128 elements, no swizzle,
+// zeros outside.
+bool encode_x(CUtensorMap* map, const uint16_t* ptr, int64_t T, int64_t D, uint32_t box_rows) {
   auto encode = tensor_map_encoder();
   if (!encode) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(ptr), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -768,15 +776,18 @@ bool encode_x(CUtensorMap* map, const uint16_t* ptr, int64_t T, int64_t D) {
 
 }  // namespace
 
-// Per-device function attributes: the dynamic shared memory and clusters of
-// up to 16 CTAs (beyond the portable 8; the planner asks first).
+// Per-device function attributes of both instantiations: the dynamic shared
+// memory and clusters of up to 16 CTAs (beyond the portable 8; the planner
+// asks first).
 static cudaError_t fused_prepare(int dev) {
   static bool done[kMaxDevices] = {};
   if (done[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(fused_qgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fused_qgemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
+  for (auto* fn : {fused_qgemm_kernel<128>, fused_qgemm_kernel<112>}) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   done[dev] = true;
   return cudaSuccess;
 }
@@ -804,7 +815,8 @@ int fused_cluster_capacity(int S) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fused_qgemm_kernel, &cfg) != cudaSuccess) n = 0;
+  // both instantiations have the same resources
+  if (cudaOccupancyMaxActiveClusters(&n, fused_qgemm_kernel<128>, &cfg) != cudaSuccess) n = 0;
   cudaGetLastError();
   cap[dev][slot] = n;
   known[dev][slot] = true;
@@ -815,17 +827,18 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
-                               bool test_stall, cudaStream_t s) {
+                               int tile_rows, bool test_stall, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVR_ERR_CUDA;
   if (N > 256 || k > kMaxKmax || S < 1 || S > 16 || 128 % S) return NVR_ERR_UNSUPPORTED;
+  if (tile_rows != 128 && tile_rows != 112) return NVR_ERR_UNSUPPORTED;
   if (static_cast<size_t>(S) * static_cast<size_t>((T + 127) / 128 * 128) > splitk_partial_rows(T))
     return NVR_ERR_UNSUPPORTED;
   const cudaError_t e = fused_prepare(dev);
   if (e != cudaSuccess) return cuda_status(e);
   FusedParams g;
   const int n_half = N > 128 ? 2 : 1;
-  if (!encode_x(&g.tmap_x, x, T, D)) return NVR_ERR_UNSUPPORTED;
+  if (!encode_x(&g.tmap_x, x, T, D, static_cast<uint32_t>(tile_rows))) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes(&g.tmap_b, W_codes, N, D, 128u * n_half)) return NVR_ERR_UNSUPPORTED;
   g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
   g.amax_sync = amax_sync; g.gsa_out = x_gsa;
@@ -842,13 +855,14 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((T + 127) / 128 * S));
+  cfg.gridDim = dim3(static_cast<unsigned>((T + tile_rows - 1) / tile_rows * S));
   cfg.blockDim = dim3(kFThreads);
   cfg.dynamicSmemBytes = kFSmem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cuda_status(cudaLaunchKernelEx(&cfg, fused_qgemm_kernel, g));
+  return cuda_status(tile_rows == 112 ? cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<112>, g)
+                                      : cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<128>, g));
 }
 
 }  // namespace nvr

@@ -96,7 +96,8 @@ nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64
                               uint32_t* status, int S, bool test_stall, cudaStream_t s);
 // The router for bf16 activations and N <= 256 in one kernel: quantization
 // inside the K-split GEMM, partials through L2 and the epilogue (cluster of S
-// CTAs per 128-token tile, S in {1,2,4,8,16}).  With amax_sync (4 zeroed
+// CTAs per token tile of tile_rows = 128 or 112 rows, S in {1,2,4,8,16}).
+// With amax_sync (4 zeroed
 // workspace words) the kernel also computes max|x| itself and publishes qrec
 // and x_gsa -- every CTA of the grid must then be resident at once; without
 // it, qrec and x_gsa come from the amax kernel launched before.
@@ -106,7 +107,7 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
-                               bool test_stall, cudaStream_t s);
+                               int tile_rows, bool test_stall, cudaStream_t s);
 nvr_status launch_router_epilogue(const float* partials, int S, const float* x_gsa, const float* w_gsa,
                                   int64_t T, int64_t N, const float* bias, int k, float routed_scaling,
                                   bool raw, int32_t* out_ids, float* out_w, float* logits, cudaStream_t s);

@@ -68,9 +68,9 @@ __device__ __forceinline__ void store_partial_tile(const CUtensorMap* tmap_p, ui
 // through the warp's 4 KB staging buffer at stg_base + (warp-2) * 4 KB (128-byte
 // swizzle, conflict-free both ways) and leaves as 512-byte coalesced rows.
 __device__ __forceinline__ void store_partial_rows(float* plane, uint8_t* stg_base, uint32_t tmem, int warp,
-                                                   int lane, int m_tile, int n_half, int T, bool have_acc) {
+                                                   int lane, int64_t row0, int rows, int n_half, bool have_acc) {
   const int q = warp & 3, h = (warp - 2) >> 2;
-  if (h >= n_half || m_tile * 128 + q * 32 >= T) return;
+  if (h >= n_half || q * 32 >= rows) return;
   uint8_t* buf = stg_base + (warp - 2) * 4096;
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
@@ -89,9 +89,8 @@ __device__ __forceinline__ void store_partial_rows(float* plane, uint8_t* stg_ba
     for (int i = 0; i < 8; ++i) {
       const int r = 4 * i + (lane >> 3), j = lane & 7;
       const uint4 val = ld_shared_v4(buf + r * 128 + ((j ^ (r & 7)) << 4));
-      const int64_t token = static_cast<int64_t>(m_tile) * 128 + q * 32 + r;
-      if (token < T)
-        *reinterpret_cast<uint4*>(plane + token * 256 + h * 128 + c * 32 + 4 * j) = val;
+      if (q * 32 + r < rows)
+        *reinterpret_cast<uint4*>(plane + (row0 + q * 32 + r) * 256 + h * 128 + c * 32 + 4 * j) = val;
     }
     __syncwarp();
   }
