@@ -38,6 +38,8 @@
 //              planes, one warp per token (TokenRouter, nvr_splitk.cuh).
 // Tensor memory: accumulator at columns 0-255; scales of A slot a at
 // 256 + 48 a (x: 4 columns per K step, W: 8).
+#include <type_traits>
+
 #include "nvr_splitk.cuh"
 
 namespace nvr {
@@ -730,16 +732,24 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     static_assert(8 * 16384 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
     const int per = kRows / p.S;
     const int64_t t0 = static_cast<int64_t>(m_tile) * kRows + static_cast<int64_t>(rank) * per;
-    for (int i = warp - 2; i < per; i += 32) {
-      int64_t tt[4];
+    // as many token slots per call as the warp has tokens (8, 16 or more
+    // tokens per CTA: 1, 2 or 4) -- empty slots would still be sorted
+    const auto route_n = [&](auto nt) {
+      constexpr int NT = decltype(nt)::value;
+      for (int i = warp - 2; i < per; i += 8 * NT) {
+        int64_t tt[NT];
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const int64_t t = t0 + i + 8 * n;
-        tt[n] = (i + 8 * n < per && t < p.T) ? t : -1;
+        for (int n = 0; n < NT; ++n) {
+          const int64_t t = t0 + i + 8 * n;
+          tt[n] = (i + 8 * n < per && t < p.T) ? t : -1;
+        }
+        rt.route<NT>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row, lane, p.out_ids, p.out_w,
+                     p.logits, stage);
       }
-      rt.route<4>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row, lane, p.out_ids, p.out_w,
-                  p.logits, stage);
-    }
+    };
+    if (per <= 8) route_n(std::integral_constant<int, 1>());
+    else if (per <= 16) route_n(std::integral_constant<int, 2>());
+    else route_n(std::integral_constant<int, 4>());
   }
 
   tc_fence_before();
