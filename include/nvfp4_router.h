@@ -100,12 +100,15 @@ enum {
   NVR_FLAG_FORCE_TENSOR_CORE = 2u,
   NVR_FLAG_FORCE_DECODE = 4u,
   /* Tensor-core kernel choice (each implies FORCE_TENSOR_CORE; at most one).
-   * By default heads of up to 256 experts split K over S CTAs per 128-token
-   * tile (S from T, D and the SM count; fp32 partial logits in the workspace,
-   * summed by a second, warp-per-token epilogue kernel), and wider heads split
-   * N across CTAs.  SPLIT_K_2/4/8 force S (NVR_ERR_UNSUPPORTED when N > 256);
-   * SPLIT_N forces the N-split kernel for any N.  Results agree within the
-   * same tolerances; the logits' fp32 summation order differs. */
+   * By default heads of up to 256 experts split K over a cluster of S CTAs
+   * per token tile (S and the tile height, 128 or 112 rows, from T, D and
+   * the number of clusters the device holds at once; fp32 partial logits
+   * pass through the workspace, L2-resident, to the CTAs of the same
+   * cluster, which route the tile's tokens), and wider heads split N across
+   * CTAs.  SPLIT_K_2/4/8 force S with 128-row tiles (NVR_ERR_UNSUPPORTED
+   * when N > 256); SPLIT_N forces the N-split kernel for any N.  Results
+   * agree within the same tolerances; the logits' fp32 summation order
+   * differs. */
   NVR_FLAG_SPLIT_K_2 = 8u,
   NVR_FLAG_SPLIT_K_4 = 16u,
   NVR_FLAG_SPLIT_K_8 = 32u,
@@ -210,12 +213,21 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k);
  *                selected sigmoid scores s (RAW: the selected logits)
  *   workspace    router_gate_workspace_size(T, D, N, k) bytes, zeroed once
  *
- * Small batches (decode) run as a single kernel launch.  Larger ones run as
- * amax, quantize, GEMM and epilogue launches (programmatic dependent launch
- * chains them without host involvement): with up to 256 experts the K-split
- * fp32 partial logits pass through the workspace (L2-resident) to the
- * epilogue kernel; wider heads consume the logits from tensor memory in the
- * GEMM kernel itself.
+ * Launches per call (programmatic dependent launch chains several without
+ * host involvement):
+ *   - T <= 16 (decode): one kernel; for T >= 2 its CTAs form clusters of 4
+ *     that share the staging and quantization of x through distributed
+ *     shared memory.
+ *   - bf16 x, N <= 256: one kernel that takes max|x| itself (a bounded grid
+ *     barrier, or a cluster barrier when the grid is one cluster), quantizes
+ *     x inside the K-split GEMM and routes each tile's tokens from the fp32
+ *     partial logits (L2-resident workspace).  When the grid cannot be
+ *     resident at once (a forced split on a large T), an amax kernel runs
+ *     first and the same kernel skips its own max|x| pass.
+ *   - fp32 x, N <= 256: amax, quantize, K-split GEMM and a warp-per-token
+ *     epilogue kernel.
+ *   - N > 256: amax, quantize and the N-split GEMM, which routes from the
+ *     logits in tensor memory.
  */
 nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
                             const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,
