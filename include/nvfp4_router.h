@@ -39,8 +39,10 @@
  *   the workspace status word, which nvr_read_device_status returns.
  * - Workspace: caller-allocated device memory of at least the size the
  *   matching *_workspace_size function returns, 256-byte aligned, ZEROED ONCE
- *   before first use.  Every call leaves its counters at zero again, so the
- *   same workspace serves any number of calls on one stream.  Calls that share
+ *   before first use.  Every call leaves its counters ready for the next, so the
+ *   same workspace serves any number of calls on one stream, of any T up to
+ *   the T_max it was sized for (the counters sit at fixed offsets, outside the
+ *   regions whose size depends on T).  Calls that share
  *   a workspace must not run concurrently.  After a call that returned an
  *   error or timed out, zero the workspace again.
  * - Non-finite inputs (NaN, Inf) are outside the contract: the output is
@@ -128,6 +130,19 @@ const char* nvr_status_string(nvr_status s);
  * host thread ("cudaSuccess" if none; static string, never NULL).  No
  * counterpart on the pages: a diagnostic for launch failures. */
 const char* nvr_last_cuda_error(void);
+
+/* The launch plan of the most recent router_gate_topk / router_gate_logits
+ * call that reached a launch on this host thread, as four ints:
+ *   out[0] kernel sequence: 0 none yet, 1 the decode kernel, 2 the one-launch
+ *          fused router, 3 amax then the fused router, 4 amax, quantize,
+ *          K-split GEMM and epilogue kernel, 5 amax, quantize and the
+ *          N-split GEMM;
+ *   out[1] token-tile rows (128 or 112; 0 for sequences 0, 1);
+ *   out[2] CTAs per token tile (K splits for 2-4, N splits for 5; 0 for 0, 1);
+ *   out[3] 1 when the CTAs of a tile form a thread-block cluster, else 0.
+ * No counterpart on the pages: a diagnostic for tests and benchmarks.
+ * NVR_ERR_INVALID_ARG for a NULL out. */
+nvr_status nvr_last_router_plan(int* out);
 
 /* Bytes of a scale-byte buffer for [rows, D] in the given layout
  * (0 for invalid arguments). */

@@ -29,7 +29,7 @@ from ._native import (NVR_FLAG_FORCE_DECODE, NVR_FLAG_FORCE_TENSOR_CORE, NVR_FLA
 
 __all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits",
            "router_gate_workspace_size", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
-           "nvr_read_device_status", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
+           "nvr_read_device_status", "last_router_plan", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
            "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "NVR_FLAG_SPLIT_K_2",
            "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "new_workspace"]
 
@@ -151,6 +151,20 @@ def router_gate_logits(x, W_fp4, W_sf, w_gsa, logits=None, workspace=None, flags
         workspace.numel(), _stream(stream))
     _native.check("router_gate_logits", st)
     return logits
+
+
+_PLAN_SEQUENCES = {0: "none", 1: "decode", 2: "fused", 3: "amax+fused", 4: "amax+quantize+splitk+epilogue",
+                   5: "amax+quantize+splitn"}
+
+
+def last_router_plan():
+    """The launch plan of this thread's latest router call: a dict with the
+    kernel sequence, token-tile rows, CTAs per tile and whether they form a
+    cluster."""
+    out = (ctypes.c_int * 4)()
+    _native.check("nvr_last_router_plan", _native.lib().nvr_last_router_plan(out))
+    return {"sequence": _PLAN_SEQUENCES.get(out[0], str(out[0])), "tile_rows": out[1],
+            "ctas_per_tile": out[2], "clustered": bool(out[3])}
 
 
 def nvr_read_device_status(workspace, stream=None):

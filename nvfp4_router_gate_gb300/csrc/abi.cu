@@ -70,8 +70,12 @@ WsLayout router_ws_layout(int64_t T, int64_t D, int64_t N) {
   const int64_t rows_pad = (T + 127) / 128 * 128;
   const int m_tiles = static_cast<int>(rows_pad / 128);
   const int n_tiles = static_cast<int>((N + 127) / 128);
+  // The counters sit at offsets and sizes that do not depend on T: calls of
+  // any size may share a workspace sized for the largest, and no call's data
+  // regions may cover the words another call expects at zero.
   L.tickets = L.total;
-  L.x_codes = a256(L.tickets + static_cast<size_t>(m_tiles) * 4);
+  L.tile_sync = a256(L.tickets + static_cast<size_t>(kMaxTicketTiles) * 4);
+  L.x_codes = a256(L.tile_sync + static_cast<size_t>(kMaxFlatTiles) * 8);
   L.x_sf = a256(L.x_codes + static_cast<size_t>(rows_pad) * (D / 2));
   L.partials = a256(L.x_sf + static_cast<size_t>(rows_pad) * (D / 16));
   const int splits = split_bound(m_tiles, n_tiles);
@@ -91,6 +95,15 @@ WsLayout router_ws_layout(int64_t T, int64_t D, int64_t N) {
 namespace nvr {
 
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+// nvr_last_router_plan: {kernel sequence, tile rows, CTAs per tile, clustered}
+thread_local int g_last_plan[4] = {0, 0, 0, 0};
+
+static void record_plan(int seq, int rows, int per_tile, bool clustered) {
+  g_last_plan[0] = seq;
+  g_last_plan[1] = rows;
+  g_last_plan[2] = per_tile;
+  g_last_plan[3] = clustered ? 1 : 0;
+}
 
 nvr_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return NVR_OK;
@@ -206,6 +219,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     if (!dp.ok) return NVR_ERR_UNSUPPORTED;
     float* keys = reinterpret_cast<float*>(w + L.decode);
     float* scores = keys + T * N;
+    record_plan(1, 0, 0, dp.cluster > 1);
     ProfileScope prof(s);
     prof.before();
     cudaError_t e = launch_decode(x, bf16, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
@@ -231,34 +245,41 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
                                                               : plan_splitk(T, D, sms);
   float* partials = reinterpret_cast<float*>(w + L.partials);
   if (split_k > 0 && bf16) {
-    // Token tiles of 128 or 112 rows, one cluster of S CTAs per tile: S a
-    // power of two (each CTA routes rows/S tokens), no larger than the plan
-    // and small enough that every tile's cluster is resident at once (else
-    // the smallest size).  The tile height with the least work per CTA (rows
-    // x K stages per CTA) among the grids resident at once wins: 112-row
-    // tiles put 148 CTAs on T = 4096 where 128-row ones leave 24 SMs idle.
-    // Forced split factors keep 128-row tiles.
+    // Token tiles of 128 or 112 rows, S CTAs per tile (S a power of two no
+    // larger than the plan; each CTA routes rows/S tokens) that form a cluster
+    // or, without clusters, meet at a barrier in the workspace.  Among the
+    // grids resident at once the one with the least work per CTA (rows x K
+    // stages per CTA) wins, clusters on a tie; the device holds fewer CTAs in
+    // clusters than without (whole clusters per GPC), so at T = 4096 112-row
+    // tiles put 148 CTAs on the SMs without clusters where clusters of 4 hold
+    // 128.  Forced split factors keep 128-row tiles.  With no resident grid:
+    // clusters, after the amax kernel.
     const int n_st = static_cast<int>((D / kBlock + 15) / 16);
+    const int block_cap = fused_block_capacity();
     int tile_rows = 128, S = 1;
-    bool one_launch = false;
+    bool one_launch = false, flat = false;
     int64_t best = -1;
     for (int rows : {128, 112}) {
       if (forced_split && rows != 128) continue;
       const int64_t m_tiles = (T + rows - 1) / rows;
-      int c_best = 1;
-      for (int c = 16; c >= 2; c >>= 1) {
-        if (c > split_k) continue;
-        if (forced_split || fused_cluster_capacity(c) >= m_tiles) { c_best = c; break; }
-      }
-      const bool resident = fused_cluster_capacity(c_best) >= m_tiles;
-      const int64_t cost = static_cast<int64_t>(rows) * ((n_st + c_best - 1) / c_best);
-      if (best < 0 || (resident && !one_launch) || (resident == one_launch && cost < best)) {
-        best = cost;
-        tile_rows = rows;
-        S = c_best;
-        one_launch = resident;
+      for (int c = 16; c >= 1; c >>= 1) {
+        if (forced_split ? c != forced_split : c > split_k) continue;
+        const int64_t cost = static_cast<int64_t>(rows) * ((n_st + c - 1) / c);
+        for (int f = 0; f < (c > 1 ? 2 : 1); ++f) {
+          const bool resident = f ? m_tiles * c <= block_cap && m_tiles <= kMaxFlatTiles
+                                  : fused_cluster_capacity(c) >= m_tiles;
+          if (f && !resident) continue;
+          if (best < 0 || (resident && !one_launch) || (resident == one_launch && cost < best)) {
+            best = cost;
+            tile_rows = rows;
+            S = c;
+            flat = f != 0;
+            one_launch = resident;
+          }
+        }
       }
     }
+    record_plan(one_launch ? 2 : 3, tile_rows, S, !flat);
     if (!one_launch) {
       prof.before();
       const cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
@@ -269,12 +290,17 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     }
     prof.before();
     st = launch_fused_router(static_cast<const uint16_t*>(x), qrec, x_gsa,
-                             one_launch ? reinterpret_cast<uint32_t*>(w + kWsFusedAmax) : nullptr, T, D, W_fp4,
+                             one_launch ? reinterpret_cast<uint32_t*>(w + kWsFusedAmax) : nullptr,
+                             one_launch ? reinterpret_cast<uint32_t*>(w + L.tile_sync) : nullptr, flat, T, D, W_fp4,
                              W_sf, w_gsa, N, bias, k, routed_scaling, raw, out_ids, out_w, logits, partials, status,
                              S, tile_rows, stall, s);
     prof.after();
     return st;
   }
+  const GemmPlan g = plan_gemm(T, N, sms);
+  if (split_k == 0 && g.m_tiles > kMaxTicketTiles) return NVR_ERR_UNSUPPORTED;
+  if (split_k > 0) record_plan(4, 128, split_k, false);
+  else record_plan(5, 128, g.n_splits, false);
   prof.before();
   cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
                                    reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec, status, sms, s);
@@ -295,7 +321,6 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     prof.after();
     return st;
   }
-  const GemmPlan g = plan_gemm(T, N, sms);
   prof.before();
   st = launch_gemm_topk(xc, xsf, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
                         out_ids, out_w, logits, reinterpret_cast<float4*>(w + L.partials),
@@ -309,6 +334,12 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
 extern "C" {
 
 const char* nvr_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
+
+nvr_status nvr_last_router_plan(int* out) {
+  if (!out) return NVR_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) out[i] = g_last_plan[i];
+  return NVR_OK;
+}
 
 const char* nvr_status_string(nvr_status s) {
   switch (s) {
@@ -369,7 +400,8 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k) {
     if (pk > part) part = pk;
   }
   const int64_t t_dec = T_max < 16 ? T_max : 16;
-  return quantize_ws_layout(T_max, D).total + static_cast<size_t>(m_max) * 4 +
+  return quantize_ws_layout(T_max, D).total + static_cast<size_t>(kMaxTicketTiles) * 4 +
+         static_cast<size_t>(kMaxFlatTiles) * 8 +
          static_cast<size_t>(rows_pad) * (D / 2) + static_cast<size_t>(rows_pad) * (D / 16) + part +
          static_cast<size_t>(t_dec) * N * 8 + 8 * 256;
 }

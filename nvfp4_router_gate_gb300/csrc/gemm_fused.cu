@@ -14,8 +14,10 @@
 // reached by table lookups and bracketing products (quant_rows_bracket) with
 // an exact pass over the rare rows near a rounding boundary.
 //
-// A token tile of 128 rows is split along K over S CTAs (S = 1 to 16, a power
-// of two) that form one thread-block cluster.  Per CTA (rank r, 320 threads):
+// A token tile of 128 (or 112) rows is split along K over S CTAs (S = 1 to
+// 16, a power of two) that form one thread-block cluster, or, in a grid the
+// device holds at once without clusters, meet at a barrier in the workspace
+// (tile_barrier) before routing.  Per CTA (rank r, 320 threads):
 //   warp 0     TMA producer: per stage of 256 K-elements two bf16 x boxes
 //              (128 rows x 128 elements, 32 KB each) into a 3-slot ring, and
 //              the W tile (128 or 256 rows x 128 bytes, 128-byte swizzle) with
@@ -34,8 +36,9 @@
 //              accumulator;
 //   warps 2-9  after the last MMA: the fp32 partial (128 x 256) goes from
 //              tensor memory to partial plane r of the workspace (L2); after a
-//              cluster barrier each CTA routes its own 128/S tokens from the S
-//              planes, one warp per token (TokenRouter, nvr_splitk.cuh).
+//              cluster (or tile) barrier each CTA routes its own 128/S tokens
+//              from the S planes, one warp per token (TokenRouter,
+//              nvr_splitk.cuh).
 // Tensor memory: accumulator at columns 0-255; scales of A slot a at
 // 256 + 48 a (x: 4 columns per K step, W: 8).
 #include <type_traits>
@@ -76,7 +79,9 @@ struct FusedParams {
   CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 x (128 * n_half)
   float* qrec;                 // quantizer record {gsa, 1/gsa, mode, amax}: from the amax kernel, or
                                // published by this kernel's last CTA when amax_sync is set
-  uint32_t* amax_sync;         // in-kernel amax: 4 workspace words (grid_amax), or null
+  uint32_t* amax_sync;         // in-kernel amax: 5 workspace words (grid_amax), or null
+  uint32_t* tile_sync;         // with amax_sync: the tile barriers' arrival counters [2][kMaxFlatTiles]
+  int flat;                    // launch without clusters: a tile's CTAs meet at tile_barrier
   float* gsa_out;              // in-kernel amax: x's global scale (also x_gsa)
   const uint8_t* sfb;          // W scales, tile layout
   float* partials;             // [S][T][256] fp32 partial logits (workspace)
@@ -109,30 +114,43 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
-// Grid-wide max |x| bits, for one thread per CTA, over 4 workspace words:
-// sync[0..1] the max of calls of even / odd generation, sync[2] arrivals,
-// sync[3] the generation.  A CTA folds its max into its generation's slot and
-// arrives (release); the last to arrive (acquire) resets the arrivals and the
-// other generation's slot -- the next call's, untouched until this grid has
-// finished -- and opens the barrier by bumping the generation (release); the
-// others wait for it (acquire, bounded).  Every CTA then reads the complete
-// max.  All CTAs of the grid must be resident.
+// Grid-wide max |x| bits, for one thread per CTA, over 5 workspace words:
+// sync[0..1] the maximum and sync[2..3] the arrivals of calls of even / odd
+// generation, sync[4] the generation.  A CTA folds its max into its
+// generation's slot and arrives (a release increment, nothing returned);
+// all then wait (acquire, bounded) until every CTA has arrived -- nobody has
+// to answer anybody -- and read the complete max.  CTA 0 then bumps the
+// generation for the next call (every CTA of this call read it before
+// arriving).  Each call zeroes the other generation's words at its start
+// (the call that used them has completed).  All CTAs of the grid must be
+// resident.
 __device__ bool grid_amax(uint32_t* sync, uint32_t cta_max, uint32_t n_ctas, uint32_t& amax_bits,
                           uint64_t deadline, volatile int* abort_flag) {
-  const uint32_t gen = ld_acquire_gpu(sync + 3);
-  uint32_t* slot = sync + (gen & 1u);
-  uint32_t t;
-  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" :: "l"(slot), "r"(cta_max) : "memory");
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(sync + 2) : "memory");
-  if (t == n_ctas - 1) {
-    sync[(gen + 1u) & 1u] = 0u;
-    sync[2] = 0u;
-    st_release_gpu(sync + 3, gen + 1u);
-  } else {
-    while (ld_acquire_gpu(sync + 3) == gen)
-      if (*abort_flag || globaltimer_ns() > deadline) return false;
-  }
-  amax_bits = ld_acquire_gpu(slot);
+  const uint32_t gen = ld_acquire_gpu(sync + 4);
+  const uint32_t par = gen & 1u;
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" :: "l"(sync + par), "r"(cta_max) : "memory");
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(sync + 2 + par) : "memory");
+  while (ld_acquire_gpu(sync + 2 + par) < n_ctas)
+    if (*abort_flag || globaltimer_ns() > deadline) return false;
+  if (blockIdx.x == 0) sync[4] = gen + 1u;
+  amax_bits = ld_acquire_gpu(sync + par);
+  return true;
+}
+
+// Barrier of the n CTAs of one token tile, for one thread per CTA, on one
+// arrival counter in the workspace: a release increment, then acquire reads
+// until all n have arrived -- no CTA has to answer another, so the barrier
+// costs one trip to L2 and back after the last arrival.  The partial rows the
+// CTA's threads stored before a __syncthreads are visible to the other CTAs
+// after theirs.  Calls alternate between two counter sets by the parity of
+// the grid barrier's generation (the same in every CTA of a call); each call
+// zeroes the other set's counter of its tile for the next call (the call that
+// used it has completed; every call with the in-kernel amax does this, with
+// or without clusters).  The n CTAs must be resident together.
+__device__ bool tile_barrier(uint32_t* count, uint32_t n, uint64_t deadline, volatile int* abort_flag) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(count) : "memory");
+  while (ld_acquire_gpu(count) < n)
+    if (*abort_flag || globaltimer_ns() > deadline) return false;
   return true;
 }
 
@@ -432,10 +450,25 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   const uint32_t tmem = *tmem_holder;
   // A grid of one cluster exchanges the CTAs' maxima through distributed
   // shared memory: every CTA must run, its mbarrier initialised, first.
-  const bool one_cluster = p.amax_sync && gridDim.x == static_cast<unsigned>(p.S) && p.S > 1;
+  const bool one_cluster = p.amax_sync && !p.flat && gridDim.x == static_cast<unsigned>(p.S) && p.S > 1;
   if (one_cluster) cluster_sync_all();
   // the amax kernel before us (programmatic launch) must have finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Barrier words: this call uses those of the grid barrier's generation
+  // parity (the same for every CTA until all have arrived there) and zeroes
+  // the other parity's -- the grid barrier's maximum and arrivals and the
+  // whole set of tile-barrier counters -- for the next call.
+  uint32_t* tile_count = nullptr;
+  if (p.amax_sync && warp == 0) {
+    const uint32_t par = ld_acquire_gpu(p.amax_sync + 4) & 1u;
+    tile_count = p.tile_sync + par * kMaxFlatTiles + m_tile;
+    uint32_t* other = p.tile_sync + (par ^ 1u) * kMaxFlatTiles;
+    for (int i = blockIdx.x * 32 + lane; i < kMaxFlatTiles; i += gridDim.x * 32) other[i] = 0u;
+    if (blockIdx.x == 0 && lane == 0) {
+      p.amax_sync[par ^ 1u] = 0u;
+      p.amax_sync[2 + (par ^ 1u)] = 0u;
+    }
+  }
   // The next kernel of the stream may launch now; it waits for this grid to
   // complete before it reads anything.
   asm volatile("griddepcontrol.launch_dependents;");
@@ -711,11 +744,22 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
                        my_st > 0 && acc_ok);
   }
 
-  // The S CTAs of this token tile form the cluster: after the barrier every
-  // partial row of the tile is visible to all of them.
+  // The S CTAs of this token tile form the cluster, or meet at the tile's
+  // barrier in the workspace: after it every partial row of the tile is
+  // visible to all of them.
   tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();
+  if (p.flat) {
+    __syncthreads();
+    if (threadIdx.x == 0 && p.S > 1 &&
+        !tile_barrier(tile_count, static_cast<uint32_t>(p.S), deadline, abort_flag)) {
+      report_timeout(p.status);
+      *abort_flag = 1;
+    }
+    __syncthreads();
+  } else {
+    __syncwarp();
+    cluster_sync_all();
+  }
   tc_fence_after();
 
   if (warp >= 2) {
@@ -802,6 +846,24 @@ static cudaError_t fused_prepare(int dev) {
   return cudaSuccess;
 }
 
+// How many CTAs of this kernel the device holds at once without clusters
+// (cached per device; 0 on error).
+int fused_block_capacity() {
+  static int cap[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cap[dev] > 0) return cap[dev];
+  if (fused_prepare(dev) != cudaSuccess) return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_qgemm_kernel<128>, kFThreads, kFSmem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cap[dev] = per_sm * device_sm_count();
+  return cap[dev];
+}
+
 // How many clusters of S CTAs of this kernel the device can hold at once
 // (cached per device and size; 0 when the size cannot be scheduled).
 int fused_cluster_capacity(int S) {
@@ -833,7 +895,8 @@ int fused_cluster_capacity(int S) {
   return n;
 }
 
-nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync, int64_t T, int64_t D,
+nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync,
+                               uint32_t* tile_sync, bool flat, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
@@ -842,6 +905,8 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVR_ERR_CUDA;
   if (N > 256 || k > kMaxKmax || S < 1 || S > 16 || 128 % S) return NVR_ERR_UNSUPPORTED;
   if (tile_rows != 128 && tile_rows != 112) return NVR_ERR_UNSUPPORTED;
+  if (amax_sync && !tile_sync) return NVR_ERR_INVALID_ARG;
+  if (flat && (!amax_sync || (T + tile_rows - 1) / tile_rows > kMaxFlatTiles)) return NVR_ERR_UNSUPPORTED;
   if (static_cast<size_t>(S) * static_cast<size_t>((T + 127) / 128 * 128) > splitk_partial_rows(T))
     return NVR_ERR_UNSUPPORTED;
   const cudaError_t e = fused_prepare(dev);
@@ -851,7 +916,7 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   if (!encode_x(&g.tmap_x, x, T, D, static_cast<uint32_t>(tile_rows))) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes(&g.tmap_b, W_codes, N, D, 128u * n_half)) return NVR_ERR_UNSUPPORTED;
   g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
-  g.amax_sync = amax_sync; g.gsa_out = x_gsa;
+  g.amax_sync = amax_sync; g.tile_sync = tile_sync; g.flat = flat ? 1 : 0; g.gsa_out = x_gsa;
   g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_half = n_half; g.S = S;
   g.x_gsa = x_gsa; g.w_gsa = w_gsa; g.bias = raw ? nullptr : bias;
   g.k = k; g.raw = raw ? 1 : 0; g.routed_scaling = routed_scaling;
@@ -870,7 +935,7 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   cfg.dynamicSmemBytes = kFSmem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = flat ? 1 : 2;            // without clusters the tiles meet at tile_barrier
   return cuda_status(tile_rows == 112 ? cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<112>, g)
                                       : cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<128>, g));
 }

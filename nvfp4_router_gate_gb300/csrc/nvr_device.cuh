@@ -25,7 +25,7 @@ constexpr int kWsStatus = 0;
 constexpr int kWsAmaxTicket = 4;
 constexpr int kWsDecodeTicket = 8;
 constexpr int kWsAmaxChunk = 12;           // amax: next chunk to claim
-constexpr int kWsFusedAmax = 16;           // fused router's in-kernel amax: 4 words (2 maxima, arrivals, generation)
+constexpr int kWsFusedAmax = 16;           // fused router's in-kernel amax: 5 words (2 maxima, 2 arrivals, generation)
 constexpr uint32_t kStatusTimeout = 6;     // == NVR_ERR_TIMEOUT
 
 // ------------------------------------------------------------------ small PTX

@@ -18,6 +18,8 @@ constexpr int kMaxAmaxGrid = 4096;       // partial slots in the workspace
 constexpr int kMaxSplits = 256;          // N splits per M tile (bounds the workspace)
 constexpr int kMaxKmax = 16;             // largest top-k list
 constexpr int kMaxDevices = 64;
+constexpr int kMaxTicketTiles = 65536;   // token tiles of the N-split router (T <= 8,388,608)
+constexpr int kMaxFlatTiles = 1024;      // token tiles of a fused router launched without clusters
 
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
 // link-time dependency on libcuda).
@@ -55,7 +57,8 @@ struct WsLayout {
   size_t control = 0;        // 256 bytes: status word and tickets
   size_t amax_partials = 0;  // kMaxAmaxGrid x u32
   size_t scalars = 0;        // x gsa (router path), quantizer record {gsa, 1/gsa, mode, amax} -- 256 bytes
-  size_t tickets = 0;        // m_tiles x u32
+  size_t tickets = 0;        // kMaxTicketTiles x u32: the N-split router's per-tile tickets
+  size_t tile_sync = 0;      // 2 x kMaxFlatTiles u32: the fused router's tile-barrier counters (no clusters)
   size_t x_codes = 0;        // [rows_pad, D/2]
   size_t x_sf = 0;           // tile layout, rows_pad rows
   size_t partials = 0;       // N-split top-k lists, or the K-split fp32 partial logits
@@ -95,15 +98,21 @@ nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64
                               const uint8_t* W_codes, const uint8_t* W_sf, int64_t N, float* partials,
                               uint32_t* status, int S, bool test_stall, cudaStream_t s);
 // The router for bf16 activations and N <= 256 in one kernel: quantization
-// inside the K-split GEMM, partials through L2 and the epilogue (cluster of S
-// CTAs per token tile of tile_rows = 128 or 112 rows, S in {1,2,4,8,16}).
-// With amax_sync (4 zeroed
-// workspace words) the kernel also computes max|x| itself and publishes qrec
-// and x_gsa -- every CTA of the grid must then be resident at once; without
-// it, qrec and x_gsa come from the amax kernel launched before.
-// fused_cluster_capacity(S): clusters of S CTAs the device holds at once.
+// inside the K-split GEMM, partials through L2 and the epilogue (S CTAs per
+// token tile of tile_rows = 128 or 112 rows, S in {1,2,4,8,16}).  With
+// amax_sync (5 zeroed workspace words) the kernel also computes max|x| itself
+// and publishes qrec and x_gsa -- every CTA of the grid must then be resident
+// at once; without it, qrec and x_gsa come from the amax kernel launched
+// before.  tile_sync (2 x kMaxFlatTiles zeroed workspace words) comes with
+// amax_sync.  flat (needs amax_sync): the launch has no clusters and a tile's
+// CTAs meet at a workspace barrier -- the grid must then be resident at once;
+// else each tile's CTAs form a cluster.
+// fused_cluster_capacity(S): clusters of S CTAs the device holds at once;
+// fused_block_capacity(): CTAs it holds at once without clusters.
 int fused_cluster_capacity(int S);
-nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync, int64_t T, int64_t D,
+int fused_block_capacity();
+nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync,
+                               uint32_t* tile_sync, bool flat, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,

@@ -382,6 +382,48 @@ def test_prefill_one_launch_back_to_back_calls_on_one_workspace():
         assert compare.topk_ok(res), (scale, res)
 
 
+def test_prefill_plans_with_and_without_clusters():
+    """Batch sizes whose plans differ: K-split tiles whose CTAs form a cluster
+    (small grids) and, where the device holds more CTAs without clusters than
+    in whole clusters, tiles whose CTAs meet at a workspace barrier (112-row
+    tiles at T = 4096).  Every plan must route like the oracle, ragged last
+    tile included."""
+    import nvfp4_router_gate_gb300 as R
+    seen = set()
+    for T in (64, 256, 1000, 1024, 2048, 3001, 4096):
+        case = Case(WL.WORKLOADS["prefill"].with_T(T))
+        ids, w = case.run(0)
+        plan = R.last_router_plan()
+        assert plan["sequence"] in ("fused", "amax+fused"), (T, plan)
+        seen.add((plan["sequence"], plan["clustered"]))
+        rows = np.concatenate([np.arange(0, T, 41), np.arange(max(T - 20, 0), T)])
+        res = case.check(ids, w, np.unique(rows))
+        assert compare.topk_ok(res), (T, plan, res)
+    assert ("fused", True) in seen and ("fused", False) in seen, seen
+
+
+def test_prefill_mixed_plans_back_to_back_on_one_workspace():
+    """Calls of different sizes -- with and without clusters, 128- and
+    112-row tiles -- queued back to back on one workspace sized for the
+    largest: the tile barriers' counters must be left at zero by every plan
+    and never overlap another call's data."""
+    import nvfp4_router_gate_gb300 as R
+    base = WL.WORKLOADS["prefill"]
+    ws = R.new_workspace(R.router_gate_workspace_size(4096, base.D, base.N, base.k))
+    calls = []
+    for T in (4096, 64, 1024, 4096, 2048, 256, 4096):
+        case = Case(base.with_T(T))
+        ids, wts = R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, base.k,
+                                      base.routed_scaling, base.raw, workspace=ws)
+        calls.append((T, case, ids, wts, R.last_router_plan()))
+    torch.cuda.synchronize()
+    assert R.nvr_read_device_status(ws) == 0
+    for T, case, ids, wts, plan in calls:
+        rows = np.unique(np.concatenate([np.arange(0, T, 97), [T - 1]]))
+        res = case.check(ids.cpu().numpy(), wts.cpu().numpy(), rows)
+        assert compare.topk_ok(res), (T, plan, res)
+
+
 @pytest.mark.parametrize("flags", [DEC, TC])
 def test_huge_logits_saturate_without_nan(flags):
     """x scaled by 2^10: logits reach +-3e4, every sigmoid saturates to 0 or 1
