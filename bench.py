@@ -3,8 +3,9 @@
 
 One step = one router call (runtime NVFP4 quantization of the activations,
 block-scaled NVFP4 gate GEMM, sigmoid / biased top-k / renormalise / scale
-epilogue; two launches: amax, then the K-split GEMM with the quantization and
-the epilogue inside it) over one batch of the prefill workload: T = 4096 tokens,
+epilogue, all in one kernel launch: max|x|, then the K-split GEMM with the
+quantization and the epilogue inside it) over one batch of the prefill
+workload: T = 4096 tokens,
 D = 7168, E = 256 experts, k = 8, bf16 activations (per-token LogNormal scale),
 NVFP4 gate weight resident on the GPU.  Synthetic, seeded inputs.
 
@@ -255,6 +256,7 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    plan = R.last_router_plan()
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / args.steps
     value = job_throughput(world, T, args.steps, ms)
@@ -398,6 +400,7 @@ def run_gpu(args, rank, world, local_rank):
                                "routed_scaling 2.5",
                    "T": T, "D": w.D, "E": w.N, "k": w.k,
                    "l2": "inputs larger than L2: 4 rotating 58.7 MB activation buffers",
+                   "plan": plan,
                    "parallelism": "replicas" if world > 1 else "single"},
         "e2e": e2e, "gpu_launches": len(names) * args.steps, "roofline": roof, "kernels": kernels,
         "decode": decode, "cpu_baseline": cpu, "clocks": clocks,

@@ -742,6 +742,9 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * 256, xring, tmem, warp, lane,
                        static_cast<int64_t>(m_tile) * kRows, min(kRows, p.T - m_tile * kRows), p.n_half,
                        my_st > 0 && acc_ok);
+    // for the producer and MMA warps when they route too (warp 2 is done with
+    // its exact-pass queue, where the word sits)
+    if (threadIdx.x == 64) reinterpret_cast<float*>(s_fixq)[9] = gscale;
   }
 
   // The S CTAs of this token tile form the cluster, or meet at the tile's
@@ -762,30 +765,43 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   }
   tc_fence_after();
 
-  if (warp >= 2) {
-    // ------------------------------- router epilogue for this CTA's tokens
-    // rank r finishes tokens [r * 128/S, (r+1) * 128/S) of the tile; warp w
-    // takes tokens w-2, w+6, ... (up to four at once, their latencies
-    // overlapping; the A ring holds each warp's copies of its rows)
-    float4* s_row = reinterpret_cast<float4*>(aring) + (warp - 2) * 256;
-    // with 8 or more partial planes the W and x rings (contiguous, idle now)
-    // stage each warp's partial rows, all copied at once (measured: fewer
-    // planes are faster loaded directly): 16 KB per warp -- a valid slot n of
-    // a route call has 8 n < 128 / S, so its rows n * S + s stay below 16
-    float4* stage = p.S >= 8 ? reinterpret_cast<float4*>(wring) + (warp - 2) * 1024 : nullptr;
+  // ------------------------------- router epilogue for this CTA's tokens
+  // rank r finishes tokens [r * rows/S, (r+1) * rows/S) of the tile.  Router
+  // warp rw takes tokens rw, rw + nrw, ... (up to NT at once, their latencies
+  // overlapping).  Usually the eight quantizer warps route (nrw = 8); with 17
+  // to 30 tokens per CTA the producer and MMA warps join in (nrw = 10), so that
+  // three token slots per warp suffice where eight warps would need four.
+  const int per = kRows / p.S;
+  const bool ten = per > 16 && per <= 30;
+  if (warp >= 2 || ten) {
+    if (warp < 2) {
+      rt.init(p.bias, p.N, p.k, p.raw, p.routed_scaling, lane);
+      gscale = reinterpret_cast<const float*>(s_fixq)[9];
+    }
+    const int rw = warp >= 2 ? warp - 2 : warp + 8;
+    const int nrw = ten ? 10 : 8;
+    // each warp's rows: the A ring (idle now) for the quantizer warps, the x
+    // ring (idle too) for the other two
+    float4* s_row = rw < 8 ? reinterpret_cast<float4*>(aring) + rw * 256
+                           : reinterpret_cast<float4*>(xring) + (rw - 8) * 256;
+    // with 8 or more partial planes (then at most 16 tokens per CTA and eight
+    // router warps) the W and x rings (contiguous, idle now) stage each warp's
+    // partial rows, all copied at once (measured: fewer planes are faster
+    // loaded directly): 16 KB per warp -- a valid slot n of a route call has
+    // 8 n < 128 / S, so its rows n * S + s stay below 16
+    float4* stage = p.S >= 8 ? reinterpret_cast<float4*>(wring) + rw * 1024 : nullptr;
     static_assert(8 * 16384 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
-    const int per = kRows / p.S;
     const int64_t t0 = static_cast<int64_t>(m_tile) * kRows + static_cast<int64_t>(rank) * per;
-    // as many token slots per call as the warp has tokens (8, 16 or more
-    // tokens per CTA: 1, 2 or 4) -- empty slots would still be sorted
+    // as many token slots per call as the warp has tokens -- empty slots
+    // would still be sorted
     const auto route_n = [&](auto nt) {
       constexpr int NT = decltype(nt)::value;
-      for (int i = warp - 2; i < per; i += 8 * NT) {
+      for (int i = rw; i < per; i += nrw * NT) {
         int64_t tt[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const int64_t t = t0 + i + 8 * n;
-          tt[n] = (i + 8 * n < per && t < p.T) ? t : -1;
+          const int64_t t = t0 + i + nrw * n;
+          tt[n] = (i + nrw * n < per && t < p.T) ? t : -1;
         }
         rt.route<NT>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row, lane, p.out_ids, p.out_w,
                      p.logits, stage);
@@ -793,6 +809,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     };
     if (per <= 8) route_n(std::integral_constant<int, 1>());
     else if (per <= 16) route_n(std::integral_constant<int, 2>());
+    else if (ten) route_n(std::integral_constant<int, 3>());
     else route_n(std::integral_constant<int, 4>());
   }
 
