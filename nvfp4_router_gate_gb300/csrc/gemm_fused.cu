@@ -1,8 +1,9 @@
 // gemm_fused.cu -- the router for up to 256 experts on bf16 activations in one
-// launch after the amax kernel: the runtime NVFP4 quantization of x runs
-// inside a K-split tensor-core GEMM and the router epilogue runs in the same
-// kernel, so the quantized activations never exist in memory and the logits
-// only pass through L2 (sm_103a).
+// launch: max|x| over the CTAs' own x boxes and a grid barrier (or, when the
+// grid cannot be resident at once, the amax kernel launched before), then the
+// runtime NVFP4 quantization of x inside a K-split tensor-core GEMM and the
+// router epilogue in the same kernel, so the quantized activations never
+// exist in memory and the logits only pass through L2 (sm_103a).
 //
 // Source: "nvfp4-megamoe-kernel commit 04cf8ca: dsv4/layers/router.py"
 // (runtime gsa = max|x| / 2688, NVFP4 activations and gate weight, gate GEMM
@@ -609,42 +610,48 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       if (lane == 0) s_wmax[qw] = m;
       ok = bar_and(3, 256, ok);
       bool gok = true;
-      if (threadIdx.x == 64 && ok) {
+      if (warp == 2 && ok) {                           // ok is the same in every thread
         uint32_t cm = 0;
         for (int w = 0; w < 8; ++w) cm = max(cm, s_wmax[w]);
         uint32_t bits = 0;
         if (one_cluster) {
           // my maximum into slot `rank` of every CTA, then an arrival on its
-          // mbarrier (release: the store is visible first); wait for all S
+          // mbarrier (release: the store is visible first) -- lane r serves
+          // CTA r, so the S round trips overlap; then wait for all S
           uint32_t* s_cmax = reinterpret_cast<uint32_t*>(s_fixq) + 16;
-          for (int r = 0; r < p.S; ++r) {
+          if (lane < p.S) {
             uint32_t slot, bar;
-            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(slot) : "r"(smem_u32(s_cmax + rank)), "r"(r));
-            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(smem_u32(amax_mbar)), "r"(r));
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(slot) : "r"(smem_u32(s_cmax + rank)), "r"(lane));
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(smem_u32(amax_mbar)), "r"(lane));
             asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(slot), "r"(cm) : "memory");
             asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar) : "memory");
           }
-          gok = false;
-          for (uint32_t it = 0;; ++it) {
-            uint32_t done;
-            asm volatile("{\n\t.reg .pred q;\n\t"
-                         "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 q, [%1], 0;\n\t"
-                         "selp.u32 %0, 1, 0, q;\n\t}"
-                         : "=r"(done) : "r"(smem_u32(amax_mbar)) : "memory");
-            if (done) { gok = true; break; }
-            if ((it & 63) == 63 && (*abort_flag || globaltimer_ns() > deadline)) break;
+          __syncwarp();
+          if (lane == 0) {
+            gok = false;
+            for (uint32_t it = 0;; ++it) {
+              uint32_t done;
+              asm volatile("{\n\t.reg .pred q;\n\t"
+                           "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 q, [%1], 0;\n\t"
+                           "selp.u32 %0, 1, 0, q;\n\t}"
+                           : "=r"(done) : "r"(smem_u32(amax_mbar)) : "memory");
+              if (done) { gok = true; break; }
+              if ((it & 63) == 63 && (*abort_flag || globaltimer_ns() > deadline)) break;
+            }
+            for (int r = 0; r < p.S; ++r) bits = max(bits, s_cmax[r]);
           }
-          for (int r = 0; r < p.S; ++r) bits = max(bits, s_cmax[r]);
-        } else {
+        } else if (lane == 0) {
           gok = grid_amax(p.amax_sync, cm, gridDim.x, bits, deadline, abort_flag);
         }
-        s_wmax[8] = bits;
-        if (!gok) {
-          report_timeout(p.status);
-          *abort_flag = 1;
+        if (lane == 0) {
+          s_wmax[8] = bits;
+          if (!gok) {
+            report_timeout(p.status);
+            *abort_flag = 1;
+          }
         }
       }
-      ok = bar_and(3, 256, ok && gok);                 // thread 64's outcome, for every warp
+      ok = bar_and(3, 256, ok && gok);                 // warp 2's outcome, for every warp
     }
     // the quantizer record: derived here from the grid's max (the amax
     // kernel's arithmetic; CTA 0 also stores it), or the amax kernel's
