@@ -221,15 +221,34 @@ decode_router_kernel(const DecodeParams p) {
   const int grp = tid / gs, j = tid - grp * gs;
   const int e = blockIdx.x * p.epc + grp;
 
-  // 0. Prefetch this thread's weight blocks into registers (independent of x;
-  //    their latency overlaps everything up to the dot products) and stage x
-  //    in shared memory with one burst of asynchronous 16-byte copies.
-  uint2 wc[kMaxBlocksPerThread];
-  uint32_t wsb[kMaxBlocksPerThread];
   // slots i with i * gs < KB hold blocks (the bound is the same in every
   // thread, so the unrolled loops below skip the empty slots with a uniform
   // branch instead of computing on them)
   const int nb = (KB + gs - 1) / gs;
+  // The launch may overlap the previous kernel of the stream (programmatic
+  // dependent launch), which may still be writing x, W or the workspace.
+  // Until it has finished only L2 prefetches of this thread's weight blocks
+  // are issued: they return nothing to the thread, and L2 is where every
+  // write lands, so a prefetched line is never stale.
+#pragma unroll
+  for (int i = 0; i < kMaxBlocksPerThread; ++i) {
+    const int c = j + i * gs;
+    if (i >= nb) break;
+    if (e < N && c < KB) {
+      asm volatile("prefetch.global.L2 [%0];" :: "l"(p.W_codes + static_cast<size_t>(e) * (D / 2) + c * 8));
+      asm volatile("prefetch.global.L2 [%0];" :: "l"(p.W_sf + sf_tile_offset(e, c, KB)));
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel of the stream may launch now; it waits for this grid to
+  // complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // 0. Load this thread's weight blocks into registers (independent of x;
+  //    their latency overlaps everything up to the dot products) and stage x
+  //    in shared memory with one burst of asynchronous 16-byte copies.
+  uint2 wc[kMaxBlocksPerThread];
+  uint32_t wsb[kMaxBlocksPerThread];
 #pragma unroll
   for (int i = 0; i < kMaxBlocksPerThread; ++i) {
     const int c = j + i * gs;
@@ -568,22 +587,23 @@ static cudaError_t launch_t(const DecodeParams& p, const DecodePlan& plan, cudaS
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  if (plan.cluster <= 1) {
-    decode_router_kernel<kBF16><<<plan.grid, kDecodeThreads, plan.smem, s>>>(p);
-    return cudaGetLastError();
-  }
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = plan.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch (the kernel waits for its predecessor
+  // before it reads anything but L2 prefetches), and for several tokens the
+  // cluster
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = plan.cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3(kDecodeThreads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = plan.cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, decode_router_kernel<kBF16>, p);
 }
 
