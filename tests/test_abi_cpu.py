@@ -132,6 +132,29 @@ def test_host_argument_checks_without_gpu():
     assert L.router_gate_logits(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, nat.NVR_FLAG_RAW_LOGITS,
                                 fake, fake, ws_n, None) == nat.NVR_ERR_INVALID_ARG
     assert L.nvr_read_device_status(None, None, None) == nat.NVR_ERR_INVALID_ARG
+    # plan query: NULL rejected; otherwise a kernel sequence code 0-5 (0 on a
+    # thread that has not launched a router call)
+    assert L.nvr_last_router_plan(None) == nat.NVR_ERR_INVALID_ARG
+    plan = (ctypes.c_int * 4)()
+    assert L.nvr_last_router_plan(plan) == nat.NVR_OK
+    assert 0 <= plan[0] <= 5 and plan[3] in (0, 1)
+
+
+def test_workspace_counters_do_not_move_with_T():
+    """Calls of any size share a workspace sized for the largest: the bound
+    grows with T_max by the data regions only, never shrinking below what a
+    smaller call needs, and covers the fixed counter regions (65 536 N-split
+    tickets and two sets of 1024 tile-barrier counters) even for one token."""
+    nat = _lib()
+    L = nat.lib()
+    small = L.router_gate_workspace_size(1, 256, 16, 1)
+    assert small >= 65536 * 4 + 2 * 1024 * 4
+    for N in (16, 256, 384):
+        prev = 0
+        for T in (1, 15, 16, 17, 112, 113, 4096, 4097):
+            v = L.router_gate_workspace_size(T, 7168, N, 8)
+            assert v >= prev, (N, T)
+            prev = v
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
