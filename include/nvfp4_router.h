@@ -234,11 +234,13 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k);
  *     that share the staging and quantization of x through distributed
  *     shared memory.
  *   - bf16 x, N <= 256: one kernel that takes max|x| itself (a bounded grid
- *     barrier, or a cluster barrier when the grid is one cluster), quantizes
- *     x inside the K-split GEMM and routes each tile's tokens from the fp32
- *     partial logits (L2-resident workspace).  When the grid cannot be
- *     resident at once (a forced split on a large T), an amax kernel runs
- *     first and the same kernel skips its own max|x| pass.
+ *     barrier in the workspace, or an exchange through distributed shared
+ *     memory when the grid is one cluster), quantizes x inside the K-split
+ *     GEMM and routes each tile's tokens from the fp32 partial logits
+ *     (L2-resident workspace) after the tile's CTAs have met at a cluster
+ *     barrier or, launched without clusters, at a workspace barrier.  When
+ *     the grid cannot be resident at once (a forced split on a large T), an
+ *     amax kernel runs first and the same kernel skips its own max|x| pass.
  *   - fp32 x, N <= 256: amax, quantize, K-split GEMM and a warp-per-token
  *     epilogue kernel.
  *   - N > 256: amax, quantize and the N-split GEMM, which routes from the
