@@ -144,6 +144,21 @@ const char* nvr_last_cuda_error(void);
  * NVR_ERR_INVALID_ARG for a NULL out. */
 nvr_status nvr_last_router_plan(int* out);
 
+/* nvr_plan_router -- the launch plan router_gate_topk would choose for a call
+ * of T >= 1 tokens (dtype dt, hidden D, N experts, flags as for
+ * router_gate_topk) on a device with num_sms SMs that holds
+ * cluster_capacity[i] clusters of 2^i CTAs of the fused router kernel at once
+ * (i = 0..4, five ints) and block_capacity of its CTAs without clusters.  Host
+ * arithmetic only (no device access): the dispatch runs the same function
+ * with the current device's capacities.  out: the four ints described at
+ * nvr_last_router_plan.  NVR_ERR_INVALID_ARG for NULL pointers, a shape or
+ * flags router_gate_topk would reject, num_sms < 1; NVR_ERR_UNSUPPORTED where
+ * router_gate_topk would return it for the shape (a forced decode that does
+ * not fit, a forced K split with N > 256).  No counterpart on the pages: a
+ * diagnostic for capacity planning and tests. */
+nvr_status nvr_plan_router(int64_t T, int64_t D, int64_t N, nvr_dtype dt, uint32_t flags, int num_sms,
+                           const int* cluster_capacity, int block_capacity, int* out);
+
 /* Bytes of a scale-byte buffer for [rows, D] in the given layout
  * (0 for invalid arguments). */
 size_t nvr_sf_bytes(int64_t rows, int64_t D, nvr_sf_layout layout);

@@ -29,7 +29,7 @@ from ._native import (NVR_FLAG_FORCE_DECODE, NVR_FLAG_FORCE_TENSOR_CORE, NVR_FLA
 
 __all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits",
            "router_gate_workspace_size", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
-           "nvr_read_device_status", "last_router_plan", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
+           "nvr_read_device_status", "last_router_plan", "plan_router", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
            "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "NVR_FLAG_SPLIT_K_2",
            "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "new_workspace"]
 
@@ -163,6 +163,20 @@ def last_router_plan():
     cluster."""
     out = (ctypes.c_int * 4)()
     _native.check("nvr_last_router_plan", _native.lib().nvr_last_router_plan(out))
+    return {"sequence": _PLAN_SEQUENCES.get(out[0], str(out[0])), "tile_rows": out[1],
+            "ctas_per_tile": out[2], "clustered": bool(out[3])}
+
+
+def plan_router(T, D, N, *, num_sms, cluster_capacity, block_capacity, dtype="bf16", flags=0):
+    """The launch plan a router call of this shape would get on a device with
+    num_sms SMs holding cluster_capacity[i] clusters of 2**i CTAs of the fused
+    kernel (five ints) and block_capacity of its CTAs without clusters (host
+    arithmetic only), in the form of last_router_plan."""
+    caps = (ctypes.c_int * 5)(*[int(c) for c in cluster_capacity])
+    out = (ctypes.c_int * 4)()
+    code = _native.NVR_BF16 if dtype == "bf16" else _native.NVR_F32
+    _native.check("nvr_plan_router", _native.lib().nvr_plan_router(
+        int(T), int(D), int(N), code, int(flags), int(num_sms), caps, int(block_capacity), out))
     return {"sequence": _PLAN_SEQUENCES.get(out[0], str(out[0])), "tile_rows": out[1],
             "ctas_per_tile": out[2], "clustered": bool(out[3])}
 

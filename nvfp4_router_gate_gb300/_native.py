@@ -44,6 +44,8 @@ SIGNATURES = {
     "nvr_status_string": (ctypes.c_char_p, [_i32]),
     "nvr_last_cuda_error": (ctypes.c_char_p, []),
     "nvr_last_router_plan": (_i32, [ctypes.POINTER(_i32)]),
+    "nvr_plan_router": (_i32, [_i64, _i64, _i64, _i32, _u32, _i32, ctypes.POINTER(_i32), _i32,
+                               ctypes.POINTER(_i32)]),
     "nvr_sf_bytes": (_sz, [_i64, _i64, _i32]),
     "nvfp4_quantize_workspace_size": (_sz, [_i64, _i64]),
     "nvfp4_quantize_act": (_i32, [_p, _i32, _i64, _i64, _p, _p, _i32, _p, _p, _sz, _p]),

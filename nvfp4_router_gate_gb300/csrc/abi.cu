@@ -174,15 +174,11 @@ nvr_status quantize_impl(const void* x, nvr_dtype dt, int64_t rows, int64_t D, u
   return cuda_status(e);
 }
 
-nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
-                       const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias, int k,
-                       float routed_scaling, uint32_t flags, int32_t* out_ids, float* out_w,
-                       float* logits, void* ws, size_t ws_bytes, cudaStream_t s) {
-  nvr_status st = check_common(x, dt, T, D, ws);
-  if (st != NVR_OK) return st;
-  if (!W_fp4 || !W_sf || !w_gsa || N <= 0 || N > (1 << 28)) return NVR_ERR_INVALID_ARG;
-  if (!logits && (!out_ids || !out_w || k < 1 || k > kMaxKmax || k > N)) return NVR_ERR_INVALID_ARG;
-  constexpr uint32_t kKernelFlags = NVR_FLAG_SPLIT_K_2 | NVR_FLAG_SPLIT_K_4 | NVR_FLAG_SPLIT_K_8 | NVR_FLAG_SPLIT_N;
+constexpr uint32_t kKernelFlags = NVR_FLAG_SPLIT_K_2 | NVR_FLAG_SPLIT_K_4 | NVR_FLAG_SPLIT_K_8 | NVR_FLAG_SPLIT_N;
+
+// Checks the router flags and folds a kernel-choice flag into
+// FORCE_TENSOR_CORE; NVR_ERR_INVALID_ARG for unknown or conflicting flags.
+nvr_status normalize_flags(uint32_t& flags) {
   if (flags & ~static_cast<uint32_t>(NVR_FLAG_RAW_LOGITS | NVR_FLAG_FORCE_TENSOR_CORE | NVR_FLAG_FORCE_DECODE |
                                      kKernelFlags | NVR_FLAG_TEST_STALL))
     return NVR_ERR_INVALID_ARG;
@@ -191,9 +187,112 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   if (kernel_flags) flags |= NVR_FLAG_FORCE_TENSOR_CORE;
   if ((flags & NVR_FLAG_FORCE_TENSOR_CORE) && (flags & NVR_FLAG_FORCE_DECODE)) return NVR_ERR_INVALID_ARG;
   if ((flags & NVR_FLAG_TEST_STALL) && !(flags & NVR_FLAG_FORCE_TENSOR_CORE)) return NVR_ERR_INVALID_ARG;
+  return NVR_OK;
+}
+
+// The launch plan of a router call (the sequence codes of nvr_last_router_plan).
+struct RouterPlan {
+  int seq = 0;                 // 1 decode, 2 fused, 3 amax + fused, 4 amax + quantize + K split + epilogue,
+                               // 5 amax + quantize + N split
+  int tile_rows = 0, per_tile = 0;
+  bool clustered = false;      // seq 1: decode clusters; seq 2-3: the tile's CTAs form a cluster
+  DecodePlan dp;               // seq 1
+  GemmPlan g;                  // seq 5
+};
+
+// The plan for T > 0 tokens on a device with `sms` SMs that holds
+// cluster_cap[i] clusters of 2^i CTAs of the fused kernel at once (i = 0..4)
+// and block_cap of its CTAs without clusters.  Host arithmetic only: the
+// dispatch and nvr_plan_router both call it.  flags: normalised.
+//
+// The fused kernel (bf16, <= 256 experts): token tiles of 128 or 112 rows,
+// S CTAs per tile (S a power of two no larger than the K-split plan; each CTA
+// routes rows/S tokens) that form a cluster or, without clusters, meet at a
+// barrier in the workspace.  Among the grids resident at once the one with
+// the least work per CTA (rows x K stages per CTA) wins, clusters on a tie;
+// the device holds fewer CTAs in clusters than without (whole clusters per
+// GPC), so at T = 4096 112-row tiles put 148 CTAs on the SMs without clusters
+// where clusters of 4 hold 128.  Forced split factors keep 128-row tiles.
+// With no resident grid: clusters, after the amax kernel.
+nvr_status plan_router(int64_t T, int64_t D, int64_t N, bool bf16, uint32_t flags, int sms,
+                       const int (&cluster_cap)[5], int block_cap, RouterPlan& rp) {
   const int forced_split = (flags & NVR_FLAG_SPLIT_K_2) ? 2 : (flags & NVR_FLAG_SPLIT_K_4) ? 4
                            : (flags & NVR_FLAG_SPLIT_K_8) ? 8 : 0;
   if (forced_split && N > 256) return NVR_ERR_UNSUPPORTED;
+  rp.dp = plan_decode(T, D, N, sms, bf16);
+  const bool use_decode = (flags & NVR_FLAG_FORCE_DECODE) ? true
+                          : (flags & NVR_FLAG_FORCE_TENSOR_CORE) ? false
+                          : rp.dp.ok;
+  if (use_decode) {
+    if (!rp.dp.ok) return NVR_ERR_UNSUPPORTED;
+    rp.seq = 1;
+    rp.clustered = rp.dp.cluster > 1;
+    return NVR_OK;
+  }
+  // Up to 256 experts: K split over S CTAs with one tensor-core accumulator
+  // for the whole row each; bf16 activations are quantized inside the GEMM
+  // and routed in the same kernel, fp32 ones take the standalone quantizer,
+  // the K-split GEMM and the epilogue kernel.  Wider heads: N tiles split
+  // across CTAs with a top-k merge, after the standalone quantize kernel.
+  const int split_k = forced_split                        ? forced_split
+                      : (flags & NVR_FLAG_SPLIT_N) || N > 256 ? 0
+                                                              : plan_splitk(T, D, sms);
+  if (split_k > 0 && bf16) {
+    const int n_st = static_cast<int>((D / kBlock + 15) / 16);
+    int tile_rows = 128, S = 1;
+    bool one_launch = false, flat = false;
+    int64_t best = -1;
+    for (int rows : {128, 112}) {
+      if (forced_split && rows != 128) continue;
+      const int64_t m_tiles = (T + rows - 1) / rows;
+      for (int c = 16, ci = 4; c >= 1; c >>= 1, --ci) {
+        if (forced_split ? c != forced_split : c > split_k) continue;
+        const int64_t cost = static_cast<int64_t>(rows) * ((n_st + c - 1) / c);
+        for (int f = 0; f < (c > 1 ? 2 : 1); ++f) {
+          const bool resident = f ? m_tiles * c <= block_cap && m_tiles <= kMaxFlatTiles
+                                  : cluster_cap[ci] >= m_tiles;
+          if (f && !resident) continue;
+          if (best < 0 || (resident && !one_launch) || (resident == one_launch && cost < best)) {
+            best = cost;
+            tile_rows = rows;
+            S = c;
+            flat = f != 0;
+            one_launch = resident;
+          }
+        }
+      }
+    }
+    rp.seq = one_launch ? 2 : 3;
+    rp.tile_rows = tile_rows;
+    rp.per_tile = S;
+    rp.clustered = !flat;
+    return NVR_OK;
+  }
+  if (split_k > 0) {
+    rp.seq = 4;
+    rp.tile_rows = 128;
+    rp.per_tile = split_k;
+    return NVR_OK;
+  }
+  rp.g = plan_gemm(T, N, sms);
+  if (rp.g.m_tiles > kMaxTicketTiles) return NVR_ERR_UNSUPPORTED;
+  rp.seq = 5;
+  rp.tile_rows = 128;
+  rp.per_tile = rp.g.n_splits;
+  return NVR_OK;
+}
+
+nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
+                       const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias, int k,
+                       float routed_scaling, uint32_t flags, int32_t* out_ids, float* out_w,
+                       float* logits, void* ws, size_t ws_bytes, cudaStream_t s) {
+  nvr_status st = check_common(x, dt, T, D, ws);
+  if (st != NVR_OK) return st;
+  if (!W_fp4 || !W_sf || !w_gsa || N <= 0 || N > (1 << 28)) return NVR_ERR_INVALID_ARG;
+  if (!logits && (!out_ids || !out_w || k < 1 || k > kMaxKmax || k > N)) return NVR_ERR_INVALID_ARG;
+  st = normalize_flags(flags);
+  if (st != NVR_OK) return st;
+  if ((flags & kKernelFlags & ~static_cast<uint32_t>(NVR_FLAG_SPLIT_N)) && N > 256) return NVR_ERR_UNSUPPORTED;
   if (!aligned16(W_fp4) || !aligned16(W_sf) || (reinterpret_cast<uintptr_t>(w_gsa) & 3u) ||
       (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
       (out_ids && (reinterpret_cast<uintptr_t>(out_ids) & 3u)) ||
@@ -211,20 +310,29 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   const bool raw = (flags & NVR_FLAG_RAW_LOGITS) != 0;
   if (logits) k = 1;
 
-  const DecodePlan dp = plan_decode(T, D, N, sms, bf16);
-  const bool use_decode = (flags & NVR_FLAG_FORCE_DECODE) ? true
-                          : (flags & NVR_FLAG_FORCE_TENSOR_CORE) ? false
-                          : dp.ok;
-  if (use_decode) {
-    if (!dp.ok) return NVR_ERR_UNSUPPORTED;
+  // the fused kernel's capacities, queried (once per device) only where it
+  // may run -- never for a decode call, which may be the first call of a
+  // process and inside a graph capture
+  const bool maybe_fused = bf16 && N <= 256 && !(flags & (NVR_FLAG_SPLIT_N | NVR_FLAG_FORCE_DECODE)) &&
+                           ((flags & NVR_FLAG_FORCE_TENSOR_CORE) || !plan_decode(T, D, N, sms, bf16).ok);
+  int cluster_cap[5] = {0, 0, 0, 0, 0};
+  int block_cap = 0;
+  if (maybe_fused) {
+    for (int i = 0; i < 5; ++i) cluster_cap[i] = fused_cluster_capacity(1 << i);
+    block_cap = fused_block_capacity();
+  }
+  RouterPlan rp;
+  st = plan_router(T, D, N, bf16, flags, sms, cluster_cap, block_cap, rp);
+  if (st != NVR_OK) return st;
+  record_plan(rp.seq, rp.tile_rows, rp.per_tile, rp.clustered);
+  if (rp.seq == 1) {
     float* keys = reinterpret_cast<float*>(w + L.decode);
     float* scores = keys + T * N;
-    record_plan(1, 0, 0, dp.cluster > 1);
     ProfileScope prof(s);
     prof.before();
     cudaError_t e = launch_decode(x, bf16, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
                                   out_ids, out_w, logits, keys, scores,
-                                  reinterpret_cast<uint32_t*>(w + kWsDecodeTicket), dp, s);
+                                  reinterpret_cast<uint32_t*>(w + kWsDecodeTicket), rp.dp, s);
     prof.after();
     return cuda_status(e);
   }
@@ -235,51 +343,9 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   uint32_t* status = reinterpret_cast<uint32_t*>(w + kWsStatus);
   const bool stall = (flags & NVR_FLAG_TEST_STALL) != 0;
   ProfileScope prof(s);
-  // Up to 256 experts: K split over S CTAs with one tensor-core accumulator
-  // for the whole row each; bf16 activations are quantized inside the GEMM
-  // and routed in the same kernel, fp32 ones take the standalone quantizer,
-  // the K-split GEMM and the epilogue kernel.  Wider heads: N tiles split
-  // across CTAs with a top-k merge, after the standalone quantize kernel.
-  const int split_k = forced_split                        ? forced_split
-                      : (flags & NVR_FLAG_SPLIT_N) || N > 256 ? 0
-                                                              : plan_splitk(T, D, sms);
   float* partials = reinterpret_cast<float*>(w + L.partials);
-  if (split_k > 0 && bf16) {
-    // Token tiles of 128 or 112 rows, S CTAs per tile (S a power of two no
-    // larger than the plan; each CTA routes rows/S tokens) that form a cluster
-    // or, without clusters, meet at a barrier in the workspace.  Among the
-    // grids resident at once the one with the least work per CTA (rows x K
-    // stages per CTA) wins, clusters on a tie; the device holds fewer CTAs in
-    // clusters than without (whole clusters per GPC), so at T = 4096 112-row
-    // tiles put 148 CTAs on the SMs without clusters where clusters of 4 hold
-    // 128.  Forced split factors keep 128-row tiles.  With no resident grid:
-    // clusters, after the amax kernel.
-    const int n_st = static_cast<int>((D / kBlock + 15) / 16);
-    const int block_cap = fused_block_capacity();
-    int tile_rows = 128, S = 1;
-    bool one_launch = false, flat = false;
-    int64_t best = -1;
-    for (int rows : {128, 112}) {
-      if (forced_split && rows != 128) continue;
-      const int64_t m_tiles = (T + rows - 1) / rows;
-      for (int c = 16; c >= 1; c >>= 1) {
-        if (forced_split ? c != forced_split : c > split_k) continue;
-        const int64_t cost = static_cast<int64_t>(rows) * ((n_st + c - 1) / c);
-        for (int f = 0; f < (c > 1 ? 2 : 1); ++f) {
-          const bool resident = f ? m_tiles * c <= block_cap && m_tiles <= kMaxFlatTiles
-                                  : fused_cluster_capacity(c) >= m_tiles;
-          if (f && !resident) continue;
-          if (best < 0 || (resident && !one_launch) || (resident == one_launch && cost < best)) {
-            best = cost;
-            tile_rows = rows;
-            S = c;
-            flat = f != 0;
-            one_launch = resident;
-          }
-        }
-      }
-    }
-    record_plan(one_launch ? 2 : 3, tile_rows, S, !flat);
+  if (rp.seq == 2 || rp.seq == 3) {
+    const bool one_launch = rp.seq == 2, flat = !rp.clustered;
     if (!one_launch) {
       prof.before();
       const cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
@@ -293,14 +359,11 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
                              one_launch ? reinterpret_cast<uint32_t*>(w + kWsFusedAmax) : nullptr,
                              one_launch ? reinterpret_cast<uint32_t*>(w + L.tile_sync) : nullptr, flat, T, D, W_fp4,
                              W_sf, w_gsa, N, bias, k, routed_scaling, raw, out_ids, out_w, logits, partials, status,
-                             S, tile_rows, stall, s);
+                             rp.per_tile, rp.tile_rows, stall, s);
     prof.after();
     return st;
   }
-  const GemmPlan g = plan_gemm(T, N, sms);
-  if (split_k == 0 && g.m_tiles > kMaxTicketTiles) return NVR_ERR_UNSUPPORTED;
-  if (split_k > 0) record_plan(4, 128, split_k, false);
-  else record_plan(5, 128, g.n_splits, false);
+  const int split_k = rp.seq == 4 ? rp.per_tile : 0;
   prof.before();
   cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + L.amax_partials),
                                    reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec, status, sms, s);
@@ -324,7 +387,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   prof.before();
   st = launch_gemm_topk(xc, xsf, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
                         out_ids, out_w, logits, reinterpret_cast<float4*>(w + L.partials),
-                        reinterpret_cast<uint32_t*>(w + L.tickets), status, g, stall, s);
+                        reinterpret_cast<uint32_t*>(w + L.tickets), status, rp.g, stall, s);
   prof.after();
   return st;
 }
@@ -334,6 +397,26 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
 extern "C" {
 
 const char* nvr_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
+
+nvr_status nvr_plan_router(int64_t T, int64_t D, int64_t N, nvr_dtype dt, uint32_t flags, int num_sms,
+                           const int* cluster_capacity, int block_capacity, int* out) {
+  if (!cluster_capacity || !out) return NVR_ERR_INVALID_ARG;
+  if (T < 1 || D <= 0 || D % 64 != 0 || D > (1 << 24) || N <= 0 || N > (1 << 28)) return NVR_ERR_INVALID_ARG;
+  if (dt != NVR_BF16 && dt != NVR_F32) return NVR_ERR_INVALID_ARG;
+  if (num_sms < 1 || block_capacity < 0) return NVR_ERR_INVALID_ARG;
+  nvr_status st = normalize_flags(flags);
+  if (st != NVR_OK) return st;
+  int caps[5];
+  for (int i = 0; i < 5; ++i) caps[i] = cluster_capacity[i];
+  RouterPlan rp;
+  st = plan_router(T, D, N, dt == NVR_BF16, flags, num_sms, caps, block_capacity, rp);
+  if (st != NVR_OK) return st;
+  out[0] = rp.seq;
+  out[1] = rp.tile_rows;
+  out[2] = rp.per_tile;
+  out[3] = rp.clustered ? 1 : 0;
+  return NVR_OK;
+}
 
 nvr_status nvr_last_router_plan(int* out) {
   if (!out) return NVR_ERR_INVALID_ARG;
