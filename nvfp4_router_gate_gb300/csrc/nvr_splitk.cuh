@@ -64,9 +64,10 @@ __device__ __forceinline__ void store_partial_tile(const CUtensorMap* tmap_p, ui
 }
 
 // The same tile with ordinary stores, for a reader in another CTA of the
-// cluster (a cluster barrier then makes them visible): each 32 x 32 block goes
-// through the warp's 4 KB staging buffer at stg_base + (warp-2) * 4 KB (128-byte
-// swizzle, conflict-free both ways) and leaves as 512-byte coalesced rows.
+// same kernel (the tile's cluster or workspace barrier that follows makes them
+// visible): each 32 x 32 block goes through the warp's 4 KB staging buffer at
+// stg_base + (warp-2) * 4 KB (128-byte swizzle, conflict-free both ways) and
+// leaves as 512-byte coalesced rows.
 __device__ __forceinline__ void store_partial_rows(float* plane, uint8_t* stg_base, uint32_t tmem, int warp,
                                                    int lane, int64_t row0, int rows, int n_half, bool have_acc) {
   const int q = warp & 3, h = (warp - 2) >> 2;
