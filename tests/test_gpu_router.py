@@ -210,6 +210,31 @@ def test_determinism_and_graph_replay():
         assert R.nvr_read_device_status(gate.workspace) == 0
 
 
+def test_steady_state_calls_neither_sync_nor_allocate():
+    """A resident router's calls make no synchronising torch call (the sync
+    debug mode raises on one) and allocate nothing (the caching allocator's
+    count stays put over many calls): nothing hidden between the host and a
+    CUDA graph, decode and prefill alike."""
+    import nvfp4_router_gate_gb300 as R
+    for T in (1, 300):
+        w = WL.WORKLOADS["decode"].with_T(T) if T == 1 else WL.WORKLOADS["prefill"].with_T(T)
+        gate = R.RouterGate(to_device(WL.make_w(w), w.dtype), torch.from_numpy(WL.make_bias(w)).cuda(),
+                            k=8, routed_scaling=2.5, max_tokens=T)
+        x = to_device(WL.make_x(w), w.dtype)
+        gate(x)
+        torch.cuda.synchronize()
+        before = torch.cuda.memory_allocated()
+        torch.cuda.set_sync_debug_mode("error")
+        try:
+            for _ in range(200):
+                gate(x)
+        finally:
+            torch.cuda.set_sync_debug_mode("default")
+        torch.cuda.synchronize()
+        assert torch.cuda.memory_allocated() == before
+        assert R.nvr_read_device_status(gate.workspace) == 0
+
+
 def test_workspace_reuse_across_shapes():
     import nvfp4_router_gate_gb300 as R
     w = WL.WORKLOADS["prefill"]
