@@ -30,7 +30,7 @@ are closer than the logit tolerance allows to separate; routing weights within
 
 import numpy as np
 
-from .router import sigmoid64, routed_weights, selection_keys
+from .router import sigmoid64, routed_weights, selection_keys, topk_order
 
 LOGIT_REL = 1e-3
 LOGIT_ABS_FRAC = 2.0 ** -15
@@ -135,6 +135,30 @@ def topk_ok(res):
     return all(v == 0 for kk, v in res.items() if kk != "exempt_rows")
 
 
+def candidate_summary(L64, bound64, bias=None, raw=True, top=64):
+    """What a head too wide to keep every logit stores per row for
+    ``check_topk_candidates``: the ``top`` best outputs by the oracle's float32
+    key (ids in oracle order, their float64 logits and bounds) and, over every
+    other output, the largest key - slack (``rest_max``; -inf when there is
+    none).  Returns (ids int32 [T, top], logits [T, top], bounds [T, top],
+    rest_max [T])."""
+    L64 = np.asarray(L64, dtype=np.float64)
+    bound64 = np.asarray(bound64, dtype=np.float64)
+    T, N = L64.shape
+    top = min(top, N)
+    keys = selection_keys(L64, bias, raw)
+    tau = key_slack(L64, bound64, keys, bias, raw)
+    ids = topk_order(keys, top)
+    rest = np.full(T, -np.inf)
+    for t in range(T):
+        mask = np.ones(N, bool)
+        mask[ids[t]] = False
+        if mask.any():
+            rest[t] = np.max(keys[t][mask].astype(np.float64) - tau[t][mask])
+    return (ids.astype(np.int32), np.take_along_axis(L64, ids.astype(np.int64), 1),
+            np.take_along_axis(bound64, ids.astype(np.int64), 1), rest)
+
+
 def check_topk_candidates(gpu_ids, gpu_w, cand_ids, cand_L, cand_B, rest_max, raw=True,
                           bias=None, routed_scaling=1.0):
     """``check_topk`` for a head too wide to keep every logit: the oracle keeps,
@@ -158,11 +182,13 @@ def check_topk_candidates(gpu_ids, gpu_w, cand_ids, cand_L, cand_B, rest_max, ra
         idx = np.array([pos[int(e)] for e in g])
         L = np.asarray(cand_L[t], np.float64)[None, :]
         B = np.asarray(cand_B[t], np.float64)[None, :]
-        keys = selection_keys(L, bias, raw)
-        # the candidate list plus one stand-in for everything else
-        sub = check_topk(idx[None, :], np.asarray(gpu_w[t:t + 1]), L, B, keys, bias,
+        bc = None if bias is None else np.asarray(bias, np.float32)[cid]   # the candidates' bias
+        keys = selection_keys(L, bc, raw)
+        # the candidate list (stored in oracle order: among equal keys a lower
+        # position is a lower id) plus one stand-in for everything else
+        sub = check_topk(idx[None, :], np.asarray(gpu_w[t:t + 1]), L, B, keys, bc,
                          routed_scaling, raw)
-        tau = key_slack(L, B, keys, bias, raw)[0]
+        tau = key_slack(L, B, keys, bc, raw)[0]
         hi = keys[0][idx].astype(np.float64) + tau[idx]
         if rest_max[t] > hi.min():
             sub["bad_set"] += 1
