@@ -14,11 +14,15 @@ steps (inputs resident in HBM, four rotating 58.7 MB activation buffers so no
 step reads its input from L2), plus
   e2e           the same call with the batch copied from pinned host memory and
                 the ids/weights copied back inside every timed step;
-  roofline      the dominant kernel's algorithmic bytes (or flops) per launch /
-                its mean CUDA-event duration in a second pass with per-kernel
-                events, against MEASURED_PEAKS.json;
+  roofline      the dominant kernel's algorithmic bytes per launch / its mean
+                duration over the timed region (one launch per step), against
+                MEASURED_PEAKS.json; the event-bracketed duration of a second
+                pass with events around every launch is reported beside it;
   kernels       every kernel of the step, the same way;
   decode        the decode router (T = 1, 8, 64) as CUDA-graph replays;
+  other_rooflines  the wide-N raw head (k = 8 and 1), the adversarial large
+                batch (tokens/s), the standalone quantizer and the decode
+                kernel's own duration, each against the measured HBM copy rate;
   cpu_baseline  the CPU oracle on a bounded sample of the same batch;
   clocks        SM clocks and throttle reasons sampled during the timed region.
 
@@ -301,7 +305,20 @@ def run_gpu(args, rank, world, local_rank):
         ent["traffic"] = traffic.get(n)
         kernels[n] = ent
     dom = max(names, key=lambda n: kernels[n]["ms"])
-    roof = {k: kernels[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    if len(names) == 1:
+        # one launch per step: its average duration over the timed region is
+        # the step time (events between launches, as in the per-kernel pass,
+        # remove the overlap of one launch's tail with the next one's start)
+        b, _ = algorithmic(w, T, dom)
+        ach = b / (ms_per_step / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": kernels[dom]["traffic"], "bytes_per_launch": b, "ms_per_launch": ms_per_step,
+                "duration_source": "timed region / steps (one launch per step)",
+                "event_bracketed_ms": kernels[dom]["ms"],
+                "event_bracketed_frac": kernels[dom]["frac"]}
+    else:
+        roof = {k: kernels[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+        roof["duration_source"] = "per-kernel CUDA events"
     roof["kernel"] = dom
     roof["peak_source"] = peak_kind
 
@@ -380,6 +397,8 @@ def run_gpu(args, rank, world, local_rank):
         decode["launches_T1"] = 1
         decode["graph"] = "per call: 16 calls captured in one CUDA graph (the layers of a decode step)"
 
+    extra = {} if args.skip_extra else extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic)
+
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
         from oracle import pipeline
@@ -403,8 +422,131 @@ def run_gpu(args, rank, world, local_rank):
                    "plan": plan,
                    "parallelism": "replicas" if world > 1 else "single"},
         "e2e": e2e, "gpu_launches": len(names) * args.steps, "roofline": roof, "kernels": kernels,
-        "decode": decode, "cpu_baseline": cpu, "clocks": clocks,
+        "decode": decode, "other_rooflines": extra, "cpu_baseline": cpu, "clocks": clocks,
     }
+
+
+def _timed_calls(fn, n, stream, warm=3):
+    """Mean ms per call of `n` back-to-back calls (CUDA events around them all)."""
+    import torch
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def _hbm_entry(nbytes, ms, hbm, traffic=None, **kw):
+    ach = nbytes / (ms / 1e3) / 1e9
+    ent = {"bound": "hbm", "bytes_per_call": int(nbytes), "ms_per_call": ms, "achieved": ach, "peak": hbm,
+           "unit": "GB/s", "frac": ach / hbm, "traffic": traffic}
+    ent.update(kw)
+    return ent
+
+
+def extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic):
+    """Rooflines of the other configurations and kernels, each timed over
+    back-to-back calls with CUDA events on the launching stream:
+      wide_n       the N = 129280 raw head (T = 32, k = 8 and k = 1): weight
+                   streaming, 0.52 GB per call (> L2: every call reads it from HBM);
+      adversarial  the T = 16384, E = 384 batch (x 235 MB > L2): tokens/s too;
+      quantize     nvfp4_quantize_act on the prefill batch (x read once, codes
+                   and scales written), four rotating inputs;
+      decode_kernel the decode router's own device duration at T = 1 (events
+                   around every launch, so no overlap with its neighbours)."""
+    import torch
+    from nvfp4_router_gate_gb300 import _native
+    out = {}
+    g = torch.Generator(device=dev)
+    g.manual_seed(WL.SEED)
+
+    # wide-N raw head: synthetic bf16 weight of the workload's distribution,
+    # drawn on the device (0.93 G elements)
+    wn = WL.WORKLOADS["wide_n"]
+    W = (torch.randn((wn.N, wn.D), generator=g, device=dev, dtype=torch.float32) * wn.w_std).to(torch.bfloat16)
+    W_fp4, W_sf, w_gsa = R.nvfp4_pack_weight(W)
+    del W
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    x = torch.randn((wn.T, wn.D), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    wbytes = wn.N * (wn.D // 2 + wn.D // 16)
+    for k in (8, 1):
+        ws = R.new_workspace(R.router_gate_workspace_size(wn.T, wn.D, wn.N, k), dev)
+        ids = torch.empty((wn.T, k), dtype=torch.int32, device=dev)
+        wt = torch.empty((wn.T, k), dtype=torch.float32, device=dev)
+        ms = _timed_calls(lambda i: R.router_gate_topk(x, W_fp4, W_sf, w_gsa, None, k, 1.0, True, out_ids=ids,
+                                                       out_w=wt, workspace=ws), 50, stream)
+        nbytes = wbytes + wn.T * wn.D * 2 + wn.T * k * 8
+        out["wide_n_k%d" % k] = _hbm_entry(nbytes, ms, hbm, plan=R.last_router_plan(),
+                                           tensor_tflops=2 * wn.T * wn.D * wn.N / (ms / 1e3) / 1e12)
+    del W_fp4, W_sf
+    torch.cuda.empty_cache()
+
+    # adversarial large batch
+    aw = WL.WORKLOADS["adversarial"]
+    xa = torch.from_numpy(WL.make_x(aw).view(np.int16)).view(torch.bfloat16).to(dev)
+    Wa = torch.from_numpy(WL.make_w(aw).view(np.int16)).view(torch.bfloat16).to(dev)
+    Wf, Wsf, wg = R.nvfp4_pack_weight(Wa)
+    bias = torch.from_numpy(WL.make_bias(aw)).to(dev)
+    ws = R.new_workspace(R.router_gate_workspace_size(aw.T, aw.D, aw.N, aw.k), dev)
+    ids = torch.empty((aw.T, aw.k), dtype=torch.int32, device=dev)
+    wt = torch.empty((aw.T, aw.k), dtype=torch.float32, device=dev)
+    ms = _timed_calls(lambda i: R.router_gate_topk(xa, Wf, Wsf, wg, bias, aw.k, aw.routed_scaling, out_ids=ids,
+                                                   out_w=wt, workspace=ws), 50, stream)
+    nbytes = aw.T * aw.D * 2 + aw.N * (aw.D // 2 + aw.D // 16) + aw.N * 4 + aw.T * aw.k * 8
+    out["adversarial"] = _hbm_entry(nbytes, ms, hbm, plan=R.last_router_plan(), tokens_per_s=aw.T / (ms / 1e3))
+    del xa, Wa
+    torch.cuda.empty_cache()
+
+    # standalone quantizer on the prefill batch (4 rotating 58.7 MB inputs)
+    pw = WL.WORKLOADS["prefill"]
+    xp = torch.from_numpy(WL.make_x(pw).view(np.int16)).view(torch.bfloat16).to(dev)
+    xs = [xp.clone() for _ in range(4)]
+    codes = torch.empty((pw.T, pw.D // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty(R.nvr_sf_bytes(pw.T, pw.D, "tiled"), dtype=torch.uint8, device=dev)
+    gsa = torch.empty(1, dtype=torch.float32, device=dev)
+    wsq = R.new_workspace(R.nvfp4_quantize_workspace_size(pw.T, pw.D), dev)
+    ms = _timed_calls(lambda i: R.nvfp4_quantize_act(xs[i % 4], "tiled", codes, sf, gsa, wsq), 200, stream)
+    nbytes = pw.T * pw.D * 2 + pw.T * (pw.D // 2 + pw.D // 16)
+    out["quantize"] = _hbm_entry(nbytes, ms, hbm, launches_per_call=2,
+                                 note="amax kernel + quantize kernel; x read twice (second pass mostly from L2)")
+    del xs, xp
+    torch.cuda.empty_cache()
+
+    # the decode kernel's own device duration at T = 1 (graph-free, events
+    # around each launch)
+    dw = WL.WORKLOADS["decode"]
+    gate = R.RouterGate(torch.from_numpy(WL.make_w(dw).view(np.int16)).view(torch.bfloat16).to(dev),
+                        torch.from_numpy(WL.make_bias(dw)).to(dev), k=dw.k, routed_scaling=dw.routed_scaling,
+                        max_tokens=1)
+    xd = torch.from_numpy(WL.make_x(dw.with_T(1)).view(np.int16)).view(torch.bfloat16).to(dev)
+    n = 500
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for e in evs:
+        for ev in e:
+            ev.record(stream)
+    for _ in range(10):
+        gate(xd)
+    torch.cuda.synchronize()
+    handles = [ctypes_array(e) for e in evs]
+    lib = _native.lib()
+    for i in range(n):
+        lib.nvr_set_profile_events(handles[i][0], 1)
+        gate(xd)
+    lib.nvr_set_profile_events(None, 0)
+    torch.cuda.synchronize()
+    durs = sorted(e[0].elapsed_time(e[1]) for e in evs)
+    ms = statistics.mean(durs)
+    nbytes = dw.N * (dw.D // 2 + dw.D // 16) + dw.D * 2 + dw.N * 4 + dw.k * 8
+    out["decode_kernel_T1"] = _hbm_entry(nbytes, ms, hbm, traffic=traffic.get("decode_router"),
+                                         median_ms=durs[n // 2], p10_ms=durs[n // 10], p90_ms=durs[9 * n // 10],
+                                         note="latency-bound: one launch, events around each launch")
+    return out
 
 
 def ctypes_array(events):
@@ -474,6 +616,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -218,6 +218,18 @@ nvr_status nvfp4_pack_weight(const void* W, nvr_dtype dt, int64_t N, int64_t D,
 size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k);
 
 /*
+ * router_gate_x_gsa_offset -- byte offset, inside a router workspace, of the
+ * fp32 global scale gsa = max|x| / 2688 that the latest tensor-core
+ * router_gate_topk / router_gate_logits call on that workspace computed for
+ * its x ("commit df05289: dsv4/layers/grouped_linear.py", zero-sync fused
+ * quantize section: the scale is produced and kept on the GPU, and other
+ * kernels read it there).  The same for every T, D and N; 4-byte aligned.
+ * Valid once that call's kernels have completed (stream order).  The decode
+ * kernel (T <= 16) keeps its scale on chip and does not store it.
+ */
+size_t router_gate_x_gsa_offset(void);
+
+/*
  * router_gate_topk -- the whole router call: quantize x, NVFP4 gate GEMM,
  * fused sigmoid / biased top-k / renormalise / scale epilogue.
  *
@@ -295,6 +307,32 @@ nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int64_t T, int6
                                     const float* w_gsa, int64_t N, const float* bias, int k,
                                     float routed_scaling, uint32_t flags, int32_t* out_ids,
                                     float* out_w, nvr_stream_t stream);
+
+/*
+ * router_hash_topk -- the hash router of the first MoE layers: each token's
+ * experts are read from a token-id table, with no gate GEMM.
+ *
+ * Source: "nvfp4-megamoe-kernel commit df05289: dsv4/layers/grouped_linear.py",
+ * hash-router item (tid2eid is an int32 lookup).  The page gives no weights;
+ * with no gate scores the router's renormalise and scale steps see k equal
+ * scores, so every selected expert weighs fl32(routed_scaling / k).
+ *
+ *   token_ids  [T] int32 token ids (device)
+ *   tid2eid    [vocab, k] int32 table (device, row-major): row tid holds the
+ *              k expert ids of token id tid, in output order
+ *   n_experts  number of experts; 1 <= k <= min(16, n_experts)
+ *   out_ids    out [T, k] int32: out_ids[t, j] = tid2eid[token_ids[t], j]
+ *   out_w      out [T, k] fp32: routed_scaling / k
+ * A token id outside [0, vocab) gives ids -1 and weights 0 for its row; a
+ * table entry outside [0, n_experts) gives id -1 and weight 0 in its slot
+ * (no out-of-bounds access in either case).  Host checks: NULL pointers,
+ * T < 0, vocab < 1, k out of range (NVR_ERR_INVALID_ARG); pointers not 4-byte
+ * aligned (NVR_ERR_ALIGNMENT).  One kernel, no workspace, no host sync;
+ * T == 0 launches nothing.
+ */
+nvr_status router_hash_topk(const int32_t* token_ids, int64_t T, const int32_t* tid2eid, int64_t vocab,
+                            int64_t n_experts, int k, float routed_scaling, int32_t* out_ids, float* out_w,
+                            nvr_stream_t stream);
 
 /*
  * router_gate_logits -- test hook: the same quantization and gate GEMM as

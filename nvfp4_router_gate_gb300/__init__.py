@@ -11,7 +11,8 @@ Functions (same names as include/nvfp4_router.h):
 * ``router_gate_topk(x, W_fp4, W_sf, w_gsa, bias, k, routed_scaling, raw=False)``
   -> (ids int32 [T, k], weights fp32 [T, k])
 * ``router_gate_logits(x, W_fp4, W_sf, w_gsa)`` -> logits fp32 [T, N]
-* ``router_gate_workspace_size``, ``nvfp4_quantize_workspace_size``,
+* ``router_hash_topk(token_ids, tid2eid, n_experts, routed_scaling)`` -> (ids, weights)
+* ``router_gate_workspace_size``, ``router_gate_x_gsa``, ``nvfp4_quantize_workspace_size``,
   ``nvr_sf_bytes``, ``nvr_read_device_status``
 
 ``RouterGate`` keeps the packed weight, the workspace and the output buffers
@@ -27,8 +28,8 @@ from ._native import (NVR_FLAG_FORCE_DECODE, NVR_FLAG_FORCE_TENSOR_CORE, NVR_FLA
                       NVR_FLAG_SPLIT_K_2, NVR_FLAG_SPLIT_K_4, NVR_FLAG_SPLIT_K_8, NVR_FLAG_SPLIT_N,
                       RouterError)
 
-__all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits",
-           "router_gate_workspace_size", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
+__all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits", "router_hash_topk",
+           "router_gate_workspace_size", "router_gate_x_gsa", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
            "nvr_read_device_status", "last_router_plan", "plan_router", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
            "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "NVR_FLAG_SPLIT_K_2",
            "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "new_workspace"]
@@ -67,6 +68,13 @@ def nvfp4_quantize_workspace_size(rows, D):
 
 def router_gate_workspace_size(T_max, D, N, k=8):
     return int(_native.lib().router_gate_workspace_size(T_max, D, N, k))
+
+
+def router_gate_x_gsa(workspace):
+    """A one-element fp32 view of the workspace word holding the global scale of
+    x from the latest tensor-core router call on it (stays on the GPU)."""
+    off = int(_native.lib().router_gate_x_gsa_offset())
+    return workspace[off:off + 4].view(torch.float32)
 
 
 def new_workspace(nbytes, device=None):
@@ -151,6 +159,24 @@ def router_gate_logits(x, W_fp4, W_sf, w_gsa, logits=None, workspace=None, flags
         workspace.numel(), _stream(stream))
     _native.check("router_gate_logits", st)
     return logits
+
+
+def router_hash_topk(token_ids, tid2eid, n_experts, routed_scaling=1.0, out_ids=None, out_w=None, stream=None):
+    """Hash router: ids int32 [T, k] = tid2eid[token_ids], weights routed_scaling / k."""
+    if token_ids.dtype != torch.int32 or tid2eid.dtype != torch.int32:
+        raise TypeError("token_ids and tid2eid must be int32")
+    T = token_ids.shape[0]
+    vocab, k = tid2eid.shape
+    dev = token_ids.device
+    if out_ids is None:
+        out_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if out_w is None:
+        out_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    st = _native.lib().router_hash_topk(
+        _dev(token_ids, "token_ids"), T, _dev(tid2eid, "tid2eid"), vocab, int(n_experts), int(k),
+        float(routed_scaling), _dev(out_ids, "out_ids"), _dev(out_w, "out_w"), _stream(stream))
+    _native.check("router_hash_topk", st)
+    return out_ids, out_w
 
 
 _PLAN_SEQUENCES = {0: "none", 1: "decode", 2: "fused", 3: "amax+fused", 4: "amax+quantize+splitk+epilogue",

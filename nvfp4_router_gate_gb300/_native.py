@@ -51,10 +51,12 @@ SIGNATURES = {
     "nvfp4_quantize_act": (_i32, [_p, _i32, _i64, _i64, _p, _p, _i32, _p, _p, _sz, _p]),
     "nvfp4_pack_weight": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _p, _sz, _p]),
     "router_gate_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
+    "router_gate_x_gsa_offset": (_sz, []),
     "router_gate_topk": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _p, _i32, _f32, _u32,
                                 _p, _p, _p, _sz, _p]),
     "router_gate_topk_noalloc": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _p, _i32, _f32,
                                         _u32, _p, _p, _p]),
+    "router_hash_topk": (_i32, [_p, _i64, _p, _i64, _i64, _i32, _f32, _p, _p, _p]),
     "router_gate_logits": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _u32, _p, _p, _sz, _p]),
     "nvr_read_device_status": (_i32, [_p, _p, ctypes.POINTER(_i32)]),
     "nvr_set_profile_events": (_i32, [_p, _i32]),

@@ -489,6 +489,8 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k) {
          static_cast<size_t>(t_dec) * N * 8 + 8 * 256;
 }
 
+size_t router_gate_x_gsa_offset(void) { return router_ws_layout(1, 64, 1).scalars; }
+
 nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
                             const uint8_t* W_scales, const float* w_gsa, int64_t N, const float* bias,
                             int k, float routed_scaling, uint32_t flags, int32_t* out_ids,

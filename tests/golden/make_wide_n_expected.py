@@ -6,8 +6,9 @@ test reads these stored oracle values instead of recomputing them.  This
 script calls only ``oracle/`` and the seeded ``workloads`` generator; nothing
 comes from the CUDA path.  Stored per token: the 64 best outputs by float32
 logit (ids, float64 logits, the |x|.|w| bounds) and, over all other outputs,
-the largest logit plus its slack -- enough to check any GPU top-k with k <= 16
-under the oracle's comparison rules.  Checksums of the generated inputs let
+the largest logit less its slack (``oracle.compare.candidate_summary``) --
+enough to check any GPU top-k with k <= 16 under the oracle's comparison
+rules (``oracle.compare.check_topk_candidates``).  Checksums of the generated inputs let
 the test detect a generator that produces different numbers.
 
 Run:  python tests/golden/make_wide_n_expected.py
@@ -23,7 +24,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__)
 sys.path.insert(0, ROOT)
 
 import workloads as WL  # noqa: E402
-from oracle import quantize as Q, gemm, router, compare  # noqa: E402
+from oracle import quantize as Q, gemm, compare  # noqa: E402
 
 OUT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "wide_n_expected.npz")
 TOP = 64
@@ -59,17 +60,9 @@ def main():
         wq, ws, _ = Q.quantize(WL.bf16_bits_to_float32(c), gsa=wg)
         L[:, n0:n0 + c.shape[0]], B[:, n0:n0 + c.shape[0]] = gemm.logits(xq, xs, xg, wq, ws, wg)
         print("rows", n0 + c.shape[0], flush=True)
-    keys = router.selection_keys(L, None, raw=True)
-    tau = compare.key_slack(L, B, keys, None, raw=True)
-    ids = router.topk_order(keys, TOP)
-    rest = np.empty(w.T)
-    for t in range(w.T):
-        mask = np.ones(w.N, bool)
-        mask[ids[t]] = False
-        rest[t] = np.max(keys[t][mask].astype(np.float64) - tau[t][mask])
+    ids, cand_L, cand_B, rest = compare.candidate_summary(L, B, None, raw=True, top=TOP)
     np.savez_compressed(
-        OUT, ids=ids.astype(np.int32), logits=np.take_along_axis(L, ids, 1),
-        bounds=np.take_along_axis(B, ids, 1), rest_max=rest, x_gsa=np.float32(xg), w_gsa=wg,
+        OUT, ids=ids, logits=cand_L, bounds=cand_B, rest_max=rest, x_gsa=np.float32(xg), w_gsa=wg,
         digest=np.array(input_digest(w)))
     print("wrote", OUT)
 

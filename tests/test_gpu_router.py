@@ -49,6 +49,23 @@ def test_logits_within_tolerance(name, T, flags):
     assert rel.max() < 1e-4
 
 
+def test_prefill_logits_full_size_default_plan():
+    """All 4096 x 256 logits of the prefill batch on the plan a default call
+    takes (one launch; at T = 4096 on a GB300: 112-row tiles, K split over 4
+    CTAs, no clusters), element by element under the logit tolerance."""
+    import nvfp4_router_gate_gb300 as R
+    w = WL.WORKLOADS["prefill"]
+    case = Case(w)
+    R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, w.k, w.routed_scaling)
+    plan_topk = R.last_router_plan()
+    g = _logits(case, 0)
+    assert R.last_router_plan() == plan_topk and plan_topk["sequence"] == "fused", plan_topk
+    L, B = case.oracle_rows(np.arange(w.T))
+    assert compare.check_logits(g, L, B) == 0
+    rel = np.abs(g - L) / (compare.LOGIT_ABS_FRAC * B + np.abs(L) + 1e-30)
+    assert rel.max() < 1e-4
+
+
 def _grid_operands(rng, rows, D, amax_block):
     """Inputs whose NVFP4 quantization is exact: gsa = 1 (one element 2688 =
     6 * 448 alone in block `amax_block` of row 0) and block scales 2**b,
@@ -114,11 +131,20 @@ def test_prefill_router_odd_tile_count():
     assert compare.topk_ok(res), res
 
 
-def test_prefill_router_sampled_rows():
-    case = Case(WL.WORKLOADS["prefill"])
-    ids, w = case.run()
-    rows = np.unique(np.concatenate([np.arange(0, 4096, 37), np.arange(4090, 4096), [127, 128, 129]]))
-    res = case.check(ids, w, rows)
+def test_prefill_router_all_rows():
+    """Every row of the T = 4096 prefill batch on the default one-launch plan,
+    and the global scale that launch computed itself (bit-exact)."""
+    import nvfp4_router_gate_gb300 as R
+    w = WL.WORKLOADS["prefill"]
+    case = Case(w)
+    ws = R.new_workspace(R.router_gate_workspace_size(w.T, w.D, w.N, w.k))
+    ids, wts = R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, w.k,
+                                  w.routed_scaling, w.raw, workspace=ws)
+    torch.cuda.synchronize()
+    assert R.last_router_plan()["sequence"] == "fused"
+    gsa = R.router_gate_x_gsa(ws).item()
+    assert np.float32(gsa).view(np.uint32) == Q.global_scale(case.x32).view(np.uint32)
+    res = case.check(ids.cpu().numpy(), wts.cpu().numpy(), np.arange(w.T))
     assert compare.topk_ok(res), res
 
 
@@ -131,11 +157,10 @@ def test_ragged_batches_all_rows(T):
 
 
 def test_adversarial_router():
+    """Every row of the T = 16384, E = 384 adversarial batch."""
     case = Case(WL.WORKLOADS["adversarial"])
     ids, w = case.run()
-    rows = np.unique(np.concatenate([np.arange(0, 16384, 61), np.arange(16376, 16384),
-                                     np.arange(0, 64)]))
-    res = case.check(ids, w, rows)
+    res = case.check(ids, w, np.arange(case.w.T))
     assert compare.topk_ok(res), res
     # all-zero rows (t % 4 == 1): every logit is exactly 0, so the ids are 0..7
     # and each weight is routed_scaling / 8
@@ -567,3 +592,70 @@ def test_fused_quantizer_codes_via_one_hot_gate(flags):
             g = out.cpu().numpy().astype(np.float64)
             err = np.abs(g - L)
             assert np.all(err <= 1e-6 * np.abs(L)), (half_x, c0, np.argwhere(err > 1e-6 * np.abs(L))[:5])
+
+
+def _probe_x_vectorized(rng, T, D, crafted):
+    """_fused_probe_x for batches too large for a Python loop: the rows in the
+    boolean mask `crafted` get the crafted blocks (E2M1 midpoints times every
+    E4M3 significand and their bf16 neighbours, zeros, subnormals; gsa = 1 for
+    the whole batch), the others LogNormal-scaled normals."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    x = (rng.standard_normal((T, D)) * np.exp(rng.standard_normal((T, 1)))).astype(np.float32)
+    bits = WL.float32_to_bf16_bits(x)
+    rows = np.nonzero(crafted)[0]
+    nb = D // 16
+    t = rows[:, None]
+    b = np.arange(nb)[None, :]
+    s = (8 + (t + b) % 8) / 8.0 * 2.0 ** ((b % 5) - 2)                  # block scale, [R, nb]
+    vals = np.zeros((rows.size, nb, 16), np.float32)
+    vals[:, :, 0] = 6.0 * s
+    probe = mids[(b[..., None] + np.arange(15)) % 7]                  # [1, nb, 15]
+    vals[:, :, 1:] = probe * s[..., None] * rng.choice([-1, 1], (rows.size, nb, 15))
+    vb = WL.float32_to_bf16_bits(vals).astype(np.int32)
+    off = np.zeros((rows.size, nb, 7), np.int32)
+    off[:, :, :6] = [0, 1, -1, 2, -2, 0]                              # bf16 neighbours of the ties
+    off[:, :, 6] = (t * 7 + b) % 4
+    vb[:, :, 1:8] += off
+    vb[:, :, 8] = np.where(b % 3 == 0, 0x8000, 0x0001)                # -0 or the smallest subnormal
+    bits[rows] = vb.astype(np.uint16).reshape(rows.size, D)
+    bits[rows[0], 5] = WL.float32_to_bf16_bits(np.array([2688.0], np.float32))[0]
+    return bits
+
+
+def test_fused_quantizer_codes_production_plan():
+    """The one-hot probe of the in-GEMM quantizer at the prefill shape
+    (T = 4096, D = 7168), so that it runs the default plan's tiles, K split
+    and row assignment: every x element's code and scale byte is read back
+    through one logit, on a batch with crafted rows (gsa = 1) and on a plain
+    LogNormal batch (arbitrary gsa)."""
+    import nvfp4_router_gate_gb300 as R
+    rng = np.random.default_rng(41)
+    T, D = 4096, 7168
+    ws = R.new_workspace(R.router_gate_workspace_size(T, D, 256, 8))
+    for crafted in (rng.random(T) < 0.5, None):
+        if crafted is None:
+            bits = WL.make_x(WL.WORKLOADS["prefill"])
+        else:
+            bits = _probe_x_vectorized(rng, T, D, crafted)
+        x32 = WL.bf16_bits_to_float32(bits)
+        xd = to_device(bits, "bf16")
+        xq, xs, xg = Q.quantize(x32)
+        if crafted is not None:
+            assert xg == 1.0
+        A = gemm.dequantize(xq, xs)
+        plans = set()
+        for c0 in range(0, D, 256):
+            cols = np.arange(c0, c0 + 256)
+            W = _one_hot_gate(cols, D)
+            wf, wsf, wg = R.nvfp4_pack_weight(to_device(W, "f32"))
+            out = R.router_gate_logits(xd, wf, wsf, wg, workspace=ws)
+            plans.add(tuple(sorted(R.last_router_plan().items())))
+            torch.cuda.synchronize()
+            assert np.float32(R.router_gate_x_gsa(ws).item()) == xg
+            wq, wsb, wgg = Q.quantize(W)
+            wv = gemm.dequantize(wq, wsb)[np.arange(256), cols]        # the one nonzero of each row
+            L = A[:, cols] * (wv * (np.float64(xg) * np.float64(wgg)))[None, :]
+            g = out.cpu().numpy().astype(np.float64)
+            err = np.abs(g - L)
+            assert np.all(err <= 1e-6 * np.abs(L)), (c0, np.argwhere(err > 1e-6 * np.abs(L))[:5])
+        assert len(plans) == 1 and dict(next(iter(plans)))["sequence"] == "fused", plans
