@@ -138,3 +138,38 @@ def make_bias(w: Workload, seed=SEED):
 def x_as_float32(x, w: Workload):
     """float32 view of a generated activation array (exact widening for bf16)."""
     return bf16_bits_to_float32(x) if w.dtype == "bf16" else np.asarray(x, np.float32)
+
+
+# ------------------------------------------------------------------ hash router
+# Token-id routing of the first MoE layers: a [vocab, k] int32 table of
+# expert ids (k distinct experts per token id) and a batch of token ids.
+# Table: a seeded random base expert per token id plus k distinct offsets
+# shared by all rows, modulo the expert count; token ids uniform over the
+# vocabulary.  Streams: table = seed + 4, token ids = seed + 5.
+
+@dataclass(frozen=True)
+class HashWorkload:
+    name: str
+    T: int
+    vocab: int
+    n_experts: int
+    k: int
+    routed_scaling: float
+
+    def with_T(self, T):
+        return replace(self, T=T)
+
+
+HASH_ROUTER = HashWorkload("hash_router", 4096, 129280, 256, 8, 2.5)
+
+
+def make_hash_table(h: HashWorkload, seed=SEED):
+    rng = np.random.default_rng(seed + 4)
+    base = rng.integers(0, h.n_experts, size=h.vocab)
+    offs = rng.choice(h.n_experts, size=h.k, replace=False)
+    return ((base[:, None] + offs[None, :]) % h.n_experts).astype(np.int32)
+
+
+def make_token_ids(h: HashWorkload, seed=SEED):
+    rng = np.random.default_rng(seed + 5)
+    return rng.integers(0, h.vocab, size=h.T).astype(np.int32)
