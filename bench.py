@@ -454,6 +454,7 @@ def extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic):
     back-to-back calls with CUDA events on the launching stream:
       wide_n       the N = 129280 raw head (T = 32, k = 8 and k = 1): weight
                    streaming, 0.52 GB per call (> L2: every call reads it from HBM);
+      lm_head_linear_T32  the same weight through nvfp4_linear, bf16 logits out;
       adversarial  the T = 16384, E = 384 batch (x 235 MB > L2): tokens/s too;
       quantize     nvfp4_quantize_act on the prefill batch (x read once, codes
                    and scales written), four rotating inputs;
@@ -484,7 +485,16 @@ def extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic):
         nbytes = wbytes + wn.T * wn.D * 2 + wn.T * k * 8
         out["wide_n_k%d" % k] = _hbm_entry(nbytes, ms, hbm, plan=R.last_router_plan(),
                                            tensor_tflops=2 * wn.T * wn.D * wn.N / (ms / 1e3) / 1e12)
-    del W_fp4, W_sf
+    # the same weight as an NVFP4 linear layer (lm_head shape), bf16 logits out
+    ws = R.new_workspace(R.nvfp4_linear_workspace_size(wn.T, wn.D, wn.N), dev)
+    lm_out = torch.empty((wn.T, wn.N), dtype=torch.bfloat16, device=dev)
+    ms = _timed_calls(lambda i: R.nvfp4_linear(x, W_fp4, W_sf, w_gsa, out=lm_out, workspace=ws), 50, stream)
+    nbytes = wbytes + wn.T * wn.D * 2 + wn.T * wn.N * 2
+    out_l = _hbm_entry(nbytes, ms, hbm, plan=R.last_router_plan(),
+                       tensor_tflops=2 * wn.T * wn.D * wn.N / (ms / 1e3) / 1e12,
+                       note="nvfp4_linear T=32 D=7168 N=129280 (lm_head shape), bf16 out")
+    out["lm_head_linear_T32"] = out_l
+    del W_fp4, W_sf, lm_out
     torch.cuda.empty_cache()
 
     # adversarial large batch

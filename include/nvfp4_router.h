@@ -115,6 +115,11 @@ enum {
   NVR_FLAG_SPLIT_K_4 = 16u,
   NVR_FLAG_SPLIT_K_8 = 32u,
   NVR_FLAG_SPLIT_N = 64u,
+  /* Forces the weight-streaming kernel (T <= 128; NVR_ERR_UNSUPPORTED for
+   * more tokens): the 128-row weight tiles are the MMA's M and the tokens its
+   * N, the weight is read once, per-token top-k lists are merged across CTAs.
+   * The default for heads of more than 256 experts at T <= 128. */
+  NVR_FLAG_STREAM = 128u,
   /* Failure-detection test hook (with FORCE_TENSOR_CORE or a SPLIT flag): the tensor-core
    * kernel's MMA issuer issues nothing, so its bounded waits run out after
    * about one second; the kernel stores NVR_ERR_TIMEOUT in the workspace
@@ -136,9 +141,11 @@ const char* nvr_last_cuda_error(void);
  *   out[0] kernel sequence: 0 none yet, 1 the decode kernel, 2 the one-launch
  *          fused router, 3 amax then the fused router, 4 amax, quantize,
  *          K-split GEMM and epilogue kernel, 5 amax, quantize and the
- *          N-split GEMM;
- *   out[1] token-tile rows (128 or 112; 0 for sequences 0, 1);
- *   out[2] CTAs per token tile (K splits for 2-4, N splits for 5; 0 for 0, 1);
+ *          N-split GEMM, 6 amax, quantize and the weight-streaming GEMM;
+ *   out[1] token-tile rows (128 or 112; for sequence 6 the token columns of
+ *          the MMA, 32, 64 or 128; 0 for sequences 0, 1);
+ *   out[2] CTAs per token tile (K splits for 2-4, N splits for 5 and 6; 0 for
+ *          0, 1);
  *   out[3] 1 when the CTAs of a tile form a thread-block cluster, else 0.
  * No counterpart on the pages: a diagnostic for tests and benchmarks.
  * NVR_ERR_INVALID_ARG for a NULL out. */
@@ -248,7 +255,7 @@ size_t router_gate_x_gsa_offset(void);
  *   routed_scaling  multiplies the renormalised weights
  *   flags        0 or NVR_FLAG_RAW_LOGITS, optionally with one kernel-choice
  *                flag (FORCE_TENSOR_CORE, FORCE_DECODE, SPLIT_K_2/4/8,
- *                SPLIT_N) and, with a tensor-core choice, TEST_STALL
+ *                SPLIT_N, STREAM) and, with a tensor-core choice, TEST_STALL
  *   out_ids      out [T, k] int32: expert ids, best first (key descending,
  *                equal keys: lower id first)
  *   out_w        out [T, k] fp32: routed_scaling * s_id / sum of the k
@@ -270,8 +277,12 @@ size_t router_gate_x_gsa_offset(void);
  *     amax kernel runs first and the same kernel skips its own max|x| pass.
  *   - fp32 x, N <= 256: amax, quantize, K-split GEMM and a warp-per-token
  *     epilogue kernel.
- *   - N > 256: amax, quantize and the N-split GEMM, which routes from the
- *     logits in tensor memory.
+ *   - N > 256, T <= 128: amax, quantize and the weight-streaming GEMM (the
+ *     weight rows are the MMA's M, the tokens its N; each weight byte is read
+ *     once), which routes from the logits in tensor memory and merges the
+ *     CTAs' per-token lists in its last CTA.
+ *   - N > 256, T > 128: amax, quantize and the N-split GEMM, which routes
+ *     from the logits in tensor memory.
  */
 nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
                             const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,
@@ -328,11 +339,39 @@ nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int64_t T, int6
  * (no out-of-bounds access in either case).  Host checks: NULL pointers,
  * T < 0, vocab < 1, k out of range (NVR_ERR_INVALID_ARG); pointers not 4-byte
  * aligned (NVR_ERR_ALIGNMENT).  One kernel, no workspace, no host sync;
- * T == 0 launches nothing.
+ * T == 0 launches nothing (token_ids, out_ids and out_w may then be NULL).
  */
 nvr_status router_hash_topk(const int32_t* token_ids, int64_t T, const int32_t* tid2eid, int64_t vocab,
                             int64_t n_experts, int k, float routed_scaling, int32_t* out_ids, float* out_w,
                             nvr_stream_t stream);
+
+/*
+ * nvfp4_linear -- an NVFP4 linear layer with a runtime activation scale:
+ * out = quantize(x) . W^T, i.e. out[t, n] = sum_i xq[t, i] * wq[n, i] with
+ * both operands dequantized (codes x block scales x global scales), fp32
+ * accumulation on the tensor cores, stored as fp32 or bf16 (round to nearest
+ * even).
+ *
+ * Source: "nvfp4-megamoe-kernel commit df05289: dsv4/layers/grouped_linear.py",
+ * lm_head item (BF16 weight quantized to NVFP4 at load time, the production
+ * NVFP4 GEMM, runtime gsa for the activation) and "commit 04cf8ca:
+ * dsv4/layers/router.py", runtime-gsa section (the same runtime gsa in every
+ * NVFP4 linear layer).
+ *
+ *   x        [T, D] activations (bf16 or fp32 per dt)
+ *   W_fp4, W_scales, w_gsa   the weight [N, D] from nvfp4_pack_weight
+ *   out      out [T, N] row-major, fp32 (out_dt NVR_F32) or bf16 (NVR_BF16),
+ *            16-byte aligned
+ *   workspace  nvfp4_linear_workspace_size(T, D, N) bytes, zeroed once
+ * Launches: amax, quantize, then for T <= 128 the weight-streaming GEMM
+ * (weight rows as the MMA's M, tokens as its N: each weight byte read once --
+ * the lm_head shape at decode batch sizes), for more tokens the token-tiled
+ * N-split GEMM.  Errors as for router_gate_topk.
+ */
+size_t nvfp4_linear_workspace_size(int64_t T_max, int64_t D, int64_t N);
+nvr_status nvfp4_linear(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
+                        const uint8_t* W_scales, const float* w_gsa, int64_t N, void* out, nvr_dtype out_dt,
+                        void* workspace, size_t ws_bytes, nvr_stream_t stream);
 
 /*
  * router_gate_logits -- test hook: the same quantization and gate GEMM as
@@ -340,8 +379,8 @@ nvr_status router_hash_topk(const int32_t* token_ids, int64_t T, const int32_t* 
  * logit = acc * gsa_x * gsa_w) instead of the epilogue's outputs.  Used to
  * check the GEMM on its own and to measure what writing logits to memory
  * costs.  flags: 0 or one kernel-choice flag (FORCE_TENSOR_CORE,
- * FORCE_DECODE, SPLIT_K_2/4/8, SPLIT_N); RAW_LOGITS and TEST_STALL are
- * invalid here.  Workspace as for router_gate_topk.
+ * FORCE_DECODE, SPLIT_K_2/4/8, SPLIT_N, STREAM); RAW_LOGITS and TEST_STALL
+ * are invalid here.  Workspace as for router_gate_topk.
  */
 nvr_status router_gate_logits(const void* x, nvr_dtype dt, int64_t T, int64_t D,
                               const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,

@@ -12,6 +12,8 @@ Functions (same names as include/nvfp4_router.h):
   -> (ids int32 [T, k], weights fp32 [T, k])
 * ``router_gate_logits(x, W_fp4, W_sf, w_gsa)`` -> logits fp32 [T, N]
 * ``router_hash_topk(token_ids, tid2eid, n_experts, routed_scaling)`` -> (ids, weights)
+* ``nvfp4_linear(x, W_fp4, W_sf, w_gsa, out_dtype=torch.float32)`` -> out [T, N]
+  (``Nvfp4Linear`` keeps the packed weight and a workspace resident)
 * ``router_gate_workspace_size``, ``router_gate_x_gsa``, ``nvfp4_quantize_workspace_size``,
   ``nvr_sf_bytes``, ``nvr_read_device_status``
 
@@ -26,13 +28,14 @@ import torch
 from . import _native
 from ._native import (NVR_FLAG_FORCE_DECODE, NVR_FLAG_FORCE_TENSOR_CORE, NVR_FLAG_RAW_LOGITS,
                       NVR_FLAG_SPLIT_K_2, NVR_FLAG_SPLIT_K_4, NVR_FLAG_SPLIT_K_8, NVR_FLAG_SPLIT_N,
-                      RouterError)
+                      NVR_FLAG_STREAM, RouterError)
 
 __all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits", "router_hash_topk",
            "router_gate_workspace_size", "router_gate_x_gsa", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
            "nvr_read_device_status", "last_router_plan", "plan_router", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
            "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "NVR_FLAG_SPLIT_K_2",
-           "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "new_workspace"]
+           "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "NVR_FLAG_STREAM", "new_workspace",
+           "nvfp4_linear", "nvfp4_linear_workspace_size", "Nvfp4Linear"]
 
 _LAYOUTS = {"linear": _native.NVR_SF_LINEAR, "tiled": _native.NVR_SF_TILED}
 
@@ -161,6 +164,51 @@ def router_gate_logits(x, W_fp4, W_sf, w_gsa, logits=None, workspace=None, flags
     return logits
 
 
+def nvfp4_linear_workspace_size(T_max, D, N):
+    return int(_native.lib().nvfp4_linear_workspace_size(T_max, D, N))
+
+
+def nvfp4_linear(x, W_fp4, W_sf, w_gsa, out_dtype=torch.float32, out=None, workspace=None, stream=None):
+    """NVFP4 linear with a runtime activation scale: quantize(x) [T, D] . W^T -> [T, N] fp32 or bf16."""
+    T, D = x.shape
+    N = W_fp4.shape[0]
+    dev = x.device
+    if out is None:
+        out = torch.empty((T, N), dtype=out_dtype, device=dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be float32 or bfloat16")
+    if workspace is None:
+        workspace = new_workspace(nvfp4_linear_workspace_size(T, D, N), dev)
+    code = _native.NVR_BF16 if out.dtype == torch.bfloat16 else _native.NVR_F32
+    st = _native.lib().nvfp4_linear(
+        _dev(x, "x"), _dtype_code(x), T, D, _dev(W_fp4, "W_fp4"), _dev(W_sf, "W_sf"), _dev(w_gsa, "w_gsa"), N,
+        _dev(out, "out"), code, _dev(workspace, "workspace"), workspace.numel(), _stream(stream))
+    _native.check("nvfp4_linear", st)
+    return out
+
+
+class Nvfp4Linear:
+    """Resident NVFP4 linear layer: the weight [N, D] is quantized once at
+    construction (nvfp4_pack_weight), the workspace and the output buffer
+    stay allocated, and each call quantizes its activations with their own
+    runtime global scale.  Calls allocate nothing (CUDA-graph capturable)."""
+
+    def __init__(self, W, max_tokens=128, out_dtype=torch.float32):
+        self.N, self.D = W.shape
+        dev = W.device
+        self.W_fp4, self.W_sf, self.w_gsa = nvfp4_pack_weight(W)
+        self.max_tokens = int(max_tokens)
+        self.workspace = new_workspace(nvfp4_linear_workspace_size(self.max_tokens, self.D, self.N), dev)
+        self.out = torch.empty((self.max_tokens, self.N), dtype=out_dtype, device=dev)
+
+    def __call__(self, x, stream=None):
+        T = x.shape[0]
+        if T > self.max_tokens:
+            raise ValueError("batch of %d tokens exceeds max_tokens=%d" % (T, self.max_tokens))
+        return nvfp4_linear(x, self.W_fp4, self.W_sf, self.w_gsa, out=self.out[:T], workspace=self.workspace,
+                            stream=stream)
+
+
 def router_hash_topk(token_ids, tid2eid, n_experts, routed_scaling=1.0, out_ids=None, out_w=None, stream=None):
     """Hash router: ids int32 [T, k] = tid2eid[token_ids], weights routed_scaling / k."""
     if token_ids.dtype != torch.int32 or tid2eid.dtype != torch.int32:
@@ -180,7 +228,7 @@ def router_hash_topk(token_ids, tid2eid, n_experts, routed_scaling=1.0, out_ids=
 
 
 _PLAN_SEQUENCES = {0: "none", 1: "decode", 2: "fused", 3: "amax+fused", 4: "amax+quantize+splitk+epilogue",
-                   5: "amax+quantize+splitn"}
+                   5: "amax+quantize+splitn", 6: "amax+quantize+stream"}
 
 
 def last_router_plan():

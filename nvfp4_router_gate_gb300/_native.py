@@ -30,6 +30,7 @@ NVR_FLAG_SPLIT_K_2 = 8
 NVR_FLAG_SPLIT_K_4 = 16
 NVR_FLAG_SPLIT_K_8 = 32
 NVR_FLAG_SPLIT_N = 64
+NVR_FLAG_STREAM = 128
 NVR_FLAG_TEST_STALL = 1 << 30
 
 _p = ctypes.c_void_p
@@ -57,6 +58,8 @@ SIGNATURES = {
     "router_gate_topk_noalloc": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _p, _i32, _f32,
                                         _u32, _p, _p, _p]),
     "router_hash_topk": (_i32, [_p, _i64, _p, _i64, _i64, _i32, _f32, _p, _p, _p]),
+    "nvfp4_linear_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "nvfp4_linear": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _p, _i32, _p, _sz, _p]),
     "router_gate_logits": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _u32, _p, _p, _sz, _p]),
     "nvr_read_device_status": (_i32, [_p, _p, ctypes.POINTER(_i32)]),
     "nvr_set_profile_events": (_i32, [_p, _i32]),

@@ -174,7 +174,8 @@ nvr_status quantize_impl(const void* x, nvr_dtype dt, int64_t rows, int64_t D, u
   return cuda_status(e);
 }
 
-constexpr uint32_t kKernelFlags = NVR_FLAG_SPLIT_K_2 | NVR_FLAG_SPLIT_K_4 | NVR_FLAG_SPLIT_K_8 | NVR_FLAG_SPLIT_N;
+constexpr uint32_t kKernelFlags =
+    NVR_FLAG_SPLIT_K_2 | NVR_FLAG_SPLIT_K_4 | NVR_FLAG_SPLIT_K_8 | NVR_FLAG_SPLIT_N | NVR_FLAG_STREAM;
 
 // Checks the router flags and folds a kernel-choice flag into
 // FORCE_TENSOR_CORE; NVR_ERR_INVALID_ARG for unknown or conflicting flags.
@@ -193,7 +194,7 @@ nvr_status normalize_flags(uint32_t& flags) {
 // The launch plan of a router call (the sequence codes of nvr_last_router_plan).
 struct RouterPlan {
   int seq = 0;                 // 1 decode, 2 fused, 3 amax + fused, 4 amax + quantize + K split + epilogue,
-                               // 5 amax + quantize + N split
+                               // 5 amax + quantize + N split, 6 amax + quantize + weight streaming
   int tile_rows = 0, per_tile = 0;
   bool clustered = false;      // seq 1: decode clusters; seq 2-3: the tile's CTAs form a cluster
   DecodePlan dp;               // seq 1
@@ -232,11 +233,13 @@ nvr_status plan_router(int64_t T, int64_t D, int64_t N, bool bf16, uint32_t flag
   // Up to 256 experts: K split over S CTAs with one tensor-core accumulator
   // for the whole row each; bf16 activations are quantized inside the GEMM
   // and routed in the same kernel, fp32 ones take the standalone quantizer,
-  // the K-split GEMM and the epilogue kernel.  Wider heads: N tiles split
-  // across CTAs with a top-k merge, after the standalone quantize kernel.
-  const int split_k = forced_split                        ? forced_split
-                      : (flags & NVR_FLAG_SPLIT_N) || N > 256 ? 0
-                                                              : plan_splitk(T, D, sms);
+  // the K-split GEMM and the epilogue kernel.  Wider heads, after the
+  // standalone quantize kernel: up to 128 tokens stream the weight (its
+  // 128-row tiles as the MMA's M, the tokens as its N), more tokens split the
+  // N tiles across CTAs; both merge the per-token top-k lists across CTAs.
+  const int split_k = forced_split ? forced_split
+                      : (flags & (NVR_FLAG_SPLIT_N | NVR_FLAG_STREAM)) || N > 256 ? 0
+                                                                                   : plan_splitk(T, D, sms);
   if (split_k > 0 && bf16) {
     const int n_st = static_cast<int>((D / kBlock + 15) / 16);
     int tile_rows = 128, S = 1;
@@ -274,6 +277,13 @@ nvr_status plan_router(int64_t T, int64_t D, int64_t N, bool bf16, uint32_t flag
     rp.per_tile = split_k;
     return NVR_OK;
   }
+  if ((flags & NVR_FLAG_STREAM) || (!(flags & NVR_FLAG_SPLIT_N) && T <= 128)) {
+    if (T > 128) return NVR_ERR_UNSUPPORTED;
+    rp.seq = 6;
+    rp.tile_rows = stream_token_tile(T);
+    rp.per_tile = stream_splits(N, sms);
+    return NVR_OK;
+  }
   rp.g = plan_gemm(T, N, sms);
   if (rp.g.m_tiles > kMaxTicketTiles) return NVR_ERR_UNSUPPORTED;
   rp.seq = 5;
@@ -285,14 +295,18 @@ nvr_status plan_router(int64_t T, int64_t D, int64_t N, bool bf16, uint32_t flag
 nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
                        const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias, int k,
                        float routed_scaling, uint32_t flags, int32_t* out_ids, float* out_w,
-                       float* logits, void* ws, size_t ws_bytes, cudaStream_t s) {
+                       void* out_logits, bool logits_bf16, void* ws, size_t ws_bytes, cudaStream_t s) {
+  // logits mode (out_logits set): fp32 on every path; bf16 only on the
+  // streaming and N-split kernels (the callers force one of them)
+  float* logits = static_cast<float*>(out_logits);
   nvr_status st = check_common(x, dt, T, D, ws);
   if (st != NVR_OK) return st;
   if (!W_fp4 || !W_sf || !w_gsa || N <= 0 || N > (1 << 28)) return NVR_ERR_INVALID_ARG;
   if (!logits && (!out_ids || !out_w || k < 1 || k > kMaxKmax || k > N)) return NVR_ERR_INVALID_ARG;
   st = normalize_flags(flags);
   if (st != NVR_OK) return st;
-  if ((flags & kKernelFlags & ~static_cast<uint32_t>(NVR_FLAG_SPLIT_N)) && N > 256) return NVR_ERR_UNSUPPORTED;
+  if ((flags & kKernelFlags & ~static_cast<uint32_t>(NVR_FLAG_SPLIT_N | NVR_FLAG_STREAM)) && N > 256)
+    return NVR_ERR_UNSUPPORTED;
   if (!aligned16(W_fp4) || !aligned16(W_sf) || (reinterpret_cast<uintptr_t>(w_gsa) & 3u) ||
       (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
       (out_ids && (reinterpret_cast<uintptr_t>(out_ids) & 3u)) ||
@@ -313,7 +327,8 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   // the fused kernel's capacities, queried (once per device) only where it
   // may run -- never for a decode call, which may be the first call of a
   // process and inside a graph capture
-  const bool maybe_fused = bf16 && N <= 256 && !(flags & (NVR_FLAG_SPLIT_N | NVR_FLAG_FORCE_DECODE)) &&
+  const bool maybe_fused = bf16 && N <= 256 &&
+                           !(flags & (NVR_FLAG_SPLIT_N | NVR_FLAG_STREAM | NVR_FLAG_FORCE_DECODE)) &&
                            ((flags & NVR_FLAG_FORCE_TENSOR_CORE) || !plan_decode(T, D, N, sms, bf16).ok);
   int cluster_cap[5] = {0, 0, 0, 0, 0};
   int block_cap = 0;
@@ -324,6 +339,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   RouterPlan rp;
   st = plan_router(T, D, N, bf16, flags, sms, cluster_cap, block_cap, rp);
   if (st != NVR_OK) return st;
+  if (logits_bf16 && rp.seq != 5 && rp.seq != 6) return NVR_ERR_UNSUPPORTED;
   record_plan(rp.seq, rp.tile_rows, rp.per_tile, rp.clustered);
   if (rp.seq == 1) {
     float* keys = reinterpret_cast<float*>(w + L.decode);
@@ -373,6 +389,14 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   e = launch_quantize(x, bf16, T, D, true, qrec, xc, xsf, s);
   prof.after();
   if (e != cudaSuccess) return cuda_status(e);
+  if (rp.seq == 6) {
+    prof.before();
+    st = launch_gemm_stream(xc, xsf, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw, out_ids,
+                            out_w, out_logits, logits_bf16, reinterpret_cast<float4*>(w + L.partials),
+                            reinterpret_cast<uint32_t*>(w + L.tickets), status, rp.per_tile, stall, s);
+    prof.after();
+    return st;
+  }
   if (split_k > 0) {
     prof.before();
     st = launch_splitk_gemm(xc, xsf, T, D, W_fp4, W_sf, N, partials, status, split_k, stall, s);
@@ -386,7 +410,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   }
   prof.before();
   st = launch_gemm_topk(xc, xsf, x_gsa, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
-                        out_ids, out_w, logits, reinterpret_cast<float4*>(w + L.partials),
+                        out_ids, out_w, out_logits, logits_bf16, reinterpret_cast<float4*>(w + L.partials),
                         reinterpret_cast<uint32_t*>(w + L.tickets), status, rp.g, stall, s);
   prof.after();
   return st;
@@ -497,7 +521,7 @@ nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D, c
                             float* out_w, void* workspace, size_t ws_bytes, nvr_stream_t stream) {
   if (!out_ids || !out_w) return NVR_ERR_INVALID_ARG;
   return router_impl(x, dt, T, D, W_fp4, W_scales, w_gsa, N, bias, k, routed_scaling, flags, out_ids,
-                     out_w, nullptr, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+                     out_w, nullptr, false, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 nvr_status router_gate_logits(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
@@ -506,7 +530,23 @@ nvr_status router_gate_logits(const void* x, nvr_dtype dt, int64_t T, int64_t D,
   if (!logits) return NVR_ERR_INVALID_ARG;
   if (flags & (NVR_FLAG_RAW_LOGITS | NVR_FLAG_TEST_STALL)) return NVR_ERR_INVALID_ARG;
   return router_impl(x, dt, T, D, W_fp4, W_scales, w_gsa, N, nullptr, 1, 1.0f, flags, nullptr, nullptr,
-                     logits, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+                     logits, false, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t nvfp4_linear_workspace_size(int64_t T_max, int64_t D, int64_t N) {
+  return router_gate_workspace_size(T_max, D, N, 1);
+}
+
+nvr_status nvfp4_linear(const void* x, nvr_dtype dt, int64_t T, int64_t D, const uint8_t* W_fp4,
+                        const uint8_t* W_scales, const float* w_gsa, int64_t N, void* out, nvr_dtype out_dt,
+                        void* workspace, size_t ws_bytes, nvr_stream_t stream) {
+  if (!out) return NVR_ERR_INVALID_ARG;
+  if (out_dt != NVR_BF16 && out_dt != NVR_F32) return NVR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 15u) return NVR_ERR_ALIGNMENT;
+  // up to 128 tokens stream the weight; more take the token-tiled N-split GEMM
+  const uint32_t flags = T <= 128 ? NVR_FLAG_STREAM : NVR_FLAG_SPLIT_N;
+  return router_impl(x, dt, T, D, W_fp4, W_scales, w_gsa, N, nullptr, 1, 1.0f, flags, nullptr, nullptr, out,
+                     out_dt == NVR_BF16, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 nvr_status nvr_set_profile_events(void* const* events, int n_pairs) {

@@ -64,7 +64,8 @@ struct GemmParams {
   float routed_scaling;
   int32_t* out_ids;
   float* out_w;
-  float* logits;               // debug: write [T, N] logits instead of the top-k
+  void* logits;                // logits mode: write [T, N] logits (fp32, or bf16) instead of the top-k
+  int logits_bf16;
   float4* partials;            // [m_tiles * n_splits][128][KMAX]
   uint32_t* tickets;           // [m_tiles]
   uint32_t* status;
@@ -270,11 +271,29 @@ gemm_topk_kernel(const __grid_constant__ GemmParams p) {
         tmem_load32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * 128 + c * 32, v);
         const int n0 = j * 128 + c * 32;
         if (p.logits) {
-          if (active) {
+          // the warp's 32 rows x 32 columns through its own 4 KB of s_lg,
+          // transposed (element (r, c) at r * 32 + (c ^ r): conflict-free both
+          // ways), so that each store covers 32 consecutive columns of a row
+          float* tr = s_lg + (etid >> 5) * 1024;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (n0 + i < p.N) p.logits[token * p.N + n0 + i] = __fmul_rn(v[i], gscale);
+          for (int i = 0; i < 32; ++i) tr[lane * 32 + (i ^ lane)] = __fmul_rn(v[i], gscale);
+          __syncwarp();
+          const int64_t row0 = static_cast<int64_t>(m_tile) * 128 + quarter * 32;
+          const int n = n0 + lane;
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r) {
+            const float l = tr[r * 32 + (lane ^ r)];
+            if (row0 + r < p.T && n < p.N) {
+              const size_t o = static_cast<size_t>(row0 + r) * p.N + n;
+              if (p.logits_bf16) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(l);
+                reinterpret_cast<__nv_bfloat16*>(p.logits)[o] = h;
+              } else {
+                reinterpret_cast<float*>(p.logits)[o] = l;
+              }
+            }
           }
+          __syncwarp();
         } else {
           // Pass 1 (unrolled, branch-free): the exact key of every column of
           // the chunk; the logits go to this thread's column of s_lg.  A
@@ -550,8 +569,8 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
                             int64_t T, int64_t D, const uint8_t* W_codes, const uint8_t* W_sf,
                             const float* w_gsa, int64_t N, const float* bias, int k,
                             float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
-                            float* logits, float4* partials, uint32_t* tickets, uint32_t* status,
-                            const GemmPlan& g, bool test_stall, cudaStream_t s) {
+                            void* logits, bool logits_bf16, float4* partials, uint32_t* tickets,
+                            uint32_t* status, const GemmPlan& g, bool test_stall, cudaStream_t s) {
   GemmParams p;
   if (!encode_codes_map(&p.tmap_a, x_codes, T, D)) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes_map(&p.tmap_b, W_codes, N, D)) return NVR_ERR_UNSUPPORTED;
@@ -559,7 +578,7 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
   p.T = static_cast<int>(T); p.N = static_cast<int>(N); p.D = static_cast<int>(D); p.k = k;
   p.raw = raw ? 1 : 0; p.n_splits = g.n_splits; p.n_tiles = g.n_tiles;
   p.routed_scaling = routed_scaling;
-  p.out_ids = out_ids; p.out_w = out_w; p.logits = logits;
+  p.out_ids = out_ids; p.out_w = out_w; p.logits = logits; p.logits_bf16 = logits_bf16 ? 1 : 0;
   p.partials = partials; p.tickets = tickets; p.status = status;
   p.test_stall = test_stall ? 1 : 0;
   const int grid = g.m_tiles * g.n_splits;

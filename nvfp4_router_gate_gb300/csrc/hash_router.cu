@@ -48,8 +48,8 @@ extern "C" nvr_status router_hash_topk(const int32_t* token_ids, int64_t T, cons
                                        int64_t vocab, int64_t n_experts, int k, float routed_scaling,
                                        int32_t* out_ids, float* out_w, nvr_stream_t stream) {
   using namespace nvr;
-  if (!token_ids || !tid2eid || !out_ids || !out_w) return NVR_ERR_INVALID_ARG;
   if (T < 0 || vocab < 1 || n_experts < 1 || k < 1 || k > kMaxKmax || k > n_experts) return NVR_ERR_INVALID_ARG;
+  if (!tid2eid || (T > 0 && (!token_ids || !out_ids || !out_w))) return NVR_ERR_INVALID_ARG;
   if (vocab > (int64_t(1) << 40) || T > (int64_t(1) << 40)) return NVR_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(token_ids) | reinterpret_cast<uintptr_t>(tid2eid) |
        reinterpret_cast<uintptr_t>(out_ids) | reinterpret_cast<uintptr_t>(out_w)) & 3u)

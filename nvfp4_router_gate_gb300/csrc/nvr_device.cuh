@@ -501,6 +501,26 @@ struct TopK {
     }
   }
 
+  // The same for any power-of-two K: the element-wise better of list[j] and
+  // b[K-1-j] is bitonic and holds the K best; log2(K) half-cleaner stages
+  // sort it.
+  __device__ __forceinline__ void merge_sorted(const float (&bk)[K], const int (&bi)[K], const float (&bs)[K]) {
+    static_assert((K & (K - 1)) == 0, "merge_sorted needs a power-of-two list");
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const bool keep = topk_better(key[j], id[j], bk[K - 1 - j], bi[K - 1 - j]);
+      key[j] = keep ? key[j] : bk[K - 1 - j];
+      id[j] = keep ? id[j] : bi[K - 1 - j];
+      sc[j] = keep ? sc[j] : bs[K - 1 - j];
+    }
+#pragma unroll
+    for (int d = K / 2; d > 0; d >>= 1) {
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if ((j & d) == 0) cswap(key, id, sc, j, j + d);
+    }
+  }
+
   // Drop the best entry (shift the list up by one; the tail becomes empty).
   __device__ __forceinline__ void pop_front() {
 #pragma unroll

@@ -83,8 +83,23 @@ nvr_status launch_gemm_topk(const uint8_t* x_codes, const uint8_t* x_sf, const f
                             int64_t T, int64_t D, const uint8_t* W_codes, const uint8_t* W_sf,
                             const float* w_gsa, int64_t N, const float* bias, int k,
                             float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
-                            float* logits, float4* partials, uint32_t* tickets, uint32_t* status,
-                            const GemmPlan& g, bool test_stall, cudaStream_t s);
+                            void* logits, bool logits_bf16, float4* partials, uint32_t* tickets,
+                            uint32_t* status, const GemmPlan& g, bool test_stall, cudaStream_t s);
+
+// Few tokens (T <= 128), many outputs: the weight-streaming GEMM with the
+// token tile as the MMA's N (32, 64 or 128 columns), n_splits CTAs over the
+// 128-row weight tiles.  Top-k mode (out == null): per-token candidates
+// merged by the last CTA (partials: [128][n_splits * k] float4; tickets: the
+// ticket at word 0, per-token counts at words 64..191, per-token 32 64-bit
+// slot words at words 512..8703, all left at zero); logits mode: out [T, N] fp32
+// or bf16.  stream_splits: CTAs for N outputs.
+int stream_token_tile(int64_t T);
+int stream_splits(int64_t N, int num_sms);
+nvr_status launch_gemm_stream(const uint8_t* x_codes, const uint8_t* x_sf, const float* x_gsa, int64_t T, int64_t D,
+                              const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
+                              const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
+                              float* out_w, void* out, bool out_bf16, float4* partials, uint32_t* ticket,
+                              uint32_t* status, int n_splits, bool test_stall, cudaStream_t s);
 
 // Router for N <= 256: the GEMM split along K over S CTAs (fp32 partials in
 // the workspace), then the warp-per-token epilogue kernel.

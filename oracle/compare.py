@@ -48,6 +48,18 @@ def check_logits(gpu, L64, bound64):
     return int(np.count_nonzero(~(err <= logit_tolerance(L64, bound64))))
 
 
+def check_logits_bf16(gpu, L64, bound64):
+    """Logits stored as bf16 (round to nearest even of the float32 result):
+    the float32 value obeys the logit tolerance, and rounding it to bf16 moves
+    it by at most half a bf16 ulp, 2**-8 of its magnitude (8 significant
+    bits).  Returns the number of outputs outside |gpu - exact| <=
+    tol + 2**-8 * (|exact| + tol)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    tol = logit_tolerance(L64, bound64)
+    err = np.abs(gpu - L64)
+    return int(np.count_nonzero(~(err <= tol + 2.0 ** -8 * (np.abs(L64) + tol))))
+
+
 def _ulp32(v):
     v = np.abs(np.asarray(v, dtype=np.float32))
     return (np.nextafter(v, np.float32(np.inf)) - v).astype(np.float64)

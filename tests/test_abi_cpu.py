@@ -87,8 +87,11 @@ def test_host_argument_checks_without_gpu():
     st = L.router_gate_topk(fake, 7, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
                             fake, fake, fake, ws_n, None)
     assert st == nat.NVR_ERR_INVALID_ARG
-    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 128,
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 256,
                             fake, fake, fake, ws_n, None)
+    assert st == nat.NVR_ERR_INVALID_ARG
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0,
+                            nat.NVR_FLAG_STREAM | nat.NVR_FLAG_SPLIT_N, fake, fake, fake, ws_n, None)
     assert st == nat.NVR_ERR_INVALID_ARG
     # two kernel-choice flags at once
     st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0,
@@ -132,12 +135,33 @@ def test_host_argument_checks_without_gpu():
     assert L.router_gate_logits(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, nat.NVR_FLAG_RAW_LOGITS,
                                 fake, fake, ws_n, None) == nat.NVR_ERR_INVALID_ARG
     assert L.nvr_read_device_status(None, None, None) == nat.NVR_ERR_INVALID_ARG
-    # plan query: NULL rejected; otherwise a kernel sequence code 0-5 (0 on a
+    # NVFP4 linear: NULL or misaligned output, bad output dtype, small workspace
+    lw = L.nvfp4_linear_workspace_size(4, 256, 16)
+    assert lw >= ws_n
+    assert L.nvfp4_linear(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, nat.NVR_F32, fake, lw,
+                          None) == nat.NVR_ERR_INVALID_ARG
+    assert L.nvfp4_linear(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, odd, nat.NVR_F32, fake, lw,
+                          None) == nat.NVR_ERR_ALIGNMENT
+    assert L.nvfp4_linear(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, fake, 9, fake, lw,
+                          None) == nat.NVR_ERR_INVALID_ARG
+    assert L.nvfp4_linear(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, fake, nat.NVR_BF16, fake, 16,
+                          None) == nat.NVR_ERR_WORKSPACE
+    assert L.nvfp4_linear(fake, nat.NVR_BF16, 0, 256, fake, fake, fake, 16, fake, nat.NVR_BF16, fake, lw,
+                          None) == nat.NVR_OK
+    # hash router: NULL table, k > experts, misaligned ids, empty batch
+    assert L.router_hash_topk(fake, 4, None, 10, 8, 2, 1.0, fake, fake, None) == nat.NVR_ERR_INVALID_ARG
+    assert L.router_hash_topk(fake, 4, fake, 10, 1, 2, 1.0, fake, fake, None) == nat.NVR_ERR_INVALID_ARG
+    assert L.router_hash_topk(fake, 4, fake, 10, 8, 17, 1.0, fake, fake, None) == nat.NVR_ERR_INVALID_ARG
+    assert L.router_hash_topk(ctypes.c_void_p(0x10002), 4, fake, 10, 8, 2, 1.0, fake, fake, None) == \
+        nat.NVR_ERR_ALIGNMENT
+    assert L.router_hash_topk(fake, 0, fake, 10, 8, 2, 1.0, fake, fake, None) == nat.NVR_OK
+    assert L.router_hash_topk(None, 0, fake, 10, 8, 2, 1.0, None, None, None) == nat.NVR_OK
+    # plan query: NULL rejected; otherwise a kernel sequence code 0-6 (0 on a
     # thread that has not launched a router call)
     assert L.nvr_last_router_plan(None) == nat.NVR_ERR_INVALID_ARG
     plan = (ctypes.c_int * 4)()
     assert L.nvr_last_router_plan(plan) == nat.NVR_OK
-    assert 0 <= plan[0] <= 5 and plan[3] in (0, 1)
+    assert 0 <= plan[0] <= 6 and plan[3] in (0, 1)
 
 
 def test_workspace_counters_do_not_move_with_T():

@@ -185,3 +185,19 @@ def test_compare_accepts_near_tie_swap():
     w_sw = router.routed_weights(L, swapped, 2.5)
     res = compare.check_topk(swapped, w_sw, L, B, keys2, bias, 2.5)
     assert compare.topk_ok(res) and res["exempt_rows"] == 1, res
+
+
+def test_compare_bf16_logits_rule():
+    """bf16-stored logits: the oracle's float64 logits rounded to bf16 (an
+    independent RNE rounding, workloads.float32_to_bf16_bits) pass; a value
+    two bf16 ulps off fails; the float32 rule alone would reject bf16 output."""
+    import workloads as WL
+    L, B, *_ = _case(seed=5)
+    bits = WL.float32_to_bf16_bits(L.astype(np.float32))
+    g = WL.bf16_bits_to_float32(bits).astype(np.float64)
+    assert compare.check_logits_bf16(g, L, B) == 0
+    assert compare.check_logits(g, L, B) > 0
+    bad = bits.copy()
+    r, c = np.unravel_index(np.argmax(np.abs(L)), L.shape)
+    bad[r, c] = np.uint16(int(bad[r, c]) + 2)
+    assert compare.check_logits_bf16(WL.bf16_bits_to_float32(bad), L, B) == 1

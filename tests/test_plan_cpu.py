@@ -65,6 +65,19 @@ def test_other_sequences():
     assert p["sequence"] == "amax+quantize+splitn" and p["tile_rows"] == 128, p
     p = plan(4096, flags=_native.NVR_FLAG_SPLIT_N)
     assert p["sequence"] == "amax+quantize+splitn", p
+    # wide heads at up to 128 tokens stream the weight: token tiles of 32, 64
+    # or 128 MMA columns, one CTA per SM (at most one per 128-row weight tile)
+    for T, tn in ((1, 32), (32, 32), (33, 64), (64, 64), (65, 128), (128, 128)):
+        p = plan(T, n=129280)
+        assert (p["sequence"], p["tile_rows"], p["ctas_per_tile"]) == ("amax+quantize+stream", tn, SMS), (T, p)
+    assert plan(129, n=129280)["sequence"] == "amax+quantize+splitn"
+    p = plan(40, n=384)
+    assert (p["sequence"], p["tile_rows"], p["ctas_per_tile"]) == ("amax+quantize+stream", 64, 3), p
+    p = plan(100, flags=_native.NVR_FLAG_STREAM)
+    assert (p["sequence"], p["ctas_per_tile"]) == ("amax+quantize+stream", 2), p
+    assert plan(32, n=129280, flags=_native.NVR_FLAG_SPLIT_N)["sequence"] == "amax+quantize+splitn"
+    with pytest.raises(Exception):
+        plan(200, flags=_native.NVR_FLAG_STREAM)            # more tokens than one token tile
     # a forced split keeps 128-row tiles; 20 clusters of 8 are not resident at
     # once, so the amax kernel runs first
     p = plan(2560, flags=_native.NVR_FLAG_SPLIT_K_8)
@@ -121,7 +134,7 @@ def test_plan_query_rejects_bad_arguments():
         (64, 200, N, _native.NVR_BF16, 0, SMS, caps, BLOCKS, out),         # D % 64
         (64, D, 0, _native.NVR_BF16, 0, SMS, caps, BLOCKS, out),           # N < 1
         (64, D, N, 7, 0, SMS, caps, BLOCKS, out),                          # dtype
-        (64, D, N, _native.NVR_BF16, 128, SMS, caps, BLOCKS, out),         # unknown flag
+        (64, D, N, _native.NVR_BF16, 256, SMS, caps, BLOCKS, out),         # unknown flag
         (64, D, N, _native.NVR_BF16, _native.NVR_FLAG_FORCE_DECODE | _native.NVR_FLAG_FORCE_TENSOR_CORE,
          SMS, caps, BLOCKS, out),
         (64, D, N, _native.NVR_BF16, 0, 0, caps, BLOCKS, out),             # no SMs
