@@ -458,6 +458,8 @@ def extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic):
       adversarial  the T = 16384, E = 384 batch (x 235 MB > L2): tokens/s too;
       quantize     nvfp4_quantize_act on the prefill batch (x read once, codes
                    and scales written), four rotating inputs;
+      moe_gemm     nvfp4_moe_gemm on the prefill batch routed by the router
+                   (E = 256, k = 8) into experts of N = 512, and the combine;
       decode_kernel the decode router's own device duration at T = 1 (events
                    around every launch, so no overlap with its neighbours)."""
     import torch
@@ -526,6 +528,35 @@ def extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic):
     out["quantize"] = _hbm_entry(nbytes, ms, hbm, launches_per_call=2,
                                  note="amax kernel + quantize kernel; x read twice (second pass mostly from L2)")
     del xs, xp
+    torch.cuda.empty_cache()
+
+    # the grouped expert GEMM on the prefill batch, routed by the router
+    # itself (E = 256, k = 8): 256 experts of N = 512 outputs (0.53 GB packed,
+    # drawn on the device), y in bf16, then the weighted combine
+    pw = WL.WORKLOADS["prefill"]
+    xp = torch.from_numpy(WL.make_x(pw).view(np.int16)).view(torch.bfloat16).to(dev)
+    gate = R.RouterGate(torch.from_numpy(WL.make_w(pw).view(np.int16)).view(torch.bfloat16).to(dev),
+                        torch.from_numpy(WL.make_bias(pw)).to(dev), k=pw.k, routed_scaling=pw.routed_scaling,
+                        max_tokens=pw.T)
+    ids, wts = gate(xp)
+    E, Nx = pw.N, 512
+    We = (torch.randn((E, Nx, pw.D), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    Ef, Esf, Eg = R.nvfp4_pack_experts(We)
+    del We
+    torch.cuda.empty_cache()
+    wsm = R.new_workspace(R.nvfp4_moe_gemm_workspace_size(pw.T, pw.D, E, pw.k), dev)
+    y = torch.empty((pw.T, pw.k, Nx), dtype=torch.bfloat16, device=dev)
+    comb = torch.empty((pw.T, Nx), dtype=torch.float32, device=dev)
+    ms = _timed_calls(lambda i: R.nvfp4_moe_gemm(xp, ids, Ef, Esf, Eg, y=y, workspace=wsm), 20, stream)
+    nbytes = E * Nx * (pw.D // 2 + pw.D // 16) + pw.T * pw.D * 2 + pw.T * pw.k * (4 + Nx * 2)
+    out["moe_gemm"] = _hbm_entry(nbytes, ms, hbm, tokens_per_s=pw.T / (ms / 1e3),
+                                 tensor_tflops=2 * pw.T * pw.k * pw.D * Nx / (ms / 1e3) / 1e12,
+                                 note="nvfp4_moe_gemm T=4096 routed k=8 over E=256 experts of N=512, D=7168, "
+                                      "bf16 y; 5 launches (amax, quantize, route, gather, grouped GEMM)")
+    ms = _timed_calls(lambda i: R.nvfp4_moe_combine(y, wts, out=comb), 50, stream)
+    nbytes = pw.T * pw.k * (Nx * 2 + 4) + pw.T * Nx * 4
+    out["moe_combine"] = _hbm_entry(nbytes, ms, hbm)
+    del Ef, Esf, y, xp, gate
     torch.cuda.empty_cache()
 
     # the decode kernel's own device duration at T = 1 (graph-free, events

@@ -374,6 +374,59 @@ nvr_status nvfp4_linear(const void* x, nvr_dtype dt, int64_t T, int64_t D, const
                         void* workspace, size_t ws_bytes, nvr_stream_t stream);
 
 /*
+ * nvfp4_moe_gemm -- the NVFP4 grouped expert GEMM fed by the router: every
+ * routed (token, slot) pair is one row of expert ids[t, j]'s linear layer,
+ *   y[t, j, n] = quantize(x)[t] . W_{ids[t,j]}[n]
+ * with both operands dequantized (codes x block scales x global scales) and
+ * fp32 accumulation on the tensor cores.
+ *
+ * Source: "nvfp4-megamoe-kernel commit df05289: dsv4/layers/grouped_linear.py"
+ * (grouped NVFP4 linear: the groups' rows flattened into one tensor quantized
+ * with one runtime global scale in one pass; expert offsets computed on the
+ * GPU with no host synchronisation; pre-allocated buffers) and "commit
+ * 04cf8ca: dsv4/layers/router.py", runtime-gsa section (Nvfp4GroupedLinear,
+ * Nvfp4MoE).  x's global scale is max|x| / 2688 over x (each token is routed
+ * k >= 1 times, so the flattened rows have the same maximum).
+ *
+ *   x          [T, D] activations (bf16 or fp32 per dt)
+ *   ids        [T, k] int32 expert ids (router_gate_topk's out_ids); a pair
+ *              whose id is outside [0, n_experts) gets a zero row
+ *   W_fp4      [n_experts * N, D/2] the experts' packed weights stacked (expert
+ *              e at rows e*N..), each from nvfp4_pack_weight of its [N, D]
+ *   W_scales   their scale bytes, NVR_SF_TILED over the n_experts * N rows
+ *              (expert e's nvr_sf_bytes(N, D, NVR_SF_TILED) bytes at
+ *              e * nvr_sf_bytes(N, D, NVR_SF_TILED))
+ *   w_gsa      [n_experts] the experts' global scales
+ *   N          outputs per expert, a multiple of 128; n_experts <= 1024
+ *   y          out [T, k, N] fp32 (y_dt NVR_F32) or bf16 (NVR_BF16), 16-byte
+ *              aligned
+ *   workspace  nvfp4_moe_gemm_workspace_size(T, D, n_experts, k) bytes,
+ *              zeroed once
+ * Five kernels, no host synchronisation: amax, quantize, a one-CTA routing
+ * kernel (expert counts, 128-row padded segments, work units), a gather of
+ * each segment row's codes and scales, and the grouped GEMM (each expert's
+ * weight tiles as the MMA's M, 128 of its token rows as N).  The rows of one
+ * expert are processed in an unspecified order; each output row is
+ * independent of it, so results are deterministic.
+ */
+size_t nvfp4_moe_gemm_workspace_size(int64_t T_max, int64_t D, int64_t n_experts, int k);
+nvr_status nvfp4_moe_gemm(const void* x, nvr_dtype dt, int64_t T, int64_t D, const int32_t* ids, int k,
+                          int64_t n_experts, const uint8_t* W_fp4, const uint8_t* W_scales, const float* w_gsa,
+                          int64_t N, void* y, nvr_dtype y_dt, void* workspace, size_t ws_bytes,
+                          nvr_stream_t stream);
+
+/*
+ * nvfp4_moe_combine -- out[t, n] = sum_j w[t, j] * y[t, j, n], j in order
+ * (fp32 fused multiply-adds): the router's weights (out_w) applied to the
+ * grouped GEMM's rows.  y [T, k, N] fp32 or bf16 per y_dt, w [T, k] fp32,
+ * out [T, N] fp32; N a multiple of 4; y and out 16-byte aligned.  One kernel,
+ * no workspace.  No counterpart on the pages beyond the weighted sum the
+ * router's weights exist for.
+ */
+nvr_status nvfp4_moe_combine(const void* y, nvr_dtype y_dt, int64_t T, int k, int64_t N, const float* w,
+                             float* out, nvr_stream_t stream);
+
+/*
  * router_gate_logits -- test hook: the same quantization and gate GEMM as
  * router_gate_topk, writing the fp32 logits [T, N] (row-major,
  * logit = acc * gsa_x * gsa_w) instead of the epilogue's outputs.  Used to

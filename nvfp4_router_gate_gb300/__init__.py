@@ -14,6 +14,8 @@ Functions (same names as include/nvfp4_router.h):
 * ``router_hash_topk(token_ids, tid2eid, n_experts, routed_scaling)`` -> (ids, weights)
 * ``nvfp4_linear(x, W_fp4, W_sf, w_gsa, out_dtype=torch.float32)`` -> out [T, N]
   (``Nvfp4Linear`` keeps the packed weight and a workspace resident)
+* ``nvfp4_pack_experts(W [E, N, D])``, ``nvfp4_moe_gemm(x, ids, W_fp4, W_sf, w_gsa)`` -> y [T, k, N],
+  ``nvfp4_moe_combine(y, w)`` -> out [T, N]
 * ``router_gate_workspace_size``, ``router_gate_x_gsa``, ``nvfp4_quantize_workspace_size``,
   ``nvr_sf_bytes``, ``nvr_read_device_status``
 
@@ -35,7 +37,8 @@ __all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "route
            "nvr_read_device_status", "last_router_plan", "plan_router", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
            "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "NVR_FLAG_SPLIT_K_2",
            "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "NVR_FLAG_STREAM", "new_workspace",
-           "nvfp4_linear", "nvfp4_linear_workspace_size", "Nvfp4Linear"]
+           "nvfp4_linear", "nvfp4_linear_workspace_size", "Nvfp4Linear", "nvfp4_pack_experts",
+           "nvfp4_moe_gemm", "nvfp4_moe_gemm_workspace_size", "nvfp4_moe_combine"]
 
 _LAYOUTS = {"linear": _native.NVR_SF_LINEAR, "tiled": _native.NVR_SF_TILED}
 
@@ -207,6 +210,63 @@ class Nvfp4Linear:
             raise ValueError("batch of %d tokens exceeds max_tokens=%d" % (T, self.max_tokens))
         return nvfp4_linear(x, self.W_fp4, self.W_sf, self.w_gsa, out=self.out[:T], workspace=self.workspace,
                             stream=stream)
+
+
+def nvfp4_pack_experts(W):
+    """Load-time NVFP4 quantization of E expert weights W [E, N, D] (N a
+    multiple of 128) into the stacked layout nvfp4_moe_gemm reads: codes
+    [E * N, D/2], tile-layout scales over the E * N rows, w_gsa [E] (each
+    expert with its own global scale)."""
+    E, N, D = W.shape
+    dev = W.device
+    codes = torch.empty((E * N, D // 2), dtype=torch.uint8, device=dev)
+    per = nvr_sf_bytes(N, D, "tiled")
+    sf = torch.empty(E * per, dtype=torch.uint8, device=dev)
+    gsa = torch.empty(E, dtype=torch.float32, device=dev)
+    ws = new_workspace(nvfp4_quantize_workspace_size(N, D), dev)
+    for e in range(E):
+        nvfp4_pack_weight(W[e], W_fp4=codes[e * N:(e + 1) * N], W_sf=sf[e * per:(e + 1) * per],
+                          w_gsa=gsa[e:e + 1], workspace=ws)
+    return codes, sf, gsa
+
+
+def nvfp4_moe_gemm_workspace_size(T_max, D, n_experts, k):
+    return int(_native.lib().nvfp4_moe_gemm_workspace_size(T_max, D, n_experts, k))
+
+
+def nvfp4_moe_gemm(x, ids, W_fp4, W_sf, w_gsa, out_dtype=torch.float32, y=None, workspace=None, stream=None):
+    """Grouped expert GEMM of the routed pairs: y [T, k, N] (fp32 or bf16) with
+    y[t, j] = quantize(x)[t] . W_{ids[t, j]}^T."""
+    T, D = x.shape
+    k = ids.shape[1]
+    E = w_gsa.shape[0]
+    N = W_fp4.shape[0] // E
+    dev = x.device
+    if ids.dtype != torch.int32:
+        raise TypeError("ids must be int32")
+    if y is None:
+        y = torch.empty((T, k, N), dtype=out_dtype, device=dev)
+    if workspace is None:
+        workspace = new_workspace(nvfp4_moe_gemm_workspace_size(T, D, E, k), dev)
+    code = _native.NVR_BF16 if y.dtype == torch.bfloat16 else _native.NVR_F32
+    st = _native.lib().nvfp4_moe_gemm(
+        _dev(x, "x"), _dtype_code(x), T, D, _dev(ids, "ids"), k, E, _dev(W_fp4, "W_fp4"), _dev(W_sf, "W_sf"),
+        _dev(w_gsa, "w_gsa"), N, _dev(y, "y"), code, _dev(workspace, "workspace"), workspace.numel(),
+        _stream(stream))
+    _native.check("nvfp4_moe_gemm", st)
+    return y
+
+
+def nvfp4_moe_combine(y, w, out=None, stream=None):
+    """out [T, N] fp32 = sum_j w[t, j] * y[t, j, :] (j in order)."""
+    T, k, N = y.shape
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float32, device=y.device)
+    code = _native.NVR_BF16 if y.dtype == torch.bfloat16 else _native.NVR_F32
+    st = _native.lib().nvfp4_moe_combine(_dev(y, "y"), code, T, k, N, _dev(w, "w"), _dev(out, "out"),
+                                         _stream(stream))
+    _native.check("nvfp4_moe_combine", st)
+    return out
 
 
 def router_hash_topk(token_ids, tid2eid, n_experts, routed_scaling=1.0, out_ids=None, out_w=None, stream=None):

@@ -60,6 +60,9 @@ SIGNATURES = {
     "router_hash_topk": (_i32, [_p, _i64, _p, _i64, _i64, _i32, _f32, _p, _p, _p]),
     "nvfp4_linear_workspace_size": (_sz, [_i64, _i64, _i64]),
     "nvfp4_linear": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _p, _i32, _p, _sz, _p]),
+    "nvfp4_moe_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32]),
+    "nvfp4_moe_gemm": (_i32, [_p, _i32, _i64, _i64, _p, _i32, _i64, _p, _p, _p, _i64, _p, _i32, _p, _sz, _p]),
+    "nvfp4_moe_combine": (_i32, [_p, _i32, _i64, _i32, _i64, _p, _p, _p]),
     "router_gate_logits": (_i32, [_p, _i32, _i64, _i64, _p, _p, _p, _i64, _u32, _p, _p, _sz, _p]),
     "nvr_read_device_status": (_i32, [_p, _p, ctypes.POINTER(_i32)]),
     "nvr_set_profile_events": (_i32, [_p, _i32]),

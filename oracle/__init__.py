@@ -41,4 +41,4 @@ which is "parity unpinned" beyond the floating-point error bound used in
 documented).
 """
 
-from . import formats, quantize, gemm, router, compare, pipeline  # noqa: F401
+from . import formats, quantize, gemm, router, compare, pipeline, hash_router, moe  # noqa: F401

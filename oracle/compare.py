@@ -60,6 +60,21 @@ def check_logits_bf16(gpu, L64, bound64):
     return int(np.count_nonzero(~(err <= tol + 2.0 ** -8 * (np.abs(L64) + tol))))
 
 
+def check_moe_combine(gpu_out, y64, bound64, w):
+    """out[t, n] = sum_j w[t, j] y[t, j, n] against the oracle's float64 y:
+    each term carries its y's logit tolerance times |w|, and the float32
+    chain of k fused multiply-adds adds at most k roundings of the running
+    sum (2**-23 of sum_j |w y| is a generous bound).  Returns the number of
+    outputs outside it."""
+    y64 = np.asarray(y64, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    ref = np.einsum("tj,tjn->tn", w, y64)
+    tol = np.einsum("tj,tjn->tn", np.abs(w), logit_tolerance(y64, bound64))
+    tol += 2.0 ** -23 * y64.shape[1] * np.einsum("tj,tjn->tn", np.abs(w), np.abs(y64))
+    err = np.abs(np.asarray(gpu_out, dtype=np.float64) - ref)
+    return int(np.count_nonzero(~(err <= tol)))
+
+
 def _ulp32(v):
     v = np.abs(np.asarray(v, dtype=np.float32))
     return (np.nextafter(v, np.float32(np.inf)) - v).astype(np.float64)
