@@ -23,6 +23,7 @@ step reads its input from L2), plus
   other_rooflines  the wide-N raw head (k = 8 and 1), the adversarial large
                 batch (tokens/s), the standalone quantizer and the decode
                 kernel's own duration, each against the measured HBM copy rate;
+  no_cooperative  the same steps launched with NVR_FLAG_NO_COOPERATIVE;
   cpu_baseline  the CPU oracle on a bounded sample of the same batch;
   clocks        SM clocks and throttle reasons sampled during the timed region.
 
@@ -264,6 +265,28 @@ def run_gpu(args, rank, world, local_rank):
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / args.steps
     value = job_throughput(world, T, args.steps, ms)
+    plan["cooperative"] = int(_native.lib().nvr_router_cooperative_state())
+
+    # the same steps without the cooperative launch (NVR_FLAG_NO_COOPERATIVE:
+    # for a caller that owns the GPU; the next call's launch then overlaps the
+    # previous call's tail)
+    n_nc = max(3, min(args.steps, 2000))
+
+    def step_nc(i):
+        R.router_gate_topk(xs[i % NBUF], W_fp4, W_sf, w_gsa, bias, w.k, w.routed_scaling,
+                           out_ids=ids[i % NBUF], out_w=wts[i % NBUF], workspace=ws,
+                           flags=R.NVR_FLAG_NO_COOPERATIVE)
+    for i in range(3):
+        step_nc(i)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n_nc):
+        step_nc(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    nc_ms = e0.elapsed_time(e1) / n_nc
+    no_coop = {"ms_per_step": nc_ms, "tokens_per_s": T / (nc_ms / 1e3), "steps": n_nc,
+               "hbm_frac": algorithmic(w, T, "fused")[0] / (nc_ms / 1e3) / 1e9 / load_peaks()[0]}
 
     # per-kernel pass (events between the launches)
     names = kernel_names("tc")
@@ -422,7 +445,8 @@ def run_gpu(args, rank, world, local_rank):
                    "plan": plan,
                    "parallelism": "replicas" if world > 1 else "single"},
         "e2e": e2e, "gpu_launches": len(names) * args.steps, "roofline": roof, "kernels": kernels,
-        "decode": decode, "other_rooflines": extra, "cpu_baseline": cpu, "clocks": clocks,
+        "no_cooperative": no_coop, "decode": decode, "other_rooflines": extra, "cpu_baseline": cpu,
+        "clocks": clocks,
     }
 
 

@@ -120,6 +120,17 @@ enum {
    * N, the weight is read once, per-token top-k lists are merged across CTAs.
    * The default for heads of more than 256 experts at T <= 128. */
   NVR_FLAG_STREAM = 128u,
+  /* The one-launch prefill router is launched cooperatively by default (the
+   * runtime then guarantees that its whole grid is resident at once, which
+   * its grid barrier needs even while other streams' kernels hold SMs; see
+   * nvr_router_cooperative_state).  A cooperative grid cannot start while the
+   * previous kernel of the stream is still draining, which costs about 3 us
+   * per call back to back on a GB300.  This flag launches it as an ordinary
+   * programmatic dependent launch instead: for callers that know no other
+   * work holds the SMs during the call (the host's occupancy check and the
+   * barriers' bounded waits are then the only safeguards; a wait that runs
+   * out records NVR_ERR_TIMEOUT in the workspace). */
+  NVR_FLAG_NO_COOPERATIVE = 256u,
   /* Failure-detection test hook (with FORCE_TENSOR_CORE or a SPLIT flag): the tensor-core
    * kernel's MMA issuer issues nothing, so its bounded waits run out after
    * about one second; the kernel stores NVR_ERR_TIMEOUT in the workspace
@@ -150,6 +161,23 @@ const char* nvr_last_cuda_error(void);
  * No counterpart on the pages: a diagnostic for tests and benchmarks.
  * NVR_ERR_INVALID_ARG for a NULL out. */
 nvr_status nvr_last_router_plan(int* out);
+
+/* Whether the one-launch prefill router (plan sequence 2) is launched
+ * cooperatively on the current device: 1 yes (the runtime guarantees that its
+ * whole grid is resident at once, which its grid barrier needs, also next to
+ * other kernels), -1 the runtime refused the cooperative attribute together
+ * with programmatic launch and clusters (the host's occupancy check and the
+ * barriers' bounded waits remain), 0 not known yet (found out on the first
+ * one-launch call outside stream capture).  No counterpart on the pages. */
+int nvr_router_cooperative_state(void);
+
+/* nvr_test_occupy -- test hook (no counterpart on the pages): launches n_ctas
+ * CTAs on `stream` that each hold smem_bytes of shared memory (at most 227 KB)
+ * and return by themselves after duration_ns (at most one second; a
+ * %globaltimer deadline and an iteration cap), so that a test can run router
+ * calls while other work holds the SMs.  NVR_ERR_INVALID_ARG outside those
+ * bounds. */
+nvr_status nvr_test_occupy(int n_ctas, int smem_bytes, uint64_t duration_ns, nvr_stream_t stream);
 
 /* nvr_plan_router -- the launch plan router_gate_topk would choose for a call
  * of T >= 1 tokens (dtype dt, hidden D, N experts, flags as for

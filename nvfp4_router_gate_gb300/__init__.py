@@ -30,13 +30,13 @@ import torch
 from . import _native
 from ._native import (NVR_FLAG_FORCE_DECODE, NVR_FLAG_FORCE_TENSOR_CORE, NVR_FLAG_RAW_LOGITS,
                       NVR_FLAG_SPLIT_K_2, NVR_FLAG_SPLIT_K_4, NVR_FLAG_SPLIT_K_8, NVR_FLAG_SPLIT_N,
-                      NVR_FLAG_STREAM, RouterError)
+                      NVR_FLAG_STREAM, NVR_FLAG_NO_COOPERATIVE, RouterError)
 
 __all__ = ["nvfp4_quantize_act", "nvfp4_pack_weight", "router_gate_topk", "router_gate_logits", "router_hash_topk",
            "router_gate_workspace_size", "router_gate_x_gsa", "nvfp4_quantize_workspace_size", "nvr_sf_bytes",
            "nvr_read_device_status", "last_router_plan", "plan_router", "RouterGate", "RouterError", "NVR_FLAG_RAW_LOGITS",
            "NVR_FLAG_FORCE_TENSOR_CORE", "NVR_FLAG_FORCE_DECODE", "NVR_FLAG_SPLIT_K_2",
-           "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "NVR_FLAG_STREAM", "new_workspace",
+           "NVR_FLAG_SPLIT_K_4", "NVR_FLAG_SPLIT_K_8", "NVR_FLAG_SPLIT_N", "NVR_FLAG_STREAM", "NVR_FLAG_NO_COOPERATIVE", "new_workspace",
            "nvfp4_linear", "nvfp4_linear_workspace_size", "Nvfp4Linear", "nvfp4_pack_experts",
            "nvfp4_moe_gemm", "nvfp4_moe_gemm_workspace_size", "nvfp4_moe_combine"]
 
@@ -343,6 +343,13 @@ class RouterGate:
             router_gate_workspace_size(self.max_tokens, self.D, self.N, self.k), dev)
         self.ids = torch.empty((self.max_tokens, self.k), dtype=torch.int32, device=dev)
         self.weights = torch.empty((self.max_tokens, self.k), dtype=torch.float32, device=dev)
+
+    def status(self, stream=None):
+        """The workspace status word (0 ok, 6 = a device-side bounded wait of
+        some call timed out and its outputs are unspecified).  Reads device
+        memory and waits for the stream: call it outside graph capture, e.g.
+        every few steps; re-zero the workspace after a timeout."""
+        return nvr_read_device_status(self.workspace, stream)
 
     def __call__(self, x, flags=0, stream=None):
         T = x.shape[0]

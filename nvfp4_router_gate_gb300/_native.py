@@ -31,6 +31,7 @@ NVR_FLAG_SPLIT_K_4 = 16
 NVR_FLAG_SPLIT_K_8 = 32
 NVR_FLAG_SPLIT_N = 64
 NVR_FLAG_STREAM = 128
+NVR_FLAG_NO_COOPERATIVE = 256
 NVR_FLAG_TEST_STALL = 1 << 30
 
 _p = ctypes.c_void_p
@@ -45,6 +46,8 @@ SIGNATURES = {
     "nvr_status_string": (ctypes.c_char_p, [_i32]),
     "nvr_last_cuda_error": (ctypes.c_char_p, []),
     "nvr_last_router_plan": (_i32, [ctypes.POINTER(_i32)]),
+    "nvr_router_cooperative_state": (_i32, []),
+    "nvr_test_occupy": (_i32, [_i32, _i32, ctypes.c_uint64, _p]),
     "nvr_plan_router": (_i32, [_i64, _i64, _i64, _i32, _u32, _i32, ctypes.POINTER(_i32), _i32,
                                ctypes.POINTER(_i32)]),
     "nvr_sf_bytes": (_sz, [_i64, _i64, _i32]),

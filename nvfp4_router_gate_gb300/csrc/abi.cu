@@ -111,6 +111,19 @@ nvr_status cuda_status(cudaError_t e) {
   return NVR_ERR_CUDA;
 }
 
+// Test hook kernel: holds its SM's shared memory for a bounded time
+// (%globaltimer deadline, and an iteration cap), then returns by itself.
+__global__ void occupy_kernel(uint64_t ns) {
+  extern __shared__ uint8_t held[];
+  const uint64_t t0 = globaltimer_ns();
+  const uint32_t cap = static_cast<uint32_t>(ns / 500) + 1000;
+  for (uint32_t it = 0; it < cap; ++it) {
+    if (globaltimer_ns() - t0 >= ns) break;
+    __nanosleep(500);
+  }
+  if (threadIdx.x == 0) held[0] = 1;
+}
+
 }  // namespace nvr
 
 using namespace nvr;
@@ -181,7 +194,7 @@ constexpr uint32_t kKernelFlags =
 // FORCE_TENSOR_CORE; NVR_ERR_INVALID_ARG for unknown or conflicting flags.
 nvr_status normalize_flags(uint32_t& flags) {
   if (flags & ~static_cast<uint32_t>(NVR_FLAG_RAW_LOGITS | NVR_FLAG_FORCE_TENSOR_CORE | NVR_FLAG_FORCE_DECODE |
-                                     kKernelFlags | NVR_FLAG_TEST_STALL))
+                                     kKernelFlags | NVR_FLAG_TEST_STALL | NVR_FLAG_NO_COOPERATIVE))
     return NVR_ERR_INVALID_ARG;
   const uint32_t kernel_flags = flags & kKernelFlags;
   if (kernel_flags & (kernel_flags - 1)) return NVR_ERR_INVALID_ARG;          // at most one
@@ -375,7 +388,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
                              one_launch ? reinterpret_cast<uint32_t*>(w + kWsFusedAmax) : nullptr,
                              one_launch ? reinterpret_cast<uint32_t*>(w + L.tile_sync) : nullptr, flat, T, D, W_fp4,
                              W_sf, w_gsa, N, bias, k, routed_scaling, raw, out_ids, out_w, logits, partials, status,
-                             rp.per_tile, rp.tile_rows, stall, s);
+                             rp.per_tile, rp.tile_rows, stall, (flags & NVR_FLAG_NO_COOPERATIVE) == 0, s);
     prof.after();
     return st;
   }
@@ -440,6 +453,17 @@ nvr_status nvr_plan_router(int64_t T, int64_t D, int64_t N, nvr_dtype dt, uint32
   out[2] = rp.per_tile;
   out[3] = rp.clustered ? 1 : 0;
   return NVR_OK;
+}
+
+int nvr_router_cooperative_state(void) { return fused_cooperative_state(); }
+
+nvr_status nvr_test_occupy(int n_ctas, int smem_bytes, uint64_t duration_ns, nvr_stream_t stream) {
+  if (n_ctas < 1 || n_ctas > 65536 || smem_bytes < 0 || smem_bytes > 227 * 1024 || duration_ns > 1000000000ull)
+    return NVR_ERR_INVALID_ARG;
+  cudaError_t e = cudaFuncSetAttribute(occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return cuda_status(e);
+  occupy_kernel<<<n_ctas, 32, smem_bytes, reinterpret_cast<cudaStream_t>(stream)>>>(duration_ns);
+  return cuda_status(cudaGetLastError());
 }
 
 nvr_status nvr_last_router_plan(int* out) {

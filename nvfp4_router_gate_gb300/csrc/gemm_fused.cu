@@ -919,12 +919,16 @@ int fused_cluster_capacity(int S) {
   return n;
 }
 
+// per device: 0 unknown, 1 the runtime accepts the cooperative attribute with
+// the router's others, -1 it refused it
+static int g_fused_coop[kMaxDevices] = {};
+
 nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync,
                                uint32_t* tile_sync, bool flat, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
-                               int tile_rows, bool test_stall, cudaStream_t s) {
+                               int tile_rows, bool test_stall, bool cooperative, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVR_ERR_CUDA;
   if (N > 256 || k > kMaxKmax || S < 1 || S > 16 || 128 % S) return NVR_ERR_UNSUPPORTED;
@@ -946,22 +950,65 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   g.k = k; g.raw = raw ? 1 : 0; g.routed_scaling = routed_scaling;
   g.out_ids = out_ids; g.out_w = out_w; g.logits = logits;
   g.status = status; g.test_stall = test_stall ? 1 : 0;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;           // the S K-splits of a token tile
-  attr[1].val.clusterDim.x = S;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[3];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  if (!flat) {                            // without clusters the tiles meet at tile_barrier
+    attr[na].id = cudaLaunchAttributeClusterDimension;         // the S K-splits of a token tile
+    attr[na].val.clusterDim.x = S;
+    attr[na].val.clusterDim.y = 1;
+    attr[na++].val.clusterDim.z = 1;
+  }
+  // With the in-kernel max|x| every CTA waits at a grid barrier (and without
+  // clusters a tile's CTAs at a workspace barrier): a cooperative launch has
+  // the runtime guarantee that the whole grid is resident at once, also next
+  // to other kernels on other streams, instead of the host's occupancy
+  // estimate alone.  Whether the runtime takes it together with programmatic
+  // launch and clusters is found out once per device, on a call outside
+  // stream capture (a launch the runtime refuses returns an error and runs
+  // nothing); until then, and where it is refused, the launch is ordinary and
+  // the barriers' bounded waits remain the safeguard.
+  int* coop_ok = g_fused_coop;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool capturing = cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone;
+  const bool try_coop = cooperative && amax_sync && (coop_ok[dev] == 1 || (coop_ok[dev] == 0 && !capturing));
+  if (try_coop) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na++].val.cooperative = 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((T + tile_rows - 1) / tile_rows * S));
   cfg.blockDim = dim3(kFThreads);
   cfg.dynamicSmemBytes = kFSmem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = flat ? 1 : 2;            // without clusters the tiles meet at tile_barrier
-  return cuda_status(tile_rows == 112 ? cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<112>, g)
-                                      : cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<128>, g));
+  cfg.numAttrs = na;
+  auto launch = [&]() {
+    return tile_rows == 112 ? cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<112>, g)
+                            : cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<128>, g);
+  };
+  cudaError_t e2 = launch();
+  if (try_coop && coop_ok[dev] == 0) {
+    if (e2 == cudaSuccess) {
+      coop_ok[dev] = 1;
+    } else {
+      cudaGetLastError();                  // the refused launch ran nothing
+      coop_ok[dev] = -1;
+      cfg.numAttrs = na - 1;
+      e2 = launch();
+    }
+  }
+  return cuda_status(e2);
+}
+
+// 1 when the one-launch router's launches carry the cooperative attribute on
+// the current device, -1 when the runtime refused it, 0 before the first
+// one-launch call outside stream capture.
+int fused_cooperative_state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return g_fused_coop[dev];
 }
 
 }  // namespace nvr

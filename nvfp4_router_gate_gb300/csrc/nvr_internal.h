@@ -126,12 +126,13 @@ nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64
 // fused_block_capacity(): CTAs it holds at once without clusters.
 int fused_cluster_capacity(int S);
 int fused_block_capacity();
+int fused_cooperative_state();
 nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uint32_t* amax_sync,
                                uint32_t* tile_sync, bool flat, int64_t T, int64_t D,
                                const uint8_t* W_codes, const uint8_t* W_sf, const float* w_gsa, int64_t N,
                                const float* bias, int k, float routed_scaling, bool raw, int32_t* out_ids,
                                float* out_w, float* logits, float* partials, uint32_t* status, int S,
-                               int tile_rows, bool test_stall, cudaStream_t s);
+                               int tile_rows, bool test_stall, bool cooperative, cudaStream_t s);
 nvr_status launch_router_epilogue(const float* partials, int S, const float* x_gsa, const float* w_gsa,
                                   int64_t T, int64_t N, const float* bias, int k, float routed_scaling,
                                   bool raw, int32_t* out_ids, float* out_w, float* logits, cudaStream_t s);

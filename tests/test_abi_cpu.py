@@ -87,7 +87,7 @@ def test_host_argument_checks_without_gpu():
     st = L.router_gate_topk(fake, 7, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
                             fake, fake, fake, ws_n, None)
     assert st == nat.NVR_ERR_INVALID_ARG
-    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 256,
+    st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 512,
                             fake, fake, fake, ws_n, None)
     assert st == nat.NVR_ERR_INVALID_ARG
     st = L.router_gate_topk(fake, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0,

@@ -659,3 +659,52 @@ def test_fused_quantizer_codes_production_plan():
             err = np.abs(g - L)
             assert np.all(err <= 1e-6 * np.abs(L)), (c0, np.argwhere(err > 1e-6 * np.abs(L))[:5])
         assert len(plans) == 1 and dict(next(iter(plans)))["sequence"] == "fused", plans
+
+
+def test_fused_router_next_to_kernels_holding_sms():
+    """Half the SMs held by another stream's kernel (200 KB of shared memory
+    each, released by itself after 20 ms) while the one-launch prefill router
+    starts: its grid cannot all be resident until they return.  The call must
+    complete with status OK and route like the oracle; a cooperative launch
+    (when the runtime accepts it) waits for the whole grid, else the grid
+    barrier's bounded wait absorbs the delay."""
+    import nvfp4_router_gate_gb300 as R
+    from nvfp4_router_gate_gb300 import _native
+    w = WL.WORKLOADS["prefill"]
+    case = Case(w)
+    ws = R.new_workspace(R.router_gate_workspace_size(w.T, w.D, w.N, w.k))
+    R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, w.k, w.routed_scaling,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    other = torch.cuda.Stream()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    lib = _native.lib()
+    for _ in range(2):
+        _native.check("nvr_test_occupy",
+                      lib.nvr_test_occupy(sms // 2, 200 * 1024, 20_000_000, ctypes_stream(other)))
+        ids, wts = R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, w.k,
+                                      w.routed_scaling, workspace=ws)
+        torch.cuda.synchronize()
+        assert R.last_router_plan()["sequence"] == "fused"
+        assert R.nvr_read_device_status(ws) == 0
+        res = case.check(ids.cpu().numpy(), wts.cpu().numpy(), np.arange(w.T))
+        assert compare.topk_ok(res), res
+    assert lib.nvr_router_cooperative_state() in (1, -1)
+    print("cooperative launch state:", lib.nvr_router_cooperative_state())
+
+
+def ctypes_stream(s):
+    import ctypes
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def test_no_cooperative_flag_routes_identically():
+    """NVR_FLAG_NO_COOPERATIVE changes only how the one-launch router is
+    launched: ids and weights are bit-identical to the default call's."""
+    import nvfp4_router_gate_gb300 as R
+    w = WL.WORKLOADS["prefill"]
+    case = Case(w.with_T(2048))
+    a_ids, a_w = case.run(0)
+    b_ids, b_w = case.run(R.NVR_FLAG_NO_COOPERATIVE)
+    assert R.last_router_plan()["sequence"] == "fused"
+    assert np.array_equal(a_ids, b_ids) and np.array_equal(a_w.view(np.uint32), b_w.view(np.uint32))

@@ -134,7 +134,7 @@ def test_plan_query_rejects_bad_arguments():
         (64, 200, N, _native.NVR_BF16, 0, SMS, caps, BLOCKS, out),         # D % 64
         (64, D, 0, _native.NVR_BF16, 0, SMS, caps, BLOCKS, out),           # N < 1
         (64, D, N, 7, 0, SMS, caps, BLOCKS, out),                          # dtype
-        (64, D, N, _native.NVR_BF16, 256, SMS, caps, BLOCKS, out),         # unknown flag
+        (64, D, N, _native.NVR_BF16, 512, SMS, caps, BLOCKS, out),         # unknown flag
         (64, D, N, _native.NVR_BF16, _native.NVR_FLAG_FORCE_DECODE | _native.NVR_FLAG_FORCE_TENSOR_CORE,
          SMS, caps, BLOCKS, out),
         (64, D, N, _native.NVR_BF16, 0, 0, caps, BLOCKS, out),             # no SMs
