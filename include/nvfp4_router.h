@@ -329,11 +329,14 @@ nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
  * It runs the single-launch decode kernel only (T <= 16 and a shape whose
  * per-CTA plan fits; otherwise NVR_ERR_UNSUPPORTED); flags may be 0 or
  * NVR_FLAG_RAW_LOGITS.  Its scratch (keys and scores of every (token, expert)
- * pair plus a ticket) lives in a fixed 1 MiB array in the library's device
- * memory, held by every GPU that loads the library until the process exits;
- * calls with T * N * 8 bytes > 1 MiB - 256 are rejected with
- * NVR_ERR_WORKSPACE.  It calls no cudaMalloc/cudaFree; it clears the ticket
- * with cudaMemsetAsync on `stream` before its launch.
+ * pair plus a ticket) lives in a fixed array of 224 KiB + 256 bytes in the
+ * library's device memory, held by every GPU that loads the library until
+ * the process exits.  That is the most the decode kernel's shared-memory plan
+ * lets a call need (T * N * 8 bytes of keys and scores, the same bound); a
+ * larger shape is refused by the plan (NVR_ERR_UNSUPPORTED).  It calls no
+ * cudaMalloc/cudaFree.  Each call is two operations on `stream`: a
+ * cudaMemsetAsync that clears the 256 control bytes (the ticket), then the
+ * decode kernel.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) and caches it; make that first call before any
  *   stream capture.

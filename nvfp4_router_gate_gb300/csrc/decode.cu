@@ -34,7 +34,6 @@ constexpr int kDecodeThreads = 256;
 // for a single token the cluster barriers cost more than the sharing saves.)
 constexpr int kMaxDecodeCluster = 4;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
-constexpr int kDecodeMaxSmem = 224 * 1024;
 
 struct DecodeParams {
   const void* x;

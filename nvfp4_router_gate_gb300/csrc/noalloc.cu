@@ -22,10 +22,14 @@
 namespace {
 
 // Scratch of the allocation-free entry point: 256 bytes of control words
-// (the ticket at byte 8), then keys and scores [T, N] fp32.  Every GPU that
-// loads the library holds this memory until the process exits.
-constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;     // 1 MiB
+// (the ticket at byte 8), then keys and scores [T, N] fp32.  The decode plan
+// only accepts shapes whose T * N * 8 bytes of keys and scores fit one CTA's
+// shared-memory plan (kDecodeMaxSmem), so that much after the control words
+// holds every call the plan accepts.  Every GPU that loads the library holds
+// this memory (224 KiB + 256 bytes) until the process exits.
 constexpr size_t kNoAllocControl = 256;
+constexpr size_t kNoAllocScratchBytes = kNoAllocControl + nvr::kDecodeMaxSmem;
+static_assert(kNoAllocScratchBytes % 256 == 0, "the keys start 256-byte aligned");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_setup_mutex;
@@ -71,14 +75,15 @@ extern "C" nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int6
       (bias && (reinterpret_cast<uintptr_t>(bias) & a4)) || (reinterpret_cast<uintptr_t>(out_ids) & a4) ||
       (reinterpret_cast<uintptr_t>(out_w) & a4))
     return NVR_ERR_ALIGNMENT;
-  // keys and scores of every (token, expert) pair must fit the fixed array
-  if (static_cast<size_t>(T) * static_cast<size_t>(N) * 8 > kNoAllocScratchBytes - kNoAllocControl)
-    return NVR_ERR_WORKSPACE;
   if (T == 0) return NVR_OK;
   const int sms = device_sm_count();
   if (sms <= 0) return NVR_ERR_CUDA;
   const DecodePlan dp = plan_decode(T, D, N, sms, dt == NVR_BF16);
   if (!dp.ok) return NVR_ERR_UNSUPPORTED;
+  // the keys and scores of every (token, expert) pair fit the fixed array for
+  // every shape the decode plan accepts; checked all the same
+  if (static_cast<size_t>(T) * static_cast<size_t>(N) * 8 > kNoAllocScratchBytes - kNoAllocControl)
+    return NVR_ERR_WORKSPACE;
   cudaError_t e = cudaSuccess;
   uint8_t* scratch = scratch_for_current_device(&e);
   if (!scratch) return NVR_ERR_CUDA;

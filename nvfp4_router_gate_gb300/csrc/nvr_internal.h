@@ -41,7 +41,11 @@ struct GemmPlan {
 };
 GemmPlan plan_gemm(int64_t T, int64_t N, int num_sms);
 
-// Decode (single-launch) path limits and plan.
+// Decode (single-launch) path limits and plan.  A decode CTA's shared memory
+// (at most kDecodeMaxSmem) holds the keys and scores of every (token, expert)
+// pair, T * N * 8 bytes, so a shape the plan accepts never needs more scratch
+// for them than that.
+constexpr int kDecodeMaxSmem = 224 * 1024;
 struct DecodePlan {
   bool ok = false;
   int tmax = 0;        // template bucket >= T
