@@ -429,14 +429,15 @@ nvr_status nvfp4_linear(const void* x, nvr_dtype dt, int64_t T, int64_t D, const
  *              e * nvr_sf_bytes(N, D, NVR_SF_TILED))
  *   w_gsa      [n_experts] the experts' global scales
  *   N          outputs per expert, a multiple of 128; n_experts <= 1024
- *   y          out [T, k, N] fp32 (y_dt NVR_F32) or bf16 (NVR_BF16), 16-byte
- *              aligned
+ *   y          out [T, k, N] fp32 (y_dt NVR_F32) or bf16 (NVR_BF16)
+ * x, ids, W_fp4, W_scales and y must be 16-byte aligned (NVR_ERR_ALIGNMENT).
  *   workspace  nvfp4_moe_gemm_workspace_size(T, D, n_experts, k) bytes,
  *              zeroed once
- * Five kernels, no host synchronisation: amax, quantize, a one-CTA routing
- * kernel (expert counts, 128-row padded segments, work units), a gather of
- * each segment row's codes and scales, and the grouped GEMM (each expert's
- * weight tiles as the MMA's M, 128 of its token rows as N).  The rows of one
+ * Four kernels, no host synchronisation: amax, a one-CTA routing kernel
+ * (expert counts, 128-row padded segments, work units), a quantizer that
+ * stores each token's codes and scales into its k expert-sorted rows, and the
+ * grouped GEMM (each expert's weight tiles as the MMA's M, 128 of its token
+ * rows as N).  The rows of one
  * expert are processed in an unspecified order; each output row is
  * independent of it, so results are deterministic.
  */

@@ -10,17 +10,19 @@
 // dsv4/layers/router.py" (the same runtime gsa in Nvfp4GroupedLinear and
 // Nvfp4MoE).
 //
-// One call, five kernels chained with programmatic dependent launch, no host
+// One call, four kernels chained with programmatic dependent launch, no host
 // synchronisation and no allocation:
-//   amax, quantize   x's runtime gsa and its NVFP4 codes / scales (x once: a
-//                    token routed to k experts has the same codes in all k
-//                    rows, and the k copies share x's max|x|);
-//   moe_route        one CTA: expert counts (shared-memory atomics), each
-//                    expert's segment of rows padded to a multiple of 128, the
-//                    list of (expert, 128-row token tile) work units and every
-//                    routed pair's row -- the expert offsets stay on the GPU;
-//   moe_gather       the codes and scale bytes of every row of the segments,
-//                    in the tensor-core tile layout (padding rows zero);
+//   amax             x's runtime gsa (x once: the k copies of a token routed
+//                    to k experts share x's max|x|);
+//   moe_route        one CTA: expert counts (warp-aggregated shared-memory
+//                    atomics), each expert's segment of rows padded to a
+//                    multiple of 128, the list of (expert, 128-row token tile)
+//                    work units and every routed pair's row -- the expert
+//                    offsets stay on the GPU;
+//   moe_quantize_scatter  x's NVFP4 codes and scale bytes (the standalone
+//                    quantizer's arithmetic), each block quantized once and
+//                    stored into the token's k segment rows, scales in the
+//                    tensor-core tile layout;
 //   moe_gemm         the weight-streaming GEMM of gemm_stream.cu per work unit:
 //                    the expert's 128-row weight tiles are the MMA's M, the
 //                    unit's 128 token rows its N; the epilogue stores
@@ -44,14 +46,14 @@ constexpr int kMSmem = kMStages * kMStage + 512 /*rows*/ + 1024 /*barriers*/ + 1
 static_assert(kMStage % 1024 == 0 && kMSmem <= 227 * 1024, "shared-memory plan");
 
 // --------------------------------------------------------------- routing
-// ctl[0]: work units, ctl[1]: rows of all segments.
+// Each routed pair's rank inside its expert's group (ids outside [0, E): -1),
+// the segments (start, count), the work units; ctl[0]: work units, ctl[1]:
+// rows of all segments.
 __global__ void __launch_bounds__(kRouteThreads)
-moe_route_kernel(const int32_t* __restrict__ ids, int n_pairs, int E, int N, int32_t* __restrict__ pos_of,
-                 int32_t* __restrict__ row_of, uint32_t* __restrict__ seg_start, uint32_t* __restrict__ seg_count,
-                 uint32_t* __restrict__ units, uint32_t* __restrict__ ctl, void* __restrict__ y, int y_bf16) {
+moe_route_kernel(const int32_t* __restrict__ ids, int n_pairs, int E, int32_t* __restrict__ rank_of_pair,
+                 uint32_t* __restrict__ seg_start, uint32_t* __restrict__ seg_count, uint32_t* __restrict__ units,
+                 uint32_t* __restrict__ ctl) {
   __shared__ uint32_t cnt[kMoeMaxExperts];
-  __shared__ uint32_t start[kMoeMaxExperts];
-  __shared__ uint32_t ubase[kMoeMaxExperts];
   __shared__ uint32_t wpad[32], wtile[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the ids may come from the router kernel just before
@@ -60,11 +62,27 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n_pairs, int E, int N, int
   for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0u;
   __syncthreads();
   // each routed pair's rank inside its expert's group (the order inside a
-  // group does not affect any output row)
-  for (int i = tid; i < n_pairs; i += kRouteThreads) {
-    const int e = __ldg(ids + i);
-    pos_of[i] = (e >= 0 && e < E) ? static_cast<int32_t>(atomicAdd(&cnt[e], 1u)) : -1;
+  // group does not affect any output row); the ids are read as 16-byte
+  // vectors, eight per thread in flight at once (ids and pos_of are 16-byte
+  // aligned: checked on the host)
+  const int n4 = n_pairs / 4;
+  const int4* ids4 = reinterpret_cast<const int4*>(ids);
+  int4* pos4 = reinterpret_cast<int4*>(rank_of_pair);
+  auto rank_of = [&](int e) { return (e >= 0 && e < E) ? static_cast<int>(atomicAdd(&cnt[e], 1u)) : -1; };
+  for (int q0 = tid; q0 < n4; q0 += 8 * kRouteThreads) {
+    int4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + u * kRouteThreads;
+      v[u] = q < n4 ? __ldg(ids4 + q) : make_int4(-1, -1, -1, -1);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + u * kRouteThreads;
+      if (q < n4) pos4[q] = make_int4(rank_of(v[u].x), rank_of(v[u].y), rank_of(v[u].z), rank_of(v[u].w));
+    }
   }
+  for (int i = 4 * n4 + tid; i < n_pairs; i += kRouteThreads) rank_of_pair[i] = rank_of(__ldg(ids + i));
   __syncthreads();
   // exclusive scans over the experts (one per thread, E <= 1024) of the
   // padded segment sizes and of the token tiles
@@ -92,57 +110,96 @@ moe_route_kernel(const int32_t* __restrict__ ids, int n_pairs, int E, int N, int
   const uint32_t base_p = (warp ? wpad[warp - 1] : 0u) + ip - pad;
   const uint32_t base_t = (warp ? wtile[warp - 1] : 0u) + it - tiles;
   if (tid < E) {
-    start[tid] = base_p;
-    ubase[tid] = base_t;
     seg_start[tid] = base_p;
     seg_count[tid] = c;
     for (uint32_t u = 0; u < tiles; ++u) units[base_t + u] = (static_cast<uint32_t>(tid) << 16) | u;
-    for (uint32_t p = base_p + c; p < base_p + pad; ++p) row_of[p] = -1;      // padding rows
   }
   if (tid == 0) {
     ctl[0] = wtile[31];
     ctl[1] = wpad[31];
   }
-  __syncthreads();
-  for (int i = tid; i < n_pairs; i += kRouteThreads) {
-    const int r = pos_of[i];
-    if (r >= 0) {
-      const uint32_t p = start[__ldg(ids + i)] + static_cast<uint32_t>(r);
-      pos_of[i] = static_cast<int32_t>(p);
-      row_of[p] = i;
-    } else {
-      // an id outside [0, E): the pair's output row is zero
-      for (int n = 0; n < N; ++n) {
-        if (y_bf16) reinterpret_cast<uint16_t*>(y)[static_cast<size_t>(i) * N + n] = 0;
-        else reinterpret_cast<float*>(y)[static_cast<size_t>(i) * N + n] = 0.0f;
-      }
-    }
-  }
 }
 
-// ---------------------------------------------------------------- gather
-// One warp per segment row p < ctl[1]: the codes of token t = row_of[p] / k
-// (D/2 bytes) and its scale bytes into row p, scales in the tile layout;
-// padding rows get zeros.
+// ------------------------------------------------------- quantize-scatter
+// x quantized once per 16-element block pair (the standalone quantizer's
+// arithmetic: identical codes and scale bytes) and stored into each of the
+// token's k segment rows, seg_start[ids[t, j]] + rank: codes at [row, D/2],
+// scale bytes in the tile layout; the thread of the row's first blocks also
+// records the row's pair (row_of).  Rows of padding keep whatever they held
+// (zero or an earlier call's finite codes; row_of is never read there): they
+// only feed accumulator columns that are never stored.  A pair whose id is
+// outside [0, E) gets a zero output row (each thread zeroes a slice).
+template <bool kBF16>
 __global__ void __launch_bounds__(256)
-moe_gather_kernel(const uint8_t* __restrict__ xc, const uint8_t* __restrict__ xsf, const int32_t* __restrict__ row_of,
-                  const uint32_t* __restrict__ ctl, int k, int D, uint8_t* __restrict__ pc, uint8_t* __restrict__ psf) {
+moe_quantize_scatter_kernel(const void* __restrict__ x, int T, int D, int k, const float* __restrict__ qrec,
+                            const int32_t* __restrict__ ids, const int32_t* __restrict__ rank_of_pair,
+                            const uint32_t* __restrict__ seg_start, int32_t* __restrict__ row_of, uint8_t* __restrict__ pc,
+                            uint8_t* __restrict__ psf, void* __restrict__ y, int N, int y_bf16) {
+  __shared__ float s_rcp[128];                 // RN(1 / dec(b)) for scale bytes b
+  if (threadIdx.x < 128) {
+    const uint32_t b = threadIdx.x;
+    s_rcp[b] = (b >= 1 && b <= 126) ? __frcp_rn(e4m3_value(b)) : 0.0f;
+  }
+  __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int lane = threadIdx.x & 31;
-  const int64_t n_rows = __ldcg(ctl + 1);
   const int KB = D / kBlock;
-  const int nv = D / 32;                         // 16-byte vectors of a code row
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-  for (int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; p < n_rows; p += warps) {
-    const int32_t pair = __ldcg(row_of + p);
-    const int64_t t = pair >= 0 ? pair / k : -1;
-    const uint4* src = reinterpret_cast<const uint4*>(xc + t * (D / 2));
-    uint4* dst = reinterpret_cast<uint4*>(pc + p * (D / 2));
-    for (int v = lane; v < nv; v += 32) dst[v] = t >= 0 ? __ldcg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-    for (int g = lane; g < KB / 4; g += 32) {
-      const uint32_t s = t >= 0 ? __ldcg(reinterpret_cast<const uint32_t*>(xsf + t * KB) + g) : 0u;
-      *reinterpret_cast<uint32_t*>(psf + sf_tile_offset(p, 4 * g, KB)) = s;
+  const int pairs_per_row = KB / 2;
+  const int64_t n_thr = static_cast<int64_t>(T) * pairs_per_row;
+  QuantScale qs;
+  qs.gsa = __ldg(qrec);
+  qs.rgsa = __ldg(qrec + 1);
+  qs.mode = __float_as_int(__ldg(qrec + 2));
+  for (int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; g0 < n_thr;
+       g0 += static_cast<int64_t>(gridDim.x) * blockDim.x) {   // block-uniform trip count
+    const int64_t g = g0 + threadIdx.x;
+    const bool live = g < n_thr;
+    const int64_t t = live ? g / pairs_per_row : 0;
+    const int c = live ? 2 * static_cast<int>(g - t * pairs_per_row) : 0;    // first block of the pair
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t b0 = 0, b1 = 0;
+    if (live) {
+      Block16 blk;
+      const size_t e0 = static_cast<size_t>(t) * D + static_cast<size_t>(c) * kBlock;
+      load_block16<kBF16>(x, e0, blk);
+      b0 = quant_block16_bracket(blk, qs, q.x, q.y, s_rcp);
+      load_block16<kBF16>(x, e0 + kBlock, blk);
+      b1 = quant_block16_bracket(blk, qs, q.z, q.w, s_rcp);
+    }
+    // blocks 4c'..4c'+3 of a row are 4 consecutive bytes of one tile line:
+    // the even lane of each pair of lanes writes them (KB % 4 == 0, so both
+    // lanes hold the same row)
+    const uint32_t o = __shfl_down_sync(0xFFFFFFFFu, b0 | (b1 << 8), 1);
+    if (live) {
+      // the k destination rows first: all id and rank loads in flight at once
+      int32_t rk[kMaxKmax], ex[kMaxKmax];
+#pragma unroll
+      for (int j = 0; j < kMaxKmax; ++j) {
+        rk[j] = j < k ? __ldg(rank_of_pair + t * k + j) : -1;
+        ex[j] = j < k ? __ldg(ids + t * k + j) : 0;
+      }
+      int64_t row[kMaxKmax];
+#pragma unroll
+      for (int j = 0; j < kMaxKmax; ++j) row[j] = rk[j] >= 0 ? static_cast<int64_t>(__ldg(seg_start + ex[j])) + rk[j] : -1;
+#pragma unroll
+      for (int j = 0; j < kMaxKmax; ++j) {
+        if (j >= k) break;
+        const int64_t pair = t * k + j, p = row[j];
+        if (p < 0) {
+          // an id outside [0, E): the pair's output row is zero
+          for (int n = c * 8; n < N; n += KB * 8) {      // slices of 16 outputs, KB / 2 threads per row
+            for (int u = 0; u < 16 && n + u < N; ++u) {
+              if (y_bf16) reinterpret_cast<uint16_t*>(y)[pair * N + n + u] = 0;
+              else reinterpret_cast<float*>(y)[pair * N + n + u] = 0.0f;
+            }
+          }
+          continue;
+        }
+        *reinterpret_cast<uint4*>(pc + static_cast<size_t>(p) * (D / 2) + static_cast<size_t>(c) * 8) = q;
+        if ((c & 3) == 0)
+          *reinterpret_cast<uint32_t*>(psf + sf_tile_offset(p, c, KB)) = b0 | (b1 << 8) | (o << 16);
+        if (c == 0) row_of[p] = static_cast<int32_t>(pair);
+      }
     }
   }
 }
@@ -411,7 +468,7 @@ size_t a256(size_t v) { return (v + 255) / 256 * 256; }
 // Workspace of a grouped GEMM call: the quantize layout (control words, amax
 // partials, x's quantizer record) then the routing tables and the rows.
 struct MoeWs {
-  size_t ctl, seg_start, seg_count, units, pos_of, row_of, xc, xsf, pc, psf, total;
+  size_t ctl, seg_start, seg_count, units, pos_of, row_of, pc, psf, total;
   int64_t rows_max;            // rows of all segments at most (128-padded)
 };
 
@@ -426,9 +483,7 @@ MoeWs moe_ws_layout(int64_t T, int64_t D, int64_t E, int k) {
   L.units = a256(L.seg_count + E * 4);
   L.pos_of = a256(L.units + ((pairs + 127) / 128 + E) * 4);
   L.row_of = a256(L.pos_of + pairs * 4);
-  L.xc = a256(L.row_of + L.rows_max * 4);
-  L.xsf = a256(L.xc + T * (D / 2));
-  L.pc = a256(L.xsf + T * (D / 16));
+  L.pc = a256(L.row_of + L.rows_max * 4);
   L.psf = a256(L.pc + L.rows_max * (D / 2));
   L.total = a256(L.psf + L.rows_max * (D / 16));
   return L;
@@ -462,7 +517,7 @@ extern "C" nvr_status nvfp4_moe_gemm(const void* x, nvr_dtype dt, int64_t T, int
   const uintptr_t a16 = 15u;
   if ((reinterpret_cast<uintptr_t>(x) & a16) || (reinterpret_cast<uintptr_t>(W_fp4) & a16) ||
       (reinterpret_cast<uintptr_t>(W_scales) & a16) || (reinterpret_cast<uintptr_t>(y) & a16) ||
-      (reinterpret_cast<uintptr_t>(ids) & 3u) || (reinterpret_cast<uintptr_t>(w_gsa) & 3u) ||
+      (reinterpret_cast<uintptr_t>(ids) & 15u) || (reinterpret_cast<uintptr_t>(w_gsa) & 3u) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return NVR_ERR_ALIGNMENT;
   const MoeWs L = moe_ws_layout(T, D, n_experts, k);
@@ -481,8 +536,6 @@ extern "C" nvr_status nvfp4_moe_gemm(const void* x, nvr_dtype dt, int64_t T, int
   cudaError_t e = launch_amax_bulk(x, bf16, T * D, reinterpret_cast<uint32_t*>(w + Q.amax_partials),
                                    reinterpret_cast<uint32_t*>(w + kWsAmaxTicket), x_gsa, qrec, status, sms, s);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_quantize(x, bf16, T, D, false, qrec, w + L.xc, w + L.xsf, s);
-  if (e != cudaSuccess) return cuda_status(e);
 
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -496,23 +549,30 @@ extern "C" nvr_status nvfp4_moe_gemm(const void* x, nvr_dtype dt, int64_t T, int
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, moe_route_kernel, ids, static_cast<int>(T * k), static_cast<int>(n_experts),
-                           static_cast<int>(N), reinterpret_cast<int32_t*>(w + L.pos_of),
-                           reinterpret_cast<int32_t*>(w + L.row_of), reinterpret_cast<uint32_t*>(w + L.seg_start),
-                           reinterpret_cast<uint32_t*>(w + L.seg_count), reinterpret_cast<uint32_t*>(w + L.units), ctl,
-                           y, y_dt == NVR_BF16 ? 1 : 0);
+                           reinterpret_cast<int32_t*>(w + L.pos_of), reinterpret_cast<uint32_t*>(w + L.seg_start),
+                           reinterpret_cast<uint32_t*>(w + L.seg_count), reinterpret_cast<uint32_t*>(w + L.units), ctl);
     if (e != cudaSuccess) return cuda_status(e);
   }
   {
+    const int64_t n_thr = T * (D / kBlock / 2);
+    int64_t grid = (n_thr + 255) / 256;
+    if (grid > static_cast<int64_t>(sms) * 32) grid = static_cast<int64_t>(sms) * 32;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sms * 8));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(256);
     cfg.stream = s;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, moe_gather_kernel, static_cast<const uint8_t*>(w + L.xc),
-                           static_cast<const uint8_t*>(w + L.xsf), static_cast<const int32_t*>(
-                               reinterpret_cast<int32_t*>(w + L.row_of)),
-                           static_cast<const uint32_t*>(ctl), k, static_cast<int>(D), w + L.pc, w + L.psf);
+    const int32_t* rk = reinterpret_cast<const int32_t*>(w + L.pos_of);
+    const uint32_t* ss = reinterpret_cast<const uint32_t*>(w + L.seg_start);
+    int32_t* ro = reinterpret_cast<int32_t*>(w + L.row_of);
+    const int yb = y_dt == NVR_BF16 ? 1 : 0, n32 = static_cast<int>(N), t32 = static_cast<int>(T),
+              d32 = static_cast<int>(D);
+    const float* qr = qrec;
+    e = bf16 ? cudaLaunchKernelEx(&cfg, moe_quantize_scatter_kernel<true>, x, t32, d32, k, qr, ids, rk, ss, ro,
+                                  w + L.pc, w + L.psf, y, n32, yb)
+             : cudaLaunchKernelEx(&cfg, moe_quantize_scatter_kernel<false>, x, t32, d32, k, qr, ids, rk, ss, ro,
+                                  w + L.pc, w + L.psf, y, n32, yb);
     if (e != cudaSuccess) return cuda_status(e);
   }
   MoeParams p;
