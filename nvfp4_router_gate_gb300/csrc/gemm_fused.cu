@@ -18,30 +18,36 @@
 // A token tile of 128 (or 112) rows is split along K over S CTAs (S = 1 to
 // 16, a power of two) that form one thread-block cluster, or, in a grid the
 // device holds at once without clusters, meet at a barrier in the workspace
-// (tile_barrier) before routing.  Per CTA (rank r, 320 threads):
-//   warp 0     TMA producer: per stage of 256 K-elements two bf16 x boxes
-//              (128 rows x 128 elements, 32 KB each) into a 3-slot ring, and
-//              the W tile (128 or 256 rows x 128 bytes, 128-byte swizzle) with
-//              its scale slabs into a 2-deep ring;
-//   warps 2-9  quantizers (quant_box): each warp takes 16 token rows of a box
-//              and writes their E2M1 codes into the A tile (128-byte swizzle,
-//              the layout TMA would have produced) and their scale bytes into
-//              the stage's scale atoms; the A tile is double-buffered and the
-//              warps synchronise only through mbarriers (a warp may run about
-//              a stage ahead of another);
-//   warp 1     MMA issuer: once all eight quantizer warps have filled the A
-//              slot, copies the stage's x and W scale atoms into tensor memory
-//              (tcgen05.cp, in order with the MMAs on the otherwise idle
-//              tensor pipe) and issues one tcgen05.mma.kind::mxf4nvf4 (M=128,
-//              N=128 or 256, K=64) per 64-element K step into one fp32
-//              accumulator;
-//   warps 2-9  after the last MMA: the fp32 partial (128 x 256) goes from
-//              tensor memory to partial plane r of the workspace (L2); after a
-//              cluster (or tile) barrier each CTA routes its own 128/S tokens
-//              from the S planes, one warp per token (TokenRouter,
-//              nvr_splitk.cuh).
-// Tensor memory: accumulator at columns 0-255; scales of A slot a at
-// 256 + 48 a (x: 4 columns per K step, W: 8).
+// (tile_barrier) before routing.  Per CTA (rank r, 576 threads):
+//   warp 0      TMA producer.  With the in-kernel max|x| it first streams the
+//               CTA's contiguous 1/G slice of x (bulk copies of 32 KB into a
+//               6-slot ring laid over the other rings), then per stage of 256
+//               K-elements two bf16 x boxes (128 rows x 128 elements, 32 KB
+//               each) into a 3-slot ring, and the W tile (128 or 256 rows x
+//               128 bytes, 128-byte swizzle) with its scale slabs into a
+//               2-deep ring;
+//   warps 2-17  quantizers (quant_box): warps 2-9 take the stage's first x
+//               box, warps 10-17 its second, 1/8 of the box rows per warp;
+//               they write the E2M1 codes into the A tile (128-byte swizzle,
+//               the layout TMA would have produced) and the scale bytes into
+//               the stage's scale atoms; the A tile is double-buffered and
+//               the warps synchronise only through mbarriers (a warp may run
+//               about a stage ahead of another);
+//   warp 1      MMA issuer: once all sixteen quantizer warps have filled the A
+//               slot, copies the stage's x and W scale atoms into tensor
+//               memory (tcgen05.cp, in order with the MMAs on the otherwise
+//               idle tensor pipe) and issues one tcgen05.mma.kind::mxf4nvf4
+//               (M=128, N=128 or 256, K=64) per 64-element K step into one
+//               fp32 accumulator;
+//   warps 2-17  after the last MMA: the fp32 partial (128 x 256) goes from
+//               tensor memory to partial plane r of the workspace (L2); after a
+//               cluster (or tile) barrier each CTA routes its own 128/S tokens
+//               from the S planes, one warp per token (TokenRouter,
+//               nvr_splitk.cuh).
+// The quantizers are bound by the integer pipe: sixteen warps reach the same
+// throughput per SM as eight, but leave half as many rows per warp for the
+// epilogue.  Tensor memory: accumulator at columns 0-255; scales of A slot a
+// at 256 + 48 a (x: 4 columns per K step, W: 8).
 #include <type_traits>
 
 #include "nvr_splitk.cuh"
@@ -65,9 +71,16 @@ constexpr int kFXRing = kFXSlots * kFXBox;
 constexpr int kFARing = kFASlots * kFASlot;
 constexpr int kFByteTab = 2560;                     // scale bytes of bf16 block maxima (amax down ~20 binades)
 constexpr int kFFixQ = 256;                         // exact-pass queue entries per quantizer warp and box (>= 32 x groups)
-constexpr int kFTables = 1024 + 1024 + kFByteTab + 8 * kFFixQ * 2;   // s_scale, s_cc, s_byte, s_fixq
+constexpr int kFQWarps = 16;                        // quantizer warps: 8 per x box, both boxes of a stage at once
+constexpr int kFQThreads = 32 * kFQWarps;
+constexpr int kFTables = 1024 + 1024 + kFByteTab + kFQWarps * kFFixQ * 2;   // s_scale, s_cc, s_byte, s_fixq
 constexpr int kFSmem = kFWRing + kFXRing + kFARing + kFTables + 512 /*barriers*/ + 1024 /*align*/;
-constexpr int kFThreads = 320;
+constexpr int kFThreads = 64 + kFQThreads;
+// The max|x| pass streams the CTA's contiguous slice of x in 32 KB chunks
+// through a ring over the W, x and A rings (all idle until the pass ends).
+constexpr int kFChunk = 32768;
+constexpr int kFChunkSlots = 6;
+static_assert(kFChunkSlots * kFChunk <= kFWRing + kFXRing + kFARing, "the chunk ring fits the three rings");
 // A token tile has kRows = 128 or 112 rows (the kernel is instantiated for
 // both): each of the eight quantizer warps takes kRows / 8 rows, that is
 // kRows / 16 row pairs, quantized as one group (their chains interleave).
@@ -78,6 +91,7 @@ static_assert(8 * 8192 <= kFXRing, "store staging fits the x ring");
 struct FusedParams {
   CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
   CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 x (128 * n_half)
+  const uint8_t* x;            // the same activations as bytes (the max|x| pass)
   float* qrec;                 // quantizer record {gsa, 1/gsa, mode, amax}: from the amax kernel, or
                                // published by this kernel's last CTA when amax_sync is set
   uint32_t* amax_sync;         // in-kernel amax: 5 workspace words (grid_amax), or null
@@ -403,8 +417,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   float2* s_scale = reinterpret_cast<float2*>(aring + kFARing);        // [128] (dec(b), RN(1/dec(b)))
   float2* s_cc = s_scale + 128;                                         // [128] (c_lo, c_hi) of byte b
   uint8_t* s_byte = reinterpret_cast<uint8_t*>(s_cc + 128);             // [kFByteTab] scale byte of a block max
-  uint16_t* s_fixq = reinterpret_cast<uint16_t*>(s_byte + kFByteTab);   // [8][kFFixQ] rows for the exact pass
-  uint64_t* full_w = reinterpret_cast<uint64_t*>(s_fixq + 8 * kFFixQ);
+  uint16_t* s_fixq = reinterpret_cast<uint16_t*>(s_byte + kFByteTab);   // [16][kFFixQ] rows for the exact pass
+  uint64_t* full_w = reinterpret_cast<uint64_t*>(s_fixq + kFQWarps * kFFixQ);
   uint64_t* empty_w = full_w + kFStagesW;
   uint64_t* full_x = empty_w + kFStagesW;
   uint64_t* empty_x = full_x + kFXSlots;
@@ -412,11 +426,13 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   uint64_t* q_done = a_empty + kFASlots;                               // [kFASlots]
   uint64_t* acc_full = q_done + kFASlots;
   uint64_t* amax_mbar = acc_full + 1;           // one-cluster grids: the S CTAs' maxima have landed
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(amax_mbar + 1);
+  uint64_t* full_c = amax_mbar + 1;             // [kFChunkSlots] max|x| pass chunk ring
+  uint64_t* empty_c = full_c + kFChunkSlots;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(empty_c + kFChunkSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   // producer: ring slots with a fill in flight and the parity of their latest fill
-  uint32_t filled_w = 0, bits_w = 0, filled_x = 0, bits_x = 0;
+  uint32_t filled_w = 0, bits_w = 0, filled_x = 0, bits_x = 0, filled_c = 0, bits_c = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x / p.S;
   const int rank = blockIdx.x - m_tile * p.S;
@@ -424,16 +440,22 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   const int n_st = (KB + 15) / 16;                   // stages of 256 K-elements
   const int st0 = (rank * n_st) / p.S;
   const int my_st = ((rank + 1) * n_st) / p.S - st0;
+  // the max|x| pass: CTA b reads bytes [c_beg, c_end) of x (16-byte multiples)
+  const uint64_t x_bytes = static_cast<uint64_t>(p.T) * static_cast<uint64_t>(p.D) * 2u;
+  const uint64_t c_per = ((x_bytes + gridDim.x - 1) / gridDim.x + 15u) & ~uint64_t(15);
+  const uint64_t c_beg = min(x_bytes, c_per * blockIdx.x), c_end = min(x_bytes, c_beg + c_per);
+  const int n_chunks = static_cast<int>((c_end - c_beg + kFChunk - 1) / kFChunk);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFStagesW; ++s) { mbar_init(full_w + s, 1); mbar_init(empty_w + s, 1); }
     for (int s = 0; s < kFXSlots; ++s) { mbar_init(full_x + s, 1); mbar_init(empty_x + s, 8); }
     for (int a = 0; a < kFASlots; ++a) {
       mbar_init(a_empty + a, 1);
-      mbar_init(q_done + a, 8);
+      mbar_init(q_done + a, kFQWarps);
     }
     mbar_init(acc_full, 1);
     mbar_init(amax_mbar, p.S);
+    for (int c = 0; c < kFChunkSlots; ++c) { mbar_init(full_c + c, 1); mbar_init(empty_c + c, kFQWarps); }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_map(&p.tmap_x);
@@ -484,10 +506,33 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     uint32_t wph = 0;
     bool ok = true;
     int xi = 0;                                        // x boxes issued so far
-    // with the in-kernel amax the CTA's boxes stream twice: for the max, then
-    // (from L2) for the GEMM; the second pass follows the first without a
-    // pause, its loads overlapping the grid barrier
-    for (int pass = p.amax_sync ? 0 : 1; pass < 2 && ok; ++pass)
+    // With the in-kernel amax, x streams twice: first the CTA's contiguous
+    // slice for the max (one pass over x in HBM), then, from L2, the CTA's
+    // boxes for the GEMM.  The second pass starts as soon as every chunk of
+    // the first has been consumed (the chunk ring overlays the other rings),
+    // its loads overlapping the grid barrier.
+    if (p.amax_sync) {
+      for (int c = 0; c < n_chunks; ++c) {
+        const int cs = c % kFChunkSlots;
+        const uint32_t cph = (c / kFChunkSlots) & 1;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_c + cs, cph ^ 1u, deadline, abort_flag))) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          const uint64_t off = c_beg + static_cast<uint64_t>(c) * kFChunk;
+          const uint32_t bytes = static_cast<uint32_t>(c_end - off < kFChunk ? c_end - off : kFChunk);
+          mbar_arrive_expect_tx(full_c + cs, bytes);
+          bulk_load(smem + cs * kFChunk, p.x + off, bytes, full_c + cs);
+        }
+        __syncwarp();
+        filled_c |= 1u << cs;
+        bits_c = (bits_c & ~(1u << cs)) | (cph << cs);
+      }
+      for (int cs = 0; cs < kFChunkSlots && ok; ++cs)
+        if ((filled_c >> cs) & 1u)
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_c + cs, (bits_c >> cs) & 1u, deadline, abort_flag));
+    }
     for (int s = 0; s < my_st && ok; ++s) {
       const int ks = st0 + s;
       // the stage's two x boxes (a box past D or T reads zeros)
@@ -507,7 +552,6 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         bits_x = (bits_x & ~(1u << xs)) | (xph << xs);
       }
       if (!ok) break;
-      if (pass == 0) continue;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_w + wst, wph ^ 1u, deadline, abort_flag))) {
         ok = false;
         break;
@@ -580,45 +624,47 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     // ---------------------------------------------------------- quantizers
     rt.init(p.bias, p.N, p.k, p.raw, p.routed_scaling, lane);       // for the epilogue
     const float w_gsa = __ldg(p.w_gsa);                               // off the path after the barrier
-    const int qw = warp - 2;
+    // quantizer warp q16 = warp - 2 takes the rows qw = q16 % 8 of box q16 / 8
+    // of every stage
+    const int q16 = warp - 2, qw = q16 & 7, qh = q16 >> 3;
     bool ok = true;
     int xi = 0;                                        // x boxes consumed so far
     if (p.amax_sync) {
       // ---- in-kernel amax: max |x| over this CTA's boxes (the same
       // bit-pattern max as the amax kernel), then the grid-wide record
       uint32_t m = 0;
-      const int sub = lane >> 4, l16 = lane & 15;
-      for (int s = 0; s < my_st && ok; ++s) {
-        for (int hs = 0; hs < 2; ++hs, ++xi) {
-          const int xs = xi % kFXSlots;
-          const uint32_t xph = (xi / kFXSlots) & 1;
-          const bool okx = __all_sync(0xFFFFFFFFu, mbar_wait(full_x + xs, xph, deadline, abort_flag));
-          ok = ok && okx;
-          if (okx) {
-            const uint8_t* xb = xring + xs * kFXBox + (qw * kFRowsPerWarp + sub) * 256 + 16 * l16;
-#pragma unroll
-            for (int i = 0; i < kFRowsPerWarp / 2; ++i)
-              m = max(m, absmax_bits16B<true>(ld_shared_v4(xb + 512 * i)));
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty_x + xs);
-          if (!okx) break;
+      for (int c = 0; c < n_chunks && ok; ++c) {
+        const int cs = c % kFChunkSlots;
+        const uint32_t cph = (c / kFChunkSlots) & 1;
+        const bool okc = __all_sync(0xFFFFFFFFu, mbar_wait(full_c + cs, cph, deadline, abort_flag));
+        ok = ok && okc;
+        if (okc) {
+          // warp q16 reads the chunk's 16-byte words q16 * 32 + lane + 512 i
+          const uint64_t left = c_end - c_beg - static_cast<uint64_t>(c) * kFChunk;
+          const uint32_t bytes = static_cast<uint32_t>(left < kFChunk ? left : kFChunk);
+          const uint8_t* cb = smem + cs * kFChunk;
+#pragma unroll 8
+          for (uint32_t o = (q16 * 32 + lane) * 16u; o < bytes; o += kFQThreads * 16u)
+            m = max(m, absmax_bits16B<true>(ld_shared_v4(cb + o)));
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_c + cs);
+        if (!okc) break;
       }
       m = __reduce_max_sync(0xFFFFFFFFu, m);
       uint32_t* s_wmax = reinterpret_cast<uint32_t*>(s_fixq);     // the queue is not in use yet
-      if (lane == 0) s_wmax[qw] = m;
-      ok = bar_and(3, 256, ok);
+      if (lane == 0) s_wmax[q16] = m;
+      ok = bar_and(3, kFQThreads, ok);
       bool gok = true;
       if (warp == 2 && ok) {                           // ok is the same in every thread
         uint32_t cm = 0;
-        for (int w = 0; w < 8; ++w) cm = max(cm, s_wmax[w]);
+        for (int w = 0; w < kFQWarps; ++w) cm = max(cm, s_wmax[w]);
         uint32_t bits = 0;
         if (one_cluster) {
           // my maximum into slot `rank` of every CTA, then an arrival on its
           // mbarrier (release: the store is visible first) -- lane r serves
           // CTA r, so the S round trips overlap; then wait for all S
-          uint32_t* s_cmax = reinterpret_cast<uint32_t*>(s_fixq) + 16;
+          uint32_t* s_cmax = reinterpret_cast<uint32_t*>(s_fixq) + 32;
           if (lane < p.S) {
             uint32_t slot, bar;
             asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(slot) : "r"(smem_u32(s_cmax + rank)), "r"(lane));
@@ -644,21 +690,21 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
           gok = grid_amax(p.amax_sync, cm, gridDim.x, bits, deadline, abort_flag);
         }
         if (lane == 0) {
-          s_wmax[8] = bits;
+          s_wmax[kFQWarps] = bits;
           if (!gok) {
             report_timeout(p.status);
             *abort_flag = 1;
           }
         }
       }
-      ok = bar_and(3, 256, ok && gok);                 // warp 2's outcome, for every warp
+      ok = bar_and(3, kFQThreads, ok && gok);          // warp 2's outcome, for every warp
     }
     // the quantizer record: derived here from the grid's max (the amax
     // kernel's arithmetic; CTA 0 also stores it), or the amax kernel's
     QuantScale qs;
     float amax;
     if (p.amax_sync) {
-      amax = __uint_as_float(reinterpret_cast<const uint32_t*>(s_fixq)[8]);
+      amax = __uint_as_float(reinterpret_cast<const uint32_t*>(s_fixq)[kFQWarps]);
       qs = make_quant_scale(amax);
       if (blockIdx.x == 0 && threadIdx.x == 64) {
         p.qrec[0] = qs.gsa;
@@ -680,11 +726,11 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     const uint32_t amax_b16 = __float_as_uint(amax) >> 16;                  // bf16 bits of amax
     if (qs.mode == 1) {
       const float r6 = 0.16666667163372039794921875f;       // RN(1/6)
-      const int qt = static_cast<int>(threadIdx.x) - 64;   // 0..255 over the quantizer warps
-      static_assert(kFByteTab % 256 == 0, "whole rounds of the table");
+      const int qt = static_cast<int>(threadIdx.x) - 64;   // 0..511 over the quantizer warps
+      static_assert(kFByteTab % kFQThreads == 0, "whole rounds of the table");
 #pragma unroll
-      for (int j = 0; j < kFByteTab / 256; ++j) {          // independent entries: their latencies overlap
-        const int i = qt + 256 * j;
+      for (int j = 0; j < kFByteTab / kFQThreads; ++j) {   // independent entries: their latencies overlap
+        const int i = qt + kFQThreads * j;
         const int b16 = static_cast<int>(amax_b16) - i;
         const float mx = __uint_as_float(static_cast<uint32_t>(max(b16, 0)) << 16);
         s_byte[i] = static_cast<uint8_t>(e4m3_byte(div_rn_short(div_rn(mx, qs.gsa, qs.rgsa), 6.0f, r6)));
@@ -695,7 +741,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
                                __fmul_rn(c, 1.00000095367431640625f));    // 1 + 2^-20
       }
     }
-    bar_and(2, 256, true);
+    bar_and(2, kFQThreads, true);
     QuantTables tb;
     tb.qs = qs;
     tb.s_scale = s_scale;
@@ -713,14 +759,15 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       }
       uint8_t* ac = aring + slot * kFASlot;
       uint8_t* asf = ac + kFACodes;
-#pragma unroll 1
-      for (int hs = 0; hs < 2; ++hs, ++xi) {
+      {
+        xi = 2 * s + qh;                               // box qh of the stage
         const int xs = xi % kFXSlots;
         const uint32_t xph = (xi / kFXSlots) & 1;
         const bool okx = __all_sync(0xFFFFFFFFu, mbar_wait(full_x + xs, xph, deadline, abort_flag));
         ok = ok && okx;
         if (okx) {
-          quant_box<kRows>(xring + xs * kFXBox, ac, asf, hs, qw, lane, p.T - m_tile * kRows, tb, s_fixq + qw * kFFixQ);
+          quant_box<kRows>(xring + xs * kFXBox, ac, asf, qh, qw, lane, p.T - m_tile * kRows, tb,
+                           s_fixq + q16 * kFFixQ);
         }
         // this warp has read its rows of the box
         __syncwarp();
@@ -737,7 +784,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     }
     // --------------------------------------------- wait for the accumulator
     if (my_st > 0) {
-      acc_ok = bar_and(1, 256, mbar_wait(acc_full, 0, deadline, abort_flag));
+      acc_ok = bar_and(1, kFQThreads, mbar_wait(acc_full, 0, deadline, abort_flag));
       if (!acc_ok && threadIdx.x == 64) {
         report_timeout(p.status);
         *abort_flag = 1;
@@ -748,10 +795,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     // stages the stores
     store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * 256, xring, tmem, warp, lane,
                        static_cast<int64_t>(m_tile) * kRows, min(kRows, p.T - m_tile * kRows), p.n_half,
-                       my_st > 0 && acc_ok);
-    // for the producer and MMA warps when they route too (warp 2 is done with
-    // its exact-pass queue, where the word sits)
-    if (threadIdx.x == 64) reinterpret_cast<float*>(s_fixq)[9] = gscale;
+                       my_st > 0 && acc_ok, kFQWarps);
   }
 
   // The S CTAs of this token tile form the cluster, or meet at the tile's
@@ -774,50 +818,41 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
 
   // ------------------------------- router epilogue for this CTA's tokens
   // rank r finishes tokens [r * rows/S, (r+1) * rows/S) of the tile.  Router
-  // warp rw takes tokens rw, rw + nrw, ... (up to NT at once, their latencies
-  // overlapping).  Usually the eight quantizer warps route (nrw = 8); with 17
-  // to 30 tokens per CTA the producer and MMA warps join in (nrw = 10), so that
-  // three token slots per warp suffice where eight warps would need four.
+  // warp rw (the quantizer warps) takes tokens rw, rw + 16, ..., one or two
+  // per call (their latencies overlapping).
   const int per = kRows / p.S;
-  const bool ten = per > 16 && per <= 30;
-  if (warp >= 2 || ten) {
-    if (warp < 2) {
-      rt.init(p.bias, p.N, p.k, p.raw, p.routed_scaling, lane);
-      gscale = reinterpret_cast<const float*>(s_fixq)[9];
-    }
-    const int rw = warp >= 2 ? warp - 2 : warp + 8;
-    const int nrw = ten ? 10 : 8;
-    // each warp's rows: the A ring (idle now) for the quantizer warps, the x
-    // ring (idle too) for the other two
-    float4* s_row = rw < 8 ? reinterpret_cast<float4*>(aring) + rw * 256
-                           : reinterpret_cast<float4*>(xring) + (rw - 8) * 256;
-    // with 8 or more partial planes (then at most 16 tokens per CTA and eight
-    // router warps) the W and x rings (contiguous, idle now) stage each warp's
-    // partial rows, all copied at once (measured: fewer planes are faster
-    // loaded directly): 16 KB per warp -- a valid slot n of a route call has
-    // 8 n < 128 / S, so its rows n * S + s stay below 16
-    float4* stage = p.S >= 8 ? reinterpret_cast<float4*>(wring) + rw * 1024 : nullptr;
-    static_assert(8 * 16384 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
+  if (warp >= 2) {
+    const int rw = warp - 2;
+    // with 8 or more partial planes (then at most 16 tokens per CTA: one per
+    // router warp) the W and x rings (contiguous, idle now) stage each warp's
+    // S partial rows, all copied at once (measured: fewer planes are faster
+    // loaded directly): S KB per warp with a token, rw < 128 / S; each warp's
+    // token slot (kRouteSlot float4) is then in the A ring, else its two
+    // slots are in the x ring (all idle now)
+    float4* stage = p.S >= 8 ? reinterpret_cast<float4*>(wring) + rw * p.S * 64 : nullptr;
+    static_assert(128 * 1024 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
+    static_assert(kFQWarps * kRouteSlot * 16 <= kFARing && 2 * kFQWarps * kRouteSlot * 16 <= kFXRing,
+                  "token slots fit the A ring (one per warp) and the x ring (two per warp)");
+    float4* s_row = p.S >= 8 ? reinterpret_cast<float4*>(aring) + rw * kRouteSlot
+                             : reinterpret_cast<float4*>(xring) + rw * 2 * kRouteSlot;
     const int64_t t0 = static_cast<int64_t>(m_tile) * kRows + static_cast<int64_t>(rank) * per;
     // as many token slots per call as the warp has tokens -- empty slots
     // would still be sorted
     const auto route_n = [&](auto nt) {
       constexpr int NT = decltype(nt)::value;
-      for (int i = rw; i < per; i += nrw * NT) {
+      for (int i = rw; i < per; i += kFQWarps * NT) {
         int64_t tt[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const int64_t t = t0 + i + nrw * n;
-          tt[n] = (i + nrw * n < per && t < p.T) ? t : -1;
+          const int64_t t = t0 + i + kFQWarps * n;
+          tt[n] = (i + kFQWarps * n < per && t < p.T) ? t : -1;
         }
         rt.route<NT>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row, lane, p.out_ids, p.out_w,
                      p.logits, stage);
       }
     };
-    if (per <= 8) route_n(std::integral_constant<int, 1>());
-    else if (per <= 16) route_n(std::integral_constant<int, 2>());
-    else if (ten) route_n(std::integral_constant<int, 3>());
-    else route_n(std::integral_constant<int, 4>());
+    if (per <= kFQWarps) route_n(std::integral_constant<int, 1>());
+    else route_n(std::integral_constant<int, 2>());
   }
 
   tc_fence_before();
@@ -832,6 +867,9 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         if (globaltimer_ns() > drain) break;
     for (int s = 0; s < kFXSlots; ++s)
       while (((filled_x >> s) & 1u) && !mbar_try_wait(full_x + s, (bits_x >> s) & 1u))
+        if (globaltimer_ns() > drain) break;
+    for (int s = 0; s < kFChunkSlots; ++s)
+      while (((filled_c >> s) & 1u) && !mbar_try_wait(full_c + s, (bits_c >> s) & 1u))
         if (globaltimer_ns() > drain) break;
   }
   __syncthreads();
@@ -943,6 +981,7 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   const int n_half = N > 128 ? 2 : 1;
   if (!encode_x(&g.tmap_x, x, T, D, static_cast<uint32_t>(tile_rows))) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes(&g.tmap_b, W_codes, N, D, 128u * n_half)) return NVR_ERR_UNSUPPORTED;
+  g.x = reinterpret_cast<const uint8_t*>(x);
   g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
   g.amax_sync = amax_sync; g.tile_sync = tile_sync; g.flat = flat ? 1 : 0; g.gsa_out = x_gsa;
   g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_half = n_half; g.S = S;

@@ -284,7 +284,7 @@ struct EpiParams {
 // One warp per token (see route_token in nvr_splitk.cuh).
 __global__ void __launch_bounds__(kEpiWarpsPerCta * 32)
 router_epilogue_kernel(const __grid_constant__ EpiParams p) {
-  __shared__ float4 s_row[kEpiWarpsPerCta][64];     // each warp's 256 logits
+  __shared__ float4 s_row[kEpiWarpsPerCta][kRouteSlot];   // each warp's token slot
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kEpiWarpsPerCta + warp;
   TokenRouter rt;

@@ -67,14 +67,18 @@ __device__ __forceinline__ void store_partial_tile(const CUtensorMap* tmap_p, ui
 // same kernel (the tile's cluster or workspace barrier that follows makes them
 // visible): each 32 x 32 block goes through the warp's 4 KB staging buffer at
 // stg_base + (warp-2) * 4 KB (128-byte swizzle, conflict-free both ways) and
-// leaves as 512-byte coalesced rows.
+// leaves as 512-byte coalesced rows.  Called by n_warps = 8 or 16 warps from
+// warp 2 on; with 16, warps 2-9 store column blocks 0-1 of their quarter and
+// half, warps 10-17 blocks 2-3.
 __device__ __forceinline__ void store_partial_rows(float* plane, uint8_t* stg_base, uint32_t tmem, int warp,
-                                                   int lane, int64_t row0, int rows, int n_half, bool have_acc) {
-  const int q = warp & 3, h = (warp - 2) >> 2;
+                                                   int lane, int64_t row0, int rows, int n_half, bool have_acc,
+                                                   int n_warps = 8) {
+  const int w = warp - 2, q = warp & 3, h = (w >> 2) & 1;
   if (h >= n_half || q * 32 >= rows) return;
-  uint8_t* buf = stg_base + (warp - 2) * 4096;
+  const int c_lo = n_warps == 16 ? 2 * (w >> 3) : 0, c_hi = n_warps == 16 ? c_lo + 2 : 4;
+  uint8_t* buf = stg_base + w * 4096;
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = c_lo; c < c_hi; ++c) {
     float v[32];
     if (have_acc) {
       tmem_load32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + c * 32, v);
@@ -164,6 +168,10 @@ __device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
   cx(v, 1, 4); cx(v, 3, 6);
   cx(v, 1, 2); cx(v, 3, 4); cx(v, 5, 6);
 }
+
+// Shared memory of one token slot of a router warp, in float4: the token's
+// 256 logits.
+constexpr int kRouteSlot = 64;
 
 __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
