@@ -417,6 +417,33 @@ def run_gpu(args, rank, world, local_rank):
                 e1.record(stream)
                 torch.cuda.synchronize()
                 decode[key % Td] = e0.elapsed_time(e1) * 1e3 / (reps * calls)
+                if calls == 1 and Td == 1:
+                    # the same graph replayed once on an idle stream: launch
+                    # to completion of one call
+                    lat = []
+                    for _ in range(200):
+                        torch.cuda.synchronize()
+                        e0.record(stream)
+                        g.replay()
+                        e1.record(stream)
+                        torch.cuda.synchronize()
+                        lat.append(e0.elapsed_time(e1) * 1e3)
+                    decode["T1_one_call_graph_latency_us_median"] = statistics.median(lat)
+        # Back-to-back replays of a one-call graph are paced by the host's
+        # replay rate: the same loop over a graph of one trivial kernel
+        tiny = torch.zeros(1, device=dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            tiny.add_(1.0)
+        for _ in range(20):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(2000):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        decode["one_call_graph_host_floor_us"] = e0.elapsed_time(e1) * 1e3 / 2000
         decode["launches_T1"] = 1
         decode["graph"] = "per call: 16 calls captured in one CUDA graph (the layers of a decode step)"
 
@@ -583,34 +610,42 @@ def extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic):
     del Ef, Esf, y, xp, gate
     torch.cuda.empty_cache()
 
-    # the decode kernel's own device duration at T = 1 (graph-free, events
-    # around each launch)
+    # the decode kernel's own device duration at T = 1: 64 back-to-back calls
+    # in one CUDA graph (programmatic launch hides each launch's latency; a
+    # call's work starts when its predecessor's ends), median over replays
     dw = WL.WORKLOADS["decode"]
     gate = R.RouterGate(torch.from_numpy(WL.make_w(dw).view(np.int16)).view(torch.bfloat16).to(dev),
                         torch.from_numpy(WL.make_bias(dw)).to(dev), k=dw.k, routed_scaling=dw.routed_scaling,
                         max_tokens=1)
     xd = torch.from_numpy(WL.make_x(dw.with_T(1)).view(np.int16)).view(torch.bfloat16).to(dev)
-    n = 500
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-    for e in evs:
-        for ev in e:
-            ev.record(stream)
-    for _ in range(10):
-        gate(xd)
+    s2 = torch.cuda.Stream()
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s2):
+        for _ in range(3):
+            gate(xd)
+    torch.cuda.current_stream().wait_stream(s2)
+    n_calls = 64
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n_calls):
+            gate(xd)
+    for _ in range(5):
+        g.replay()
     torch.cuda.synchronize()
-    handles = [ctypes_array(e) for e in evs]
-    lib = _native.lib()
-    for i in range(n):
-        lib.nvr_set_profile_events(handles[i][0], 1)
-        gate(xd)
-    lib.nvr_set_profile_events(None, 0)
-    torch.cuda.synchronize()
-    durs = sorted(e[0].elapsed_time(e[1]) for e in evs)
-    ms = statistics.mean(durs)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    durs = []
+    for _ in range(21):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        durs.append(e0.elapsed_time(e1) / n_calls)
+    durs.sort()
+    ms = durs[len(durs) // 2]
     nbytes = dw.N * (dw.D // 2 + dw.D // 16) + dw.D * 2 + dw.N * 4 + dw.k * 8
     out["decode_kernel_T1"] = _hbm_entry(nbytes, ms, hbm, traffic=traffic.get("decode_router"),
-                                         median_ms=durs[n // 2], p10_ms=durs[n // 10], p90_ms=durs[9 * n // 10],
-                                         note="latency-bound: one launch, events around each launch")
+                                         p10_ms=durs[2], p90_ms=durs[-3],
+                                         note="latency-bound: 64 back-to-back calls in one graph, per call")
     return out
 
 

@@ -28,7 +28,7 @@
 
 namespace nvr {
 
-constexpr int kDecodeThreads = 256;
+constexpr int kDecodeThreads = 512;
 // Several tokens: clusters of 4 CTAs share the staging and quantization of x.
 // (Measured on GB300: clusters of 8 were launched in waves, several µs apart;
 // for a single token the cluster barriers cost more than the sharing saves.)
@@ -152,7 +152,7 @@ __device__ __forceinline__ void warp_topk_256(const float* kt, int N, int k, int
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kMaxBlocksPerThread = 16;   // W blocks a thread prefetches into registers
+constexpr int kMaxBlocksPerThread = 8;    // W blocks a thread prefetches into registers
 constexpr int kMaxT = 16;                 // tokens of one decode call
 
 // Shared memory of one CTA: the raw activations (reused for the last CTA's
@@ -431,12 +431,20 @@ decode_router_kernel(const DecodeParams p) {
   if (p.logits) return;
 
   // 5. the last CTA to finish selects, renormalises and writes
-  __threadfence();
+  // The CTA barrier orders every thread's key stores before thread 0's
+  // ticket, an acquire-release atomic at gpu scope: it publishes them
+  // (release, cumulative over the barrier) and, in the last CTA, makes every
+  // other CTA's published keys visible to the threads that read them after
+  // the next barrier (acquire) -- one round trip instead of a fence and an
+  // atomic.
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+  if (tid == 0) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ticket) : "memory");
+    s_last = old == gridDim.x - 1 ? 1 : 0;
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   float* kbuf = reinterpret_cast<float*>(xraw);                 // x is no longer needed
   float* sbuf = kbuf + static_cast<size_t>(T) * N;
   for (int i = tid; i < T * N; i += kDecodeThreads) {
@@ -464,8 +472,8 @@ decode_router_kernel(const DecodeParams p) {
     if (tid == 0) *p.ticket = 0u;
     return;
   }
-  if (T * N <= 2 * kDecodeThreads) {
-    // Small batches: every thread ranks one or two (token, expert) keys
+  if (T * N <= kDecodeThreads) {
+    // Small batches: every thread ranks at most one (token, expert) key
     // against the token's N keys (key descending, lower id first); the k
     // lowest ranks are the selection, in order.
     for (int pr = tid; pr < T * N; pr += kDecodeThreads) {
