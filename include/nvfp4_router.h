@@ -179,6 +179,28 @@ int nvr_router_cooperative_state(void);
  * bounds. */
 nvr_status nvr_test_occupy(int n_ctas, int smem_bytes, uint64_t duration_ns, nvr_stream_t stream);
 
+/* nvr_test_conversion_sweep -- test hook: checks the hardware conversions
+ * behind every quantizer path, cvt.rn.satfinite.e2m1x2.f32 (E2M1 codes) and
+ * cvt.rn.satfinite.e4m3x2.f32 (E4M3 scale bytes), on every float32 bit pattern
+ * except the NaNs, in both halves of each paired conversion.  The formats are
+ * the standard E2M1 and E4M3 ("fn") with the maxima the pages fix (6 and 448;
+ * "nvfp4-megamoe-kernel commit 04cf8ca: dsv4/layers/router.py", runtime-gsa
+ * section), rounding to nearest, ties to the even code, saturating.
+ *   th_e2m1  device, 7 uint32: t_1..t_7, t_i the smallest float32 bit pattern
+ *            whose E2M1 magnitude code is >= i (ascending);
+ *   th_e4m3  device, 126 uint32: the same for the E4M3 magnitude codes
+ *            0x01..0x7E;
+ *   counts   device, 3 uint64 (written): E2M1 mismatches, E4M3 mismatches,
+ *            inputs checked (2^32 - 2^24 + 2);
+ *   first    device, 2 uint32 (written): the smallest mismatching bit
+ *            pattern of each conversion, 0xFFFFFFFF if none.
+ * A conversion matches when its magnitude code is #{i : bits(|x|) >= t_i}
+ * and, for a nonzero code, its sign bit is the input's (the sign of a zero
+ * result is not compared).  Asynchronous on `stream` (it zeroes counts and
+ * first first); NVR_ERR_INVALID_ARG for a null pointer.  A few ms. */
+nvr_status nvr_test_conversion_sweep(const uint32_t* th_e2m1, const uint32_t* th_e4m3,
+                                     unsigned long long* counts, uint32_t* first, nvr_stream_t stream);
+
 /* nvr_plan_router -- the launch plan router_gate_topk would choose for a call
  * of T >= 1 tokens (dtype dt, hidden D, N experts, flags as for
  * router_gate_topk) on a device with num_sms SMs that holds

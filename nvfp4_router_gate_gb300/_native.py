@@ -48,6 +48,7 @@ SIGNATURES = {
     "nvr_last_router_plan": (_i32, [ctypes.POINTER(_i32)]),
     "nvr_router_cooperative_state": (_i32, []),
     "nvr_test_occupy": (_i32, [_i32, _i32, ctypes.c_uint64, _p]),
+    "nvr_test_conversion_sweep": (_i32, [_p, _p, _p, _p, _p]),
     "nvr_plan_router": (_i32, [_i64, _i64, _i64, _i32, _u32, _i32, ctypes.POINTER(_i32), _i32,
                                ctypes.POINTER(_i32)]),
     "nvr_sf_bytes": (_sz, [_i64, _i64, _i32]),

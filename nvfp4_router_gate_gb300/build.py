@@ -19,7 +19,7 @@ LIB = os.path.join(HERE, "libnvfp4_router.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["quantize.cu", "decode.cu", "gemm_topk.cu", "gemm_splitk.cu", "gemm_fused.cu", "abi.cu", "noalloc.cu",
-           "hash_router.cu", "gemm_stream.cu", "moe.cu"]
+           "hash_router.cu", "gemm_stream.cu", "moe.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr", "-I", INCLUDE]

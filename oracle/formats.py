@@ -112,3 +112,37 @@ def encode_e4m3(values):
     code = _rne_encode(mag, _E4M3_POS_VALUES, _E4M3_POS_CODES)
     sign = np.signbit(v)
     return (code | np.where(sign, 0x80, 0)).astype(np.uint8)
+
+
+# ------------------------------------------------------ rounding thresholds
+
+def _thresholds(encoder, mask, n_codes):
+    """For magnitude codes 1..n_codes-1: the smallest non-negative float32 (as
+    its bit pattern) whose encoding has magnitude code >= that code.  Found
+    by bisection over the bit patterns of [0, max finite float32], which
+    order like the values; valid because the encoders are monotone in the
+    magnitude (RNE onto an ascending grid, then saturation)."""
+    lo = np.zeros(n_codes - 1, dtype=np.int64)                # encodes below the code
+    hi = np.full(n_codes - 1, 0x7F7FFFFF, dtype=np.int64)    # encodes at or above it
+    want = np.arange(1, n_codes, dtype=np.int64)
+    top = encoder(np.array([np.float32(3.4028234663852886e38)])) & mask
+    assert int(top[0]) == n_codes - 1, "the largest float32 saturates to the largest code"
+    while np.any(hi - lo > 1):
+        mid = (lo + hi) // 2
+        codes = encoder(mid.astype(np.uint32).view(np.float32)).astype(np.int64) & mask
+        up = codes >= want
+        hi = np.where(up, mid, hi)
+        lo = np.where(up, lo, mid)
+    return hi.astype(np.uint32)
+
+
+def e2m1_thresholds():
+    """Bit patterns t_1..t_7: a float32 magnitude m encodes to the E2M1
+    magnitude code #{i : bits(m) >= t_i} (the encoder as a step function)."""
+    return _thresholds(encode_e2m1, 0x7, 8)
+
+
+def e4m3_thresholds():
+    """Bit patterns t_1..t_126 for the E4M3 magnitude codes 0x01..0x7E, as
+    e2m1_thresholds (satfinite: everything above 448 is 0x7E)."""
+    return _thresholds(encode_e4m3, 0x7F, 127)

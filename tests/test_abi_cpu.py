@@ -66,6 +66,9 @@ def test_host_argument_checks_without_gpu():
     fake = ctypes.c_void_p(0x10000)          # aligned, never dereferenced
     odd = ctypes.c_void_p(0x10008)           # 8-byte aligned only
     ws_n = L.router_gate_workspace_size(4, 256, 16, 2)
+    # the conversion sweep's null arguments are refused before any launch
+    assert L.nvr_test_conversion_sweep(None, fake, fake, fake, None) == nat.NVR_ERR_INVALID_ARG
+    assert L.nvr_test_conversion_sweep(fake, fake, None, fake, None) == nat.NVR_ERR_INVALID_ARG
     # null activations
     st = L.router_gate_topk(None, nat.NVR_BF16, 4, 256, fake, fake, fake, 16, None, 2, 1.0, 0,
                             fake, fake, fake, ws_n, None)

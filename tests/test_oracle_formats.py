@@ -143,3 +143,22 @@ def test_encoders_against_ml_dtypes_bit_sweep():
     assert np.array_equal(formats.encode_e4m3(small), ref8)
     big = v[np.abs(v) > 464.0]
     assert np.all((formats.encode_e4m3(big) & 0x7F) == 0x7E)
+
+
+def test_rounding_thresholds_are_the_ties_to_even_midpoints():
+    """The encoders as step functions: threshold i (the smallest float32 with
+    magnitude code >= i) is the midpoint of the values of codes i-1 and i
+    when code i is even (a tie goes to it), else the next float32 above the
+    midpoint -- from the decode tables, which are pinned to the printed
+    format tables above.  Catches a tie sent the wrong way, a missing
+    subnormal step or a wrong saturation point."""
+    F = formats
+    for thresholds, decode, n in ((F.e2m1_thresholds(), F.decode_e2m1, 8),
+                                  (F.e4m3_thresholds(), F.decode_e4m3, 127)):
+        vals = np.asarray(decode(np.arange(n)), dtype=np.float64)
+        assert len(thresholds) == n - 1
+        for i in range(1, n):
+            mid = np.float32((vals[i - 1] + vals[i]) / 2)     # exact: midpoints are float32 values
+            assert float(mid) == (vals[i - 1] + vals[i]) / 2
+            exp = mid if i % 2 == 0 else np.nextafter(mid, np.float32(np.inf))
+            assert thresholds[i - 1] == np.array([exp], dtype=np.float32).view(np.uint32)[0], (n, i)
