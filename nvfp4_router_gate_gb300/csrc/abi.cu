@@ -80,8 +80,9 @@ WsLayout router_ws_layout(int64_t T, int64_t D, int64_t N) {
   L.partials = a256(L.x_sf + static_cast<size_t>(rows_pad) * (D / 16));
   const int splits = split_bound(m_tiles, n_tiles);
   size_t part = splits > 1 ? static_cast<size_t>(m_tiles) * splits * 128 * kMaxKmax * 16 : 0;
-  if (N <= 256) {
-    const size_t pk = splitk_partial_rows(T) * 256 * 4;   // K-split partial logits
+  if (N <= 384) {
+    // K-split partial logits, rows of 256 (or, for 257-384 experts, 384) floats
+    const size_t pk = splitk_partial_rows(T) * (N > 256 ? 384 : 256) * 4;
     if (pk > part) part = pk;
   }
   L.decode = a256(L.partials + part);
@@ -243,16 +244,17 @@ nvr_status plan_router(int64_t T, int64_t D, int64_t N, bool bf16, uint32_t flag
     rp.clustered = rp.dp.cluster > 1;
     return NVR_OK;
   }
-  // Up to 256 experts: K split over S CTAs with one tensor-core accumulator
-  // for the whole row each; bf16 activations are quantized inside the GEMM
-  // and routed in the same kernel, fp32 ones take the standalone quantizer,
-  // the K-split GEMM and the epilogue kernel.  Wider heads, after the
-  // standalone quantize kernel: up to 128 tokens stream the weight (its
+  // Up to 256 experts (bf16: 384): K split over S CTAs with one tensor-core
+  // accumulator for the whole row each; bf16 activations are quantized inside
+  // the GEMM and routed in the same kernel, fp32 ones take the standalone
+  // quantizer, the K-split GEMM and the epilogue kernel.  Wider heads, after
+  // the standalone quantize kernel: up to 128 tokens stream the weight (its
   // 128-row tiles as the MMA's M, the tokens as its N), more tokens split the
   // N tiles across CTAs; both merge the per-token top-k lists across CTAs.
   const int split_k = forced_split ? forced_split
-                      : (flags & (NVR_FLAG_SPLIT_N | NVR_FLAG_STREAM)) || N > 256 ? 0
-                                                                                   : plan_splitk(T, D, sms);
+                      : (flags & (NVR_FLAG_SPLIT_N | NVR_FLAG_STREAM)) || N > (bf16 ? 384 : 256)
+                          ? 0
+                          : plan_splitk(T, D, sms);
   if (split_k > 0 && bf16) {
     const int n_st = static_cast<int>((D / kBlock + 15) / 16);
     int tile_rows = 128, S = 1;
@@ -340,7 +342,7 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
   // the fused kernel's capacities, queried (once per device) only where it
   // may run -- never for a decode call, which may be the first call of a
   // process and inside a graph capture
-  const bool maybe_fused = bf16 && N <= 256 &&
+  const bool maybe_fused = bf16 && N <= 384 &&
                            !(flags & (NVR_FLAG_SPLIT_N | NVR_FLAG_STREAM | NVR_FLAG_FORCE_DECODE)) &&
                            ((flags & NVR_FLAG_FORCE_TENSOR_CORE) || !plan_decode(T, D, N, sms, bf16).ok);
   int cluster_cap[5] = {0, 0, 0, 0, 0};
@@ -526,8 +528,8 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k) {
       if (v > part) part = v;
     }
   }
-  if (N <= 256) {
-    const size_t pk = splitk_partial_rows(T_max) * 256 * 4;   // monotone in T
+  if (N <= 384) {
+    const size_t pk = splitk_partial_rows(T_max) * (N > 256 ? 384 : 256) * 4;   // monotone in T
     if (pk > part) part = pk;
   }
   const int64_t t_dec = T_max < 16 ? T_max : 16;

@@ -56,37 +56,52 @@ namespace nvr {
 
 namespace {
 
-constexpr int kFStagesW = 2;
-constexpr int kFWTile = 256 * 128;                  // up to 256 W rows x 128 bytes
-constexpr int kFSfb = 2 * 4 * 512;                  // 4 atoms per 128-expert half
-constexpr int kFWStage = kFWTile + kFSfb;
-constexpr int kFXSlots = 3;
 constexpr int kFXBox = 128 * 128 * 2;               // 128 rows x 128 bf16
 constexpr int kFASlots = 2;
 constexpr int kFACodes = 128 * 128;                 // 128 token rows x 128 bytes of codes
 constexpr int kFASfa = 4 * 512;                     // 4 scale atoms
 constexpr int kFASlot = kFACodes + kFASfa;
-constexpr int kFWRing = kFStagesW * kFWStage;
-constexpr int kFXRing = kFXSlots * kFXBox;
 constexpr int kFARing = kFASlots * kFASlot;
+constexpr int kFXSlots = 3;
+constexpr int kFXRing = kFXSlots * kFXBox;
 constexpr int kFByteTab = 2560;                     // scale bytes of bf16 block maxima (amax down ~20 binades)
 constexpr int kFFixQ = 256;                         // exact-pass queue entries per quantizer warp and box (>= 32 x groups)
 constexpr int kFQWarps = 16;                        // quantizer warps: 8 per x box, both boxes of a stage at once
 constexpr int kFQThreads = 32 * kFQWarps;
 constexpr int kFTables = 1024 + 1024 + kFByteTab + kFQWarps * kFFixQ * 2;   // s_scale, s_cc, s_byte, s_fixq
-constexpr int kFSmem = kFWRing + kFXRing + kFARing + kFTables + 512 /*barriers*/ + 1024 /*align*/;
 constexpr int kFThreads = 64 + kFQThreads;
-// The max|x| pass streams the CTA's contiguous slice of x in 32 KB chunks
-// through a ring over the W, x and A rings (all idle until the pass ends).
 constexpr int kFChunk = 32768;
-constexpr int kFChunkSlots = 6;
-static_assert(kFChunkSlots * kFChunk <= kFWRing + kFXRing + kFARing, "the chunk ring fits the three rings");
+// The shared-memory plan for heads of up to 128 kNT experts (kNT = 2: up to
+// 256, kNT = 3: up to 384).  The W tile of a stage holds 128 kNT rows x 128
+// bytes and kNT x 4 scale atoms; with kNT = 3 one stage is buffered (a W
+// tile comes from L2 in about 1 us while the quantizers take longer over a
+// stage), else two.  The max|x| pass streams the CTA's contiguous slice of x
+// in 32 KB chunks through a ring over the W, x and A rings (all idle until the
+// pass ends).
+template <int kNT>
+struct FusedCfg {
+  static_assert(kNT == 2 || kNT == 3, "up to 256 or 384 experts");
+  static constexpr int kStagesW = kNT == 3 ? 1 : 2;
+  static constexpr int kWTile = 128 * kNT * 128;
+  static constexpr int kSfb = kNT * 4 * 512;
+  static constexpr int kWStage = kWTile + kSfb;
+  static constexpr int kWRing = kStagesW * kWStage;
+  static constexpr int kChunkSlots = (kWRing + kFXRing + kFARing) / kFChunk < 6 ? (kWRing + kFXRing + kFARing) / kFChunk : 6;
+  static constexpr int kSmem = kWRing + kFXRing + kFARing + kFTables + 512 /*barriers*/ + 1024 /*align*/;
+  // tensor memory: the accumulator at columns 0 .. 128 kNT - 1, then per A
+  // slot the x scales (4 columns per K step) and the W scales (4 kNT)
+  static constexpr int kScaleCol = 128 * kNT;
+  static constexpr int kScaleSlot = 16 + 16 * kNT;
+  static_assert(kScaleCol + kFASlots * kScaleSlot <= 512, "tensor memory");
+  static_assert(kWStage % 1024 == 0 && kFASlot % 1024 == 0 && kFXBox % 1024 == 0, "1024-byte aligned tiles");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(kChunkSlots >= 4, "the max|x| ring");
+};
+static_assert(16 * 4096 <= kFXRing, "store staging fits the x ring");
 // A token tile has kRows = 128 or 112 rows (the kernel is instantiated for
-// both): each of the eight quantizer warps takes kRows / 8 rows, that is
-// kRows / 16 row pairs, quantized as one group (their chains interleave).
+// both): each of the eight quantizer warps of a box takes kRows / 8 rows, that
+// is kRows / 16 row pairs, quantized as one group (their chains interleave).
 // With 112 the MMA's last 16 accumulator rows are junk and never stored.
-static_assert(kFWStage % 1024 == 0 && kFASlot % 1024 == 0 && kFXBox % 1024 == 0, "1024-byte aligned tiles");
-static_assert(8 * 8192 <= kFXRing, "store staging fits the x ring");
 
 struct FusedParams {
   CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
@@ -100,7 +115,7 @@ struct FusedParams {
   float* gsa_out;              // in-kernel amax: x's global scale (also x_gsa)
   const uint8_t* sfb;          // W scales, tile layout
   float* partials;             // [S][T][256] fp32 partial logits (workspace)
-  int T, D, N, n_half, S;
+  int T, D, N, n_groups, S;   // n_groups: 128-expert groups of the head (1 .. kNT)
   // router epilogue
   const float* x_gsa;
   const float* w_gsa;
@@ -404,9 +419,12 @@ __device__ __forceinline__ void quant_box(const uint8_t* xb, uint8_t* ac, uint8_
   }
 }
 
-template <int kRows>
+template <int kRows, int kNT>
 __global__ void __launch_bounds__(kFThreads, 1)
 fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
+  using C = FusedCfg<kNT>;
+  constexpr int kFStagesW = C::kStagesW, kFWTile = C::kWTile, kFWStage = C::kWStage, kFWRing = C::kWRing;
+  constexpr int kFChunkSlots = C::kChunkSlots;
   constexpr int kFRowsPerWarp = kRows / 8;
   constexpr uint32_t kBoxBytes = 128u * kRows * 2u;  // one bf16 x box: kRows rows x 128 elements
   extern __shared__ uint8_t smem_raw[];
@@ -498,7 +516,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   const uint64_t deadline = globaltimer_ns() + 1000000000ull;   // 1 s
 
   bool acc_ok = true;     // quantizer warps: the accumulator is complete
-  TokenRouter rt;         // quantizer warps: the epilogue's per-lane state
+  TokenRouterT<kNT> rt;   // quantizer warps: the epilogue's per-lane state
   float gscale = 0.0f;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -560,9 +578,14 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       uint8_t* b = wring + wst * kFWStage;
       uint8_t* sb = b + kFWTile;
       if (elect_one()) {
-        mbar_arrive_expect_tx(full_w + wst, static_cast<uint32_t>(p.n_half * (128 * 128 + 512 * nkk)));
-        tma_load_2d(b, &p.tmap_b, ks * 128, 0, full_w + wst);
-        for (int h = 0; h < p.n_half; ++h)
+        mbar_arrive_expect_tx(full_w + wst, static_cast<uint32_t>(p.n_groups * (128 * 128 + 512 * nkk)));
+        if (kNT == 2) {
+          tma_load_2d(b, &p.tmap_b, ks * 128, 0, full_w + wst);      // 128 or 256 rows in one box
+        } else {
+          for (int h = 0; h < p.n_groups; ++h)                        // 128-row boxes
+            tma_load_2d(b + h * 16384, &p.tmap_b, ks * 128, h * 128, full_w + wst);
+        }
+        for (int h = 0; h < p.n_groups; ++h)
           bulk_load(sb + h * 2048, p.sfb + (static_cast<size_t>(h) * (KB / 4) + 4 * ks) * 512, 512u * nkk,
                     full_w + wst);
       }
@@ -578,7 +601,10 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (!p.test_stall) {
-      const uint32_t idesc = idesc_mxf4nvf4(128, 128 * p.n_half);
+      // kNT = 2: one MMA over the 128 or 256 experts; kNT = 3: experts
+      // 0-255 (N = 256) and 256-383 (N = 128, accumulator columns 256 ..)
+      const uint32_t idesc = idesc_mxf4nvf4(128, kNT == 2 ? 128 * p.n_groups : 256);
+      const uint32_t idesc3 = idesc_mxf4nvf4(128, 128);
       int wst = 0;
       uint32_t wph = 0;
       bool ok = true;
@@ -595,18 +621,25 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         const int nkk = min(4, KB / 4 - 4 * ks);
         const uint8_t* a = aring + slot * kFASlot;
         const uint8_t* b = wring + wst * kFWStage;
-        const uint32_t sf_t = tmem + 256 + slot * 48;
+        const uint32_t sf_t = tmem + C::kScaleCol + slot * C::kScaleSlot;
         if (elect_one()) {
           // the stage's scale atoms into tensor memory (in order with the
-          // MMAs on the tensor pipe): x at +4 kk, W half h at +16 + 8 kk + 4 h
+          // MMAs on the tensor pipe): x at +4 kk, W group h at
+          // +16 + 4 kNT kk + 4 h
           for (int kk = 0; kk < nkk; ++kk) {
             tc_copy_scales(sf_t + 4 * kk, desc_scale_tile(smem_u32(a + kFACodes + 512 * kk)));
-            for (int h = 0; h < p.n_half; ++h)
-              tc_copy_scales(sf_t + 16 + 8 * kk + 4 * h, desc_scale_tile(smem_u32(b + kFWTile + 2048 * h + 512 * kk)));
+            for (int h = 0; h < p.n_groups; ++h)
+              tc_copy_scales(sf_t + 16 + 4 * kNT * kk + 4 * h,
+                             desc_scale_tile(smem_u32(b + kFWTile + 2048 * h + 512 * kk)));
           }
-          for (int kk = 0; kk < nkk; ++kk)
+          for (int kk = 0; kk < nkk; ++kk) {
             tc_mma_nvf4(tmem, desc_kmajor_sw128(smem_u32(a + 32 * kk)), desc_kmajor_sw128(smem_u32(b + 32 * kk)),
-                        idesc, sf_t + 4 * kk, sf_t + 16 + 8 * kk, (s | kk) != 0);
+                        idesc, sf_t + 4 * kk, sf_t + 16 + 4 * kNT * kk, (s | kk) != 0);
+            if (kNT == 3)
+              tc_mma_nvf4(tmem + 256, desc_kmajor_sw128(smem_u32(a + 32 * kk)),
+                          desc_kmajor_sw128(smem_u32(b + 256 * 128 + 32 * kk)), idesc3, sf_t + 4 * kk,
+                          sf_t + 16 + 4 * kNT * kk + 8, (s | kk) != 0);
+          }
           tc_commit(empty_w + wst);
           tc_commit(a_empty + slot);
         }
@@ -793,9 +826,9 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     tc_fence_after();
     // every x box has been read (the last MMA needed them all): the x ring
     // stages the stores
-    store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * 256, xring, tmem, warp, lane,
-                       static_cast<int64_t>(m_tile) * kRows, min(kRows, p.T - m_tile * kRows), p.n_half,
-                       my_st > 0 && acc_ok, kFQWarps);
+    store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * (128 * kNT), xring, tmem, warp, lane,
+                       static_cast<int64_t>(m_tile) * kRows, min(kRows, p.T - m_tile * kRows), p.n_groups,
+                       my_st > 0 && acc_ok, kFQWarps, 128 * kNT);
   }
 
   // The S CTAs of this token tile form the cluster, or meet at the tile's
@@ -824,17 +857,19 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   if (warp >= 2) {
     const int rw = warp - 2;
     // with 8 or more partial planes (then at most 16 tokens per CTA: one per
-    // router warp) the W and x rings (contiguous, idle now) stage each warp's
-    // S partial rows, all copied at once (measured: fewer planes are faster
-    // loaded directly): S KB per warp with a token, rw < 128 / S; each warp's
-    // token slot (kRouteSlot float4) is then in the A ring, else its two
-    // slots are in the x ring (all idle now)
-    float4* stage = p.S >= 8 ? reinterpret_cast<float4*>(wring) + rw * p.S * 64 : nullptr;
-    static_assert(128 * 1024 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
-    static_assert(kFQWarps * kRouteSlot * 16 <= kFARing && 2 * kFQWarps * kRouteSlot * 16 <= kFXRing,
+    // router warp) and up to 256 experts the W and x rings (contiguous, idle
+    // now) stage each warp's S partial rows, all copied at once (measured:
+    // fewer planes are faster loaded directly): S KB per warp with a token,
+    // rw < 128 / S; each warp's token slot is then in the A ring, else its
+    // two slots are in the x ring (all idle now)
+    constexpr int kSlot = RouteSlot<kNT>::kFloat4;
+    const bool staged = kNT == 2 && p.S >= 8;
+    float4* stage = staged ? reinterpret_cast<float4*>(wring) + rw * p.S * 64 : nullptr;
+    static_assert(kNT == 3 || 128 * 1024 <= kFWRing + kFXRing, "epilogue staging fits the W and x rings");
+    static_assert(kFQWarps * kSlot * 16 <= kFARing && 2 * kFQWarps * kSlot * 16 <= kFXRing,
                   "token slots fit the A ring (one per warp) and the x ring (two per warp)");
-    float4* s_row = p.S >= 8 ? reinterpret_cast<float4*>(aring) + rw * kRouteSlot
-                             : reinterpret_cast<float4*>(xring) + rw * 2 * kRouteSlot;
+    float4* s_row = staged ? reinterpret_cast<float4*>(aring) + rw * kSlot
+                           : reinterpret_cast<float4*>(xring) + rw * 2 * kSlot;
     const int64_t t0 = static_cast<int64_t>(m_tile) * kRows + static_cast<int64_t>(rank) * per;
     // as many token slots per call as the warp has tokens -- empty slots
     // would still be sorted
@@ -847,8 +882,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
           const int64_t t = t0 + i + kFQWarps * n;
           tt[n] = (i + kFQWarps * n < per && t < p.T) ? t : -1;
         }
-        rt.route<NT>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row, lane, p.out_ids, p.out_w,
-                     p.logits, stage);
+        rt.template route<NT>(p.partials, static_cast<size_t>(p.T) * (128 * kNT), p.S, tt, gscale, s_row, lane,
+                              p.out_ids, p.out_w, p.logits, stage);
       }
     };
     if (per <= kFQWarps) route_n(std::integral_constant<int, 1>());
@@ -892,16 +927,23 @@ bool encode_x(CUtensorMap* map, const uint16_t* ptr, int64_t T, int64_t D, uint3
 
 }  // namespace
 
-// Per-device function attributes of both instantiations: the dynamic shared
+// Per-device function attributes of the four instantiations (128- and
+// 112-row tiles, heads of up to 256 and 384 experts): the dynamic shared
 // memory and clusters of up to 16 CTAs (beyond the portable 8; the planner
 // asks first).
 static cudaError_t fused_prepare(int dev) {
   static bool done[kMaxDevices] = {};
   if (done[dev]) return cudaSuccess;
-  for (auto* fn : {fused_qgemm_kernel<128>, fused_qgemm_kernel<112>}) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+  struct Fn {
+    void (*fn)(FusedParams);
+    int smem;
+  };
+  const Fn fns[4] = {{fused_qgemm_kernel<128, 2>, FusedCfg<2>::kSmem}, {fused_qgemm_kernel<112, 2>, FusedCfg<2>::kSmem},
+                     {fused_qgemm_kernel<128, 3>, FusedCfg<3>::kSmem}, {fused_qgemm_kernel<112, 3>, FusedCfg<3>::kSmem}};
+  for (const Fn& f : fns) {
+    cudaError_t e = cudaFuncSetAttribute(f.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(f.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   done[dev] = true;
@@ -917,7 +959,9 @@ int fused_block_capacity() {
   if (cap[dev] > 0) return cap[dev];
   if (fused_prepare(dev) != cudaSuccess) return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_qgemm_kernel<128>, kFThreads, kFSmem) !=
+  // the widest plan (one CTA per SM either way)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_qgemm_kernel<128, 2>, kFThreads,
+                                                    FusedCfg<2>::kSmem) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -940,7 +984,7 @@ int fused_cluster_capacity(int S) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S);
   cfg.blockDim = dim3(kFThreads);
-  cfg.dynamicSmemBytes = kFSmem;
+  cfg.dynamicSmemBytes = FusedCfg<2>::kSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = S;
@@ -949,8 +993,8 @@ int fused_cluster_capacity(int S) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  // both instantiations have the same resources
-  if (cudaOccupancyMaxActiveClusters(&n, fused_qgemm_kernel<128>, &cfg) != cudaSuccess) n = 0;
+  // the widest plan (one CTA per SM either way)
+  if (cudaOccupancyMaxActiveClusters(&n, fused_qgemm_kernel<128, 2>, &cfg) != cudaSuccess) n = 0;
   cudaGetLastError();
   cap[dev][slot] = n;
   known[dev][slot] = true;
@@ -969,7 +1013,7 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
                                int tile_rows, bool test_stall, bool cooperative, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVR_ERR_CUDA;
-  if (N > 256 || k > kMaxKmax || S < 1 || S > 16 || 128 % S) return NVR_ERR_UNSUPPORTED;
+  if (N > 384 || k > kMaxKmax || S < 1 || S > 16 || 128 % S) return NVR_ERR_UNSUPPORTED;
   if (tile_rows != 128 && tile_rows != 112) return NVR_ERR_UNSUPPORTED;
   if (amax_sync && !tile_sync) return NVR_ERR_INVALID_ARG;
   if (flat && (!amax_sync || (T + tile_rows - 1) / tile_rows > kMaxFlatTiles)) return NVR_ERR_UNSUPPORTED;
@@ -978,13 +1022,14 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   const cudaError_t e = fused_prepare(dev);
   if (e != cudaSuccess) return cuda_status(e);
   FusedParams g;
-  const int n_half = N > 128 ? 2 : 1;
+  const int n_groups = static_cast<int>((N + 127) / 128);
+  const int nt = N > 256 ? 3 : 2;
   if (!encode_x(&g.tmap_x, x, T, D, static_cast<uint32_t>(tile_rows))) return NVR_ERR_UNSUPPORTED;
-  if (!encode_codes(&g.tmap_b, W_codes, N, D, 128u * n_half)) return NVR_ERR_UNSUPPORTED;
+  if (!encode_codes(&g.tmap_b, W_codes, N, D, nt == 2 ? 128u * n_groups : 128u)) return NVR_ERR_UNSUPPORTED;
   g.x = reinterpret_cast<const uint8_t*>(x);
   g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
   g.amax_sync = amax_sync; g.tile_sync = tile_sync; g.flat = flat ? 1 : 0; g.gsa_out = x_gsa;
-  g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_half = n_half; g.S = S;
+  g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_groups = n_groups; g.S = S;
   g.x_gsa = x_gsa; g.w_gsa = w_gsa; g.bias = raw ? nullptr : bias;
   g.k = k; g.raw = raw ? 1 : 0; g.routed_scaling = routed_scaling;
   g.out_ids = out_ids; g.out_w = out_w; g.logits = logits;
@@ -1019,13 +1064,16 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((T + tile_rows - 1) / tile_rows * S));
   cfg.blockDim = dim3(kFThreads);
-  cfg.dynamicSmemBytes = kFSmem;
+  cfg.dynamicSmemBytes = nt == 3 ? FusedCfg<3>::kSmem : FusedCfg<2>::kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = na;
   auto launch = [&]() {
-    return tile_rows == 112 ? cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<112>, g)
-                            : cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<128>, g);
+    if (nt == 3)
+      return tile_rows == 112 ? cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<112, 3>, g)
+                              : cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<128, 3>, g);
+    return tile_rows == 112 ? cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<112, 2>, g)
+                            : cudaLaunchKernelEx(&cfg, fused_qgemm_kernel<128, 2>, g);
   };
   cudaError_t e2 = launch();
   if (try_coop && coop_ok[dev] == 0) {

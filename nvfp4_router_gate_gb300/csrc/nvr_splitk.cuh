@@ -63,39 +63,44 @@ __device__ __forceinline__ void store_partial_tile(const CUtensorMap* tmap_p, ui
   __syncwarp();
 }
 
-// The same tile with ordinary stores, for a reader in another CTA of the
-// same kernel (the tile's cluster or workspace barrier that follows makes them
-// visible): each 32 x 32 block goes through the warp's 4 KB staging buffer at
-// stg_base + (warp-2) * 4 KB (128-byte swizzle, conflict-free both ways) and
-// leaves as 512-byte coalesced rows.  Called by n_warps = 8 or 16 warps from
-// warp 2 on; with 16, warps 2-9 store column blocks 0-1 of their quarter and
-// half, warps 10-17 blocks 2-3.
+// The same accumulator with ordinary stores, for a reader in another CTA of
+// the same kernel (the tile's cluster or workspace barrier that follows makes
+// them visible): rows of row_floats floats, n_groups groups of 128 columns
+// (tensor-memory columns 128 g ..).  Called by the n_warps (8 or 16) warps
+// from warp 2 on: warp w may only read tensor-memory lanes 32 (w % 4) .., so
+// the n_warps / 4 warps of each lane quarter share its 4 n_groups blocks of
+// 32 x 32 (block b: group b / 4, columns 32 (b % 4)); each block goes
+// through the warp's 4 KB staging buffer at stg_base + (warp-2) * 4 KB
+// (128-byte swizzle, conflict-free both ways) and leaves as coalesced rows.
 __device__ __forceinline__ void store_partial_rows(float* plane, uint8_t* stg_base, uint32_t tmem, int warp,
-                                                   int lane, int64_t row0, int rows, int n_half, bool have_acc,
-                                                   int n_warps = 8) {
-  const int w = warp - 2, q = warp & 3, h = (w >> 2) & 1;
-  if (h >= n_half || q * 32 >= rows) return;
-  const int c_lo = n_warps == 16 ? 2 * (w >> 3) : 0, c_hi = n_warps == 16 ? c_lo + 2 : 4;
+                                                   int lane, int64_t row0, int rows, int n_groups, bool have_acc,
+                                                   int n_warps, int row_floats) {
+  const int w = warp - 2, q = warp & 3, j = w >> 2, wpq = n_warps >> 2;
+  if (q * 32 >= rows) return;
+  const int total = 4 * n_groups, per = (total + wpq - 1) / wpq;
+  const int b_lo = j * per, b_hi = min(total, b_lo + per);
   uint8_t* buf = stg_base + w * 4096;
 #pragma unroll 1
-  for (int c = c_lo; c < c_hi; ++c) {
+  for (int blk = b_lo; blk < b_hi; ++blk) {
+    const int col0 = (blk >> 2) * 128 + (blk & 3) * 32;
     float v[32];
     if (have_acc) {
-      tmem_load32(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + c * 32, v);
+      tmem_load32(tmem + (static_cast<uint32_t>(q * 32) << 16) + col0, v);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = 0.0f;
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    for (int jj = 0; jj < 8; ++jj)
+      st_shared_v4(buf + lane * 128 + ((jj ^ (lane & 7)) << 4), v[4 * jj], v[4 * jj + 1], v[4 * jj + 2],
+                   v[4 * jj + 3]);
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int r = 4 * i + (lane >> 3), j = lane & 7;
-      const uint4 val = ld_shared_v4(buf + r * 128 + ((j ^ (r & 7)) << 4));
+      const int r = 4 * i + (lane >> 3), c = lane & 7;
+      const uint4 val = ld_shared_v4(buf + r * 128 + ((c ^ (r & 7)) << 4));
       if (q * 32 + r < rows)
-        *reinterpret_cast<uint4*>(plane + (row0 + q * 32 + r) * 256 + h * 128 + c * 32 + 4 * j) = val;
+        *reinterpret_cast<uint4*>(plane + (row0 + q * 32 + r) * row_floats + col0 + 4 * c) = val;
     }
     __syncwarp();
   }
@@ -130,18 +135,21 @@ inline bool encode_partials(CUtensorMap* map, float* ptr, int64_t T, int S) {
 
 // ------------------------------------------------------------ router epilogue
 //
-// One warp routes one token from its S fp32 partial-logit rows (planes
-// `plane` floats apart): lane l owns experts 4l..4l+3 and 128+4l..128+4l+3
-// (coalesced 512-byte rows).  The partials are added in rank order (the
-// result does not depend on timing), scaled by gsa_x * gsa_w; keys are
-// sigmoid(logit) + bias (RAW: the logit).  Selection: each lane sorts its 8
-// (key, id) pairs packed into order-preserving 64-bit words; k rounds then
-// take the best head of the warp (two 32-bit max reductions: the key's bits,
-// then the complemented id among the lanes holding that key) and the winning
-// lane pops its head.  Exact for any keys, ties included (equal keys: lower
-// id first), with no data-dependent trip counts.  The selected experts'
-// logits come back from the warp's copy of the row in shared memory; the
-// weights are routed_scaling * score / (sum of the k scores).
+// One warp routes one token from its S fp32 partial-logit rows (row stride
+// 128 NG floats, planes `plane` floats apart), NG = 2 for heads of up to 256
+// experts, 3 for up to 384: lane l owns experts 128 g + 4l .. 128 g + 4l + 3
+// of every group g (coalesced 512-byte rows).  The partials are added in
+// rank order (the result does not depend on timing), scaled by
+// gsa_x * gsa_w; keys are sigmoid(logit) + bias (RAW: the logit).
+// Selection: each lane sorts its keys of groups 0-1 (8 (key, id) pairs packed
+// into order-preserving 64-bit words) and, with NG = 3, those of group 2 in a
+// second list of 4; k rounds then take the best head of the warp (two 32-bit
+// max reductions: the key's bits, then the complemented id among the lanes
+// holding that key) and the winning lane pops its head.  Exact for any keys,
+// ties included (equal keys: lower id first), with no data-dependent trip
+// counts.  The selected experts' logits come back from the warp's copy of the
+// row in shared memory; the weights are routed_scaling * score / (sum of the
+// k scores).
 
 // (key descending, id ascending) as one unsigned 64-bit order: the float's
 // order-preserving bit pattern above the complemented id.  Never 0 for a
@@ -153,8 +161,10 @@ __device__ __forceinline__ uint64_t pack_key(float key, int id) {
 }
 
 // Compare-exchange so that v[a] >= v[b]; the 19-comparator 8-sorter (the
-// network of sort8 in nvr_device.cuh) on packed keys.
-__device__ __forceinline__ void cx(uint64_t (&v)[8], int a, int b) {
+// network of sort8 in nvr_device.cuh) and the 5-comparator 4-sorter on packed
+// keys.
+template <int M>
+__device__ __forceinline__ void cx(uint64_t (&v)[M], int a, int b) {
   const uint64_t x = v[a], y = v[b];
   const bool sw = y > x;
   v[a] = sw ? y : x;
@@ -168,19 +178,34 @@ __device__ __forceinline__ void sort8_desc(uint64_t (&v)[8]) {
   cx(v, 1, 4); cx(v, 3, 6);
   cx(v, 1, 2); cx(v, 3, 4); cx(v, 5, 6);
 }
+__device__ __forceinline__ void sort4_desc(uint64_t (&v)[4]) {
+  cx(v, 0, 1); cx(v, 2, 3);
+  cx(v, 0, 2); cx(v, 1, 3);
+  cx(v, 1, 2);
+}
 
 // Shared memory of one token slot of a router warp, in float4: the token's
-// 256 logits.
-constexpr int kRouteSlot = 64;
+// 128 NG logits.
+template <int NG>
+struct RouteSlot {
+  static constexpr int kFloat4 = 32 * NG;
+};
+constexpr int kRouteSlot = RouteSlot<2>::kFloat4;
 
 __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
 }
 
-struct TokenRouter {
-  float b[8];                  // bias of this lane's experts (0 in RAW mode or without bias)
+template <int NG>
+struct TokenRouterT {
+  static_assert(NG == 2 || NG == 3, "heads of up to 256 or 384 experts");
+  static constexpr int kE = 4 * NG;        // experts per lane
+  static constexpr int kRow = 128 * NG;    // floats per partial row
+  float b[kE];                 // bias of this lane's experts (0 in RAW mode or without bias)
   int N, k, raw;
   float routed_scaling;
+
+  __device__ __forceinline__ static int col_of(int j, int lane) { return 128 * (j >> 2) + 4 * lane + (j & 3); }
 
   // The bias is a caller input that no kernel of the call writes; the call's
   // first kernel has already waited for the caller's previous kernel (which
@@ -189,96 +214,107 @@ struct TokenRouter {
   __device__ __forceinline__ void init(const float* bias, int N_, int k_, int raw_, float rs, int lane) {
     N = N_; k = k_; raw = raw_; routed_scaling = rs;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int col = (j < 4 ? 0 : 128) + 4 * lane + (j & 3);
+    for (int j = 0; j < kE; ++j) {
+      const int col = col_of(j, lane);
       b[j] = (!raw && bias && col < N) ? __ldg(bias + col) : 0.0f;
     }
   }
 
   // Routes NT tokens at once (independent dependency chains interleave);
-  // t[i] < 0 marks an unused slot.  s_row: NT rows of 64 float4 for the warp.
-  // stage: null, or shared memory for the warp's partial rows (row n * S + s:
-  // 64 float4 of token slot n, plane s; only the rows of valid slots are
-  // touched) -- then every partial row is copied in at once (asynchronous
-  // copies, one round trip to L2 whatever S) before the sums.
+  // t[i] < 0 marks an unused slot.  s_row: NT token slots of
+  // RouteSlot<NG>::kFloat4 float4 for the warp.  stage: null, or shared
+  // memory for the warp's partial rows (row n * S + s: 32 NG float4 of token
+  // slot n, plane s; only the rows of valid slots are touched) -- then every
+  // partial row is copied in at once (asynchronous copies, one round trip to
+  // L2 whatever S) before the sums.
   template <int NT>
   __device__ __forceinline__ void route(const float* partials, size_t plane, int S, const int64_t (&t)[NT],
                                         float gscale, float4* s_row, int lane, int32_t* out_ids, float* out_w,
                                         float* logits, float4* stage = nullptr) const {
-    float4 a0[NT], a1[NT];
+    constexpr int kSlot = RouteSlot<NG>::kFloat4;
+    float4 a[NT][NG];
     if (stage) {
       for (int s = 0; s < S; ++s)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           if (t[n] < 0) continue;
-          const float* r = partials + static_cast<size_t>(t[n]) * 256 + s * plane;
-          float4* d = stage + 64 * (n * S + s);
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(d + lane)),
-                       "l"(reinterpret_cast<uint64_t>(r + 4 * lane)) : "memory");
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(d + 32 + lane)),
-                       "l"(reinterpret_cast<uint64_t>(r + 128 + 4 * lane)) : "memory");
+          const float* r = partials + static_cast<size_t>(t[n]) * kRow + s * plane;
+          float4* d = stage + kSlot * (n * S + s);
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(d + 32 * g + lane)),
+                         "l"(reinterpret_cast<uint64_t>(r + 128 * g + 4 * lane)) : "memory");
         }
       asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
       // each lane reads back only what it copied itself: no warp barrier needed
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         const bool ok = t[n] >= 0;
-        a0[n] = ok ? stage[64 * (n * S) + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-        a1[n] = ok ? stage[64 * (n * S) + 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+          a[n][g] = ok ? stage[kSlot * (n * S) + 32 * g + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       for (int s = 1; s < S; ++s)                        // partials in rank order
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           if (t[n] < 0) continue;
-          a0[n] = add4(a0[n], stage[64 * (n * S + s) + lane]);
-          a1[n] = add4(a1[n], stage[64 * (n * S + s) + 32 + lane]);
+#pragma unroll
+          for (int g = 0; g < NG; ++g) a[n][g] = add4(a[n][g], stage[kSlot * (n * S + s) + 32 * g + lane]);
         }
     } else {
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        const float* row = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * 256;
-        a0[n] = __ldcg(reinterpret_cast<const float4*>(row + 4 * lane));
-        a1[n] = __ldcg(reinterpret_cast<const float4*>(row + 128 + 4 * lane));
+        const float* row = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * kRow;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) a[n][g] = __ldcg(reinterpret_cast<const float4*>(row + 128 * g + 4 * lane));
       }
 #pragma unroll 2
       for (int s = 1; s < S; ++s) {                      // partials in rank order
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const float* r = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * 256 + s * plane;
-          a0[n] = add4(a0[n], __ldcg(reinterpret_cast<const float4*>(r + 4 * lane)));
-          a1[n] = add4(a1[n], __ldcg(reinterpret_cast<const float4*>(r + 128 + 4 * lane)));
+          const float* r = partials + static_cast<size_t>(t[n] < 0 ? 0 : t[n]) * kRow + s * plane;
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+            a[n][g] = add4(a[n][g], __ldcg(reinterpret_cast<const float4*>(r + 128 * g + 4 * lane)));
         }
       }
     }
-    int col[8];
+    float l[NT][kE];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) col[j] = (j < 4 ? 0 : 128) + 4 * lane + (j & 3);
-    float l[NT][8];
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const float acc[8] = {a0[n].x, a0[n].y, a0[n].z, a0[n].w, a1[n].x, a1[n].y, a1[n].z, a1[n].w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) l[n][j] = __fmul_rn(acc[j], gscale);
-    }
+      for (int g = 0; g < NG; ++g) {
+        l[n][4 * g] = __fmul_rn(a[n][g].x, gscale);
+        l[n][4 * g + 1] = __fmul_rn(a[n][g].y, gscale);
+        l[n][4 * g + 2] = __fmul_rn(a[n][g].z, gscale);
+        l[n][4 * g + 3] = __fmul_rn(a[n][g].w, gscale);
+      }
     if (logits) {
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (t[n] >= 0 && col[j] < N) logits[t[n] * N + col[j]] = l[n][j];
+        for (int j = 0; j < kE; ++j)
+          if (t[n] >= 0 && col_of(j, lane) < N) logits[t[n] * N + col_of(j, lane)] = l[n][j];
       return;
     }
-    uint64_t pk[NT][8];
+    // lists: groups 0-1 (8 words), and group 2 (4 words) when NG = 3
+    constexpr int kB = NG == 3 ? 4 : 1;
+    uint64_t pa[NT][8], pb[NT][kB];
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      s_row[64 * n + lane] = make_float4(l[n][0], l[n][1], l[n][2], l[n][3]);
-      s_row[64 * n + 32 + lane] = make_float4(l[n][4], l[n][5], l[n][6], l[n][7]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int g = 0; g < NG; ++g)
+        s_row[kSlot * n + 32 * g + lane] = make_float4(l[n][4 * g], l[n][4 * g + 1], l[n][4 * g + 2], l[n][4 * g + 3]);
+#pragma unroll
+      for (int j = 0; j < kE; ++j) {
         const float key = raw ? l[n][j] : __fadd_rn(sigmoid_f32(l[n][j]), b[j]);
-        pk[n][j] = col[j] < N ? pack_key(key, col[j]) : 0;
+        const uint64_t w = col_of(j, lane) < N ? pack_key(key, col_of(j, lane)) : 0;
+        if (j < 8) pa[n][j] = w;
+        else pb[n][(j - 8) & (kB - 1)] = w;
       }
-      sort8_desc(pk[n]);
+      sort8_desc(pa[n]);
+      if constexpr (NG == 3) sort4_desc(pb[n]);
+      else pb[n][0] = 0;
     }
     int sel_id[NT];
 #pragma unroll
@@ -288,10 +324,13 @@ struct TokenRouter {
 #pragma unroll 1
     for (int r = 0; r < k; ++r) {
       uint32_t hi[NT], lo[NT], hmax[NT], lmax[NT];
+      bool from_b[NT];
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        hi[n] = static_cast<uint32_t>(pk[n][0] >> 32);
-        lo[n] = static_cast<uint32_t>(pk[n][0]);
+        from_b[n] = NG == 3 && pb[n][0] > pa[n][0];
+        const uint64_t h = from_b[n] ? pb[n][0] : pa[n][0];
+        hi[n] = static_cast<uint32_t>(h >> 32);
+        lo[n] = static_cast<uint32_t>(h);
       }
 #pragma unroll
       for (int n = 0; n < NT; ++n) hmax[n] = __reduce_max_sync(0xFFFFFFFFu, hi[n]);
@@ -301,9 +340,15 @@ struct TokenRouter {
       for (int n = 0; n < NT; ++n) {
         if (lane == r) sel_id[n] = static_cast<int>(~lmax[n]);   // the winning expert
         const bool win = hi[n] == hmax[n] && lo[n] == lmax[n];     // its lane (ids are unique)
+        const bool wa = win && !from_b[n], wb = win && from_b[n];
 #pragma unroll
-        for (int j = 0; j < 7; ++j) pk[n][j] = win ? pk[n][j + 1] : pk[n][j];
-        pk[n][7] = win ? 0 : pk[n][7];
+        for (int j = 0; j < 7; ++j) pa[n][j] = wa ? pa[n][j + 1] : pa[n][j];
+        pa[n][7] = wa ? 0 : pa[n][7];
+        if constexpr (NG == 3) {
+#pragma unroll
+          for (int j = 0; j < 3; ++j) pb[n][j] = wb ? pb[n][j + 1] : pb[n][j];
+          pb[n][3] = wb ? 0 : pb[n][3];
+        }
       }
     }
     __syncwarp();
@@ -311,7 +356,8 @@ struct TokenRouter {
     float sc[NT], sum[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      const float sel_l = reinterpret_cast<const float*>(s_row + 64 * n)[sel_id[n] & 255];
+      const int id = sel_id[n];
+      const float sel_l = reinterpret_cast<const float*>(s_row + kSlot * n)[(id >= 0 && id < kRow) ? id : 0];
       sc[n] = raw ? sel_l : sigmoid_f32(sel_l);
       sum[n] = mine ? sc[n] : 0.0f;
     }
@@ -331,5 +377,7 @@ struct TokenRouter {
     __syncwarp();                                      // s_row is reused by the warp's next tokens
   }
 };
+
+using TokenRouter = TokenRouterT<2>;
 
 }  // namespace nvr

@@ -708,3 +708,43 @@ def test_no_cooperative_flag_routes_identically():
     b_ids, b_w = case.run(R.NVR_FLAG_NO_COOPERATIVE)
     assert R.last_router_plan()["sequence"] == "fused"
     assert np.array_equal(a_ids, b_ids) and np.array_equal(a_w.view(np.uint32), b_w.view(np.uint32))
+
+
+@pytest.mark.parametrize("N", [300, 384])
+@pytest.mark.parametrize("T", [8, 200])
+def test_exact_integer_logits_up_to_384_experts(N, T):
+    """The one-launch kernel for heads of 257-384 experts (two MMAs per K
+    step, N = 256 and N = 128, into 384 accumulator columns): grid-valued
+    operands give exact logits (any fp32 summation order), so the GPU must
+    equal the oracle's bits, the ragged last group included."""
+    import nvfp4_router_gate_gb300 as R
+    rng = np.random.default_rng(23)
+    D = 512
+    x = _grid_operands(rng, T, D, 0)
+    W = _grid_operands(rng, N, D, 1)
+    wf, ws, wg = R.nvfp4_pack_weight(to_device(W, "f32"))
+    xd = to_device(x, "f32").to(torch.bfloat16)        # the one-launch kernel takes bf16 x
+    assert torch.equal(xd.float().cpu(), torch.from_numpy(x))   # grid values are bf16-exact
+    out = R.router_gate_logits(xd, wf, ws, wg, flags=TC)
+    torch.cuda.synchronize()
+    assert R.last_router_plan()["sequence"] in ("fused", "amax+fused")
+    xq, xs, xg = Q.quantize(x)
+    wq, wsb, wgg = Q.quantize(W)
+    L, _ = gemm.logits(xq, xs, xg, wq, wsb, wgg)
+    assert np.array_equal(out.cpu().numpy().astype(np.float64), L)
+
+
+@pytest.mark.parametrize("N,T,k,raw", [(384, 129, 8, False), (300, 300, 16, False), (384, 2048, 8, False),
+                                       (384, 300, 1, True), (320, 40, 8, False)])
+def test_router_up_to_384_experts_all_rows(N, T, k, raw):
+    """Every row of prefill-like batches on heads of 257-384 experts through
+    the one-launch kernel (its plans: clusters of up to 16 CTAs, or 8 CTAs per
+    tile without clusters at T = 2048)."""
+    import nvfp4_router_gate_gb300 as R
+    w = WL.Workload("wide_gate", T, 7168, N, k, 1.0 if raw else 2.5, raw, "bf16", "lognormal_rows", 0.02,
+                    "uniform", 0.05)
+    case = Case(w)
+    ids, wts = case.run()
+    assert R.last_router_plan()["sequence"] == "fused"
+    res = case.check(ids, wts, np.arange(T))
+    assert compare.topk_ok(res), res

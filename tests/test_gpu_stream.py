@@ -68,13 +68,15 @@ def test_stream_router_256(T, k):
 
 
 @pytest.mark.parametrize("T", [16, 64, 100])
-def test_stream_router_default_for_wide_heads(T):
-    """Heads of more than 256 experts at up to 128 tokens take the streaming
-    kernel by default: the adversarial rows (all-zero rows tie every key at
-    0.5: ids 0..7; 1e4 rows saturate) on E = 384."""
+@pytest.mark.parametrize("flags", [0, ST])
+def test_wide_head_adversarial_small_batches(T, flags):
+    """The adversarial rows (all-zero rows tie every key at 0.5: ids 0..7;
+    1e4 rows saturate) on E = 384 at up to 128 tokens: by default the decode
+    kernel (T <= 16) or the one-launch kernel, forced the streaming kernel."""
     case = Case(WL.WORKLOADS["adversarial"].with_T(T))
-    ids, w = case.run()
-    assert _plan()["sequence"] == ("decode" if T <= 16 else "amax+quantize+stream"), _plan()
+    ids, w = case.run(flags)
+    want = "amax+quantize+stream" if flags else ("decode" if T <= 16 else "fused")
+    assert _plan()["sequence"] == want, _plan()
     res = case.check(ids, w, np.arange(T))
     assert compare.topk_ok(res), res
     zero = np.arange(1, T, 4)

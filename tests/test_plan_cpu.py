@@ -61,7 +61,11 @@ def test_decode_plans():
 def test_other_sequences():
     p = plan(4096, dtype="f32")
     assert p["sequence"] == "amax+quantize+splitk+epilogue" and p["ctas_per_tile"] == 4, p
+    # 257-384 experts with bf16 x: the one-launch kernel too (147 tiles of 112
+    # rows, one CTA each, all resident); fp32 x keeps the N-split path
     p = plan(16384, n=384)
+    assert (p["sequence"], p["tile_rows"], p["ctas_per_tile"]) == ("fused", 112, 1), p
+    p = plan(16384, n=384, dtype="f32")
     assert p["sequence"] == "amax+quantize+splitn" and p["tile_rows"] == 128, p
     p = plan(4096, flags=_native.NVR_FLAG_SPLIT_N)
     assert p["sequence"] == "amax+quantize+splitn", p
@@ -72,7 +76,10 @@ def test_other_sequences():
         assert (p["sequence"], p["tile_rows"], p["ctas_per_tile"]) == ("amax+quantize+stream", tn, SMS), (T, p)
     assert plan(129, n=129280)["sequence"] == "amax+quantize+splitn"
     p = plan(40, n=384)
+    assert (p["sequence"], p["tile_rows"], p["ctas_per_tile"]) == ("fused", 112, 16), p
+    p = plan(40, n=384, flags=_native.NVR_FLAG_STREAM)
     assert (p["sequence"], p["tile_rows"], p["ctas_per_tile"]) == ("amax+quantize+stream", 64, 3), p
+    assert plan(40, n=385)["sequence"] == "amax+quantize+stream"
     p = plan(100, flags=_native.NVR_FLAG_STREAM)
     assert (p["sequence"], p["ctas_per_tile"]) == ("amax+quantize+stream", 2), p
     assert plan(32, n=129280, flags=_native.NVR_FLAG_SPLIT_N)["sequence"] == "amax+quantize+splitn"
