@@ -565,7 +565,8 @@ def extra_rooflines(R, dev, stream, hbm, fp4_peak, traffic):
     ms = _timed_calls(lambda i: R.router_gate_topk(xa, Wf, Wsf, wg, bias, aw.k, aw.routed_scaling, out_ids=ids,
                                                    out_w=wt, workspace=ws), 50, stream)
     nbytes = aw.T * aw.D * 2 + aw.N * (aw.D // 2 + aw.D // 16) + aw.N * 4 + aw.T * aw.k * 8
-    out["adversarial"] = _hbm_entry(nbytes, ms, hbm, plan=R.last_router_plan(), tokens_per_s=aw.T / (ms / 1e3))
+    out["adversarial"] = _hbm_entry(nbytes, ms, hbm, plan=R.last_router_plan(), tokens_per_s=aw.T / (ms / 1e3),
+                                    traffic=traffic.get("fused_384"), traffic_kernel="fused_qgemm_kernel<112, 3>")
     del xa, Wa
     torch.cuda.empty_cache()
 
@@ -718,8 +719,9 @@ def profile_launches():
     the prefill router (fused_qgemm_kernel), the decode router at T = 1
     (decode_router_kernel), the N = 129280 raw head at T = 32 with k = 8 and
     as a bf16 linear (gemm_stream_kernel), the grouped expert GEMM and its
-    combine on the prefill routing (moe_* kernels) and the hash router.
-    Holds about 1.6 GB of device memory."""
+    combine on the prefill routing (moe_* kernels), the adversarial batch
+    (T = 16384, E = 384: the one-launch kernel for 384 experts) and the hash
+    router.  Holds about 2 GB of device memory."""
     import torch
     import nvfp4_router_gate_gb300 as R
     dev = torch.device("cuda", 0)
@@ -758,6 +760,13 @@ def profile_launches():
     for _ in range(2):
         y = R.nvfp4_moe_gemm(xp, ids, Ef, Esf, Eg, out_dtype=torch.bfloat16)
         R.nvfp4_moe_combine(y, wts)
+    aw = WL.WORKLOADS["adversarial"]
+    agate = R.RouterGate(bf16(WL.make_w(aw)), torch.from_numpy(WL.make_bias(aw)).to(dev), k=aw.k,
+                         routed_scaling=aw.routed_scaling, max_tokens=aw.T)
+    xa = bf16(WL.make_x(aw))
+    for _ in range(2):
+        agate(xa)
+    del xa, agate
     hw = WL.HASH_ROUTER
     table = torch.from_numpy(WL.make_hash_table(hw)).to(dev)
     tids = torch.from_numpy(WL.make_token_ids(hw)).to(dev)

@@ -20,12 +20,13 @@
 // device holds at once without clusters, meet at a barrier in the workspace
 // (tile_barrier) before routing.  Per CTA (rank r, 576 threads):
 //   warp 0      TMA producer.  With the in-kernel max|x| it first streams the
-//               CTA's contiguous 1/G slice of x (bulk copies of 32 KB into a
-//               6-slot ring laid over the other rings), then per stage of 256
-//               K-elements two bf16 x boxes (128 rows x 128 elements, 32 KB
-//               each) into a 3-slot ring, and the W tile (128 or 256 rows x
-//               128 bytes, 128-byte swizzle) with its scale slabs into a
-//               2-deep ring;
+//               CTA's own x boxes in reverse K order into a 5- or 6-slot
+//               ring laid over the other rings (the second pass then starts
+//               on the boxes read last, still in L2 where x is larger than
+//               L2), then per stage of 256 K-elements two bf16 x boxes (128
+//               rows x 128 elements, 32 KB each) into a 3-slot ring, and the
+//               W tile (128 kNT rows x 128 bytes, 128-byte swizzle) with its
+//               scale slabs into a 2-deep ring (kNT = 3: 1-deep);
 //   warps 2-17  quantizers (quant_box): warps 2-9 take the stage's first x
 //               box, warps 10-17 its second, 1/8 of the box rows per warp;
 //               they write the E2M1 codes into the A tile (128-byte swizzle,
@@ -38,16 +39,17 @@
 //               memory (tcgen05.cp, in order with the MMAs on the otherwise
 //               idle tensor pipe) and issues one tcgen05.mma.kind::mxf4nvf4
 //               (M=128, N=128 or 256, K=64) per 64-element K step into one
-//               fp32 accumulator;
-//   warps 2-17  after the last MMA: the fp32 partial (128 x 256) goes from
+//               fp32 accumulator (kNT = 3, 257-384 experts: an N=256 and an
+//               N=128 MMA into columns 0-255 and 256-383);
+//   warps 2-17  after the last MMA: the fp32 partial (128 x 128 kNT) goes from
 //               tensor memory to partial plane r of the workspace (L2); after a
 //               cluster (or tile) barrier each CTA routes its own 128/S tokens
 //               from the S planes, one warp per token (TokenRouter,
 //               nvr_splitk.cuh).
 // The quantizers are bound by the integer pipe: sixteen warps reach the same
 // throughput per SM as eight, but leave half as many rows per warp for the
-// epilogue.  Tensor memory: accumulator at columns 0-255; scales of A slot a
-// at 256 + 48 a (x: 4 columns per K step, W: 8).
+// epilogue.  Tensor memory: accumulator at columns 0 .. 128 kNT - 1; scales of
+// A slot a at 128 kNT + (16 + 16 kNT) a (x: 4 columns per K step, W: 4 kNT).
 #include <type_traits>
 
 #include "nvr_splitk.cuh"
@@ -75,9 +77,9 @@ constexpr int kFChunk = 32768;
 // 256, kNT = 3: up to 384).  The W tile of a stage holds 128 kNT rows x 128
 // bytes and kNT x 4 scale atoms; with kNT = 3 one stage is buffered (a W
 // tile comes from L2 in about 1 us while the quantizers take longer over a
-// stage), else two.  The max|x| pass streams the CTA's contiguous slice of x
-// in 32 KB chunks through a ring over the W, x and A rings (all idle until the
-// pass ends).
+// stage), else two.  The max|x| pass streams the CTA's x boxes (up to 32 KB
+// each) through a ring over the W, x and A rings (all idle until the pass
+// ends).
 template <int kNT>
 struct FusedCfg {
   static_assert(kNT == 2 || kNT == 3, "up to 256 or 384 experts");
@@ -106,7 +108,6 @@ static_assert(16 * 4096 <= kFXRing, "store staging fits the x ring");
 struct FusedParams {
   CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
   CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 x (128 * n_half)
-  const uint8_t* x;            // the same activations as bytes (the max|x| pass)
   float* qrec;                 // quantizer record {gsa, 1/gsa, mode, amax}: from the amax kernel, or
                                // published by this kernel's last CTA when amax_sync is set
   uint32_t* amax_sync;         // in-kernel amax: 5 workspace words (grid_amax), or null
@@ -458,11 +459,8 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   const int n_st = (KB + 15) / 16;                   // stages of 256 K-elements
   const int st0 = (rank * n_st) / p.S;
   const int my_st = ((rank + 1) * n_st) / p.S - st0;
-  // the max|x| pass: CTA b reads bytes [c_beg, c_end) of x (16-byte multiples)
-  const uint64_t x_bytes = static_cast<uint64_t>(p.T) * static_cast<uint64_t>(p.D) * 2u;
-  const uint64_t c_per = ((x_bytes + gridDim.x - 1) / gridDim.x + 15u) & ~uint64_t(15);
-  const uint64_t c_beg = min(x_bytes, c_per * blockIdx.x), c_end = min(x_bytes, c_beg + c_per);
-  const int n_chunks = static_cast<int>((c_end - c_beg + kFChunk - 1) / kFChunk);
+  // the max|x| pass reads the CTA's own 2 my_st x boxes, in reverse K order
+  const int n_chunks = 2 * my_st;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFStagesW; ++s) { mbar_init(full_w + s, 1); mbar_init(empty_w + s, 1); }
@@ -524,10 +522,12 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     uint32_t wph = 0;
     bool ok = true;
     int xi = 0;                                        // x boxes issued so far
-    // With the in-kernel amax, x streams twice: first the CTA's contiguous
-    // slice for the max (one pass over x in HBM), then, from L2, the CTA's
-    // boxes for the GEMM.  The second pass starts as soon as every chunk of
-    // the first has been consumed (the chunk ring overlays the other rings),
+    // With the in-kernel amax, x streams twice: the CTA's boxes for the max
+    // (one pass over x in HBM), then again for the GEMM.  The first pass
+    // takes them in reverse K order, so that the second starts on the boxes
+    // read last: where x is larger than L2 (T = 16384: 235 MB) those are the
+    // ones still there.  The second pass starts as soon as every box of the
+    // first has been consumed (the max-pass ring overlays the other rings),
     // its loads overlapping the grid barrier.
     if (p.amax_sync) {
       for (int c = 0; c < n_chunks; ++c) {
@@ -538,10 +538,10 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
           break;
         }
         if (elect_one()) {
-          const uint64_t off = c_beg + static_cast<uint64_t>(c) * kFChunk;
-          const uint32_t bytes = static_cast<uint32_t>(c_end - off < kFChunk ? c_end - off : kFChunk);
-          mbar_arrive_expect_tx(full_c + cs, bytes);
-          bulk_load(smem + cs * kFChunk, p.x + off, bytes, full_c + cs);
+          const int bi = n_chunks - 1 - c;             // box hs = bi % 2 of stage st0 + bi / 2
+          mbar_arrive_expect_tx(full_c + cs, kBoxBytes);
+          tma_load_2d(smem + cs * kFChunk, &p.tmap_x, (st0 + bi / 2) * 256 + (bi & 1) * 128, m_tile * kRows,
+                      full_c + cs);
         }
         __syncwarp();
         filled_c |= 1u << cs;
@@ -672,12 +672,11 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         const bool okc = __all_sync(0xFFFFFFFFu, mbar_wait(full_c + cs, cph, deadline, abort_flag));
         ok = ok && okc;
         if (okc) {
-          // warp q16 reads the chunk's 16-byte words q16 * 32 + lane + 512 i
-          const uint64_t left = c_end - c_beg - static_cast<uint64_t>(c) * kFChunk;
-          const uint32_t bytes = static_cast<uint32_t>(left < kFChunk ? left : kFChunk);
+          // warp q16 reads the box's 16-byte words q16 * 32 + lane + 512 i
+          // (rows past T and columns past D are zeros)
           const uint8_t* cb = smem + cs * kFChunk;
-#pragma unroll 8
-          for (uint32_t o = (q16 * 32 + lane) * 16u; o < bytes; o += kFQThreads * 16u)
+#pragma unroll 4
+          for (uint32_t o = (q16 * 32 + lane) * 16u; o < kBoxBytes; o += kFQThreads * 16u)
             m = max(m, absmax_bits16B<true>(ld_shared_v4(cb + o)));
         }
         __syncwarp();
@@ -1026,7 +1025,6 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   const int nt = N > 256 ? 3 : 2;
   if (!encode_x(&g.tmap_x, x, T, D, static_cast<uint32_t>(tile_rows))) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes(&g.tmap_b, W_codes, N, D, nt == 2 ? 128u * n_groups : 128u)) return NVR_ERR_UNSUPPORTED;
-  g.x = reinterpret_cast<const uint8_t*>(x);
   g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
   g.amax_sync = amax_sync; g.tile_sync = tile_sync; g.flat = flat ? 1 : 0; g.gsa_out = x_gsa;
   g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_groups = n_groups; g.S = S;
