@@ -356,9 +356,8 @@ nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
  * the process exits.  That is the most the decode kernel's shared-memory plan
  * lets a call need (T * N * 8 bytes of keys and scores, the same bound); a
  * larger shape is refused by the plan (NVR_ERR_UNSUPPORTED).  It calls no
- * cudaMalloc/cudaFree.  Each call is two operations on `stream`: a
- * cudaMemsetAsync that clears the 256 control bytes (the ticket), then the
- * decode kernel.
+ * cudaMalloc/cudaFree.  Each call is one kernel launch on `stream` (the
+ * ticket starts at zero and every launch leaves it at zero).
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) and caches it; make that first call before any
  *   stream capture.

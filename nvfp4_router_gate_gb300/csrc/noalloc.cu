@@ -88,8 +88,10 @@ extern "C" nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int6
   uint8_t* scratch = scratch_for_current_device(&e);
   if (!scratch) return NVR_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the ticket must start at zero whatever an earlier call left behind
-  if (cudaMemsetAsync(scratch, 0, kNoAllocControl, s) != cudaSuccess) return NVR_ERR_CUDA;
+  // The ticket starts at zero (a __device__ array is zero-initialised) and
+  // the decode kernel puts it back to zero on every path it takes, so each
+  // call is the one launch (which programmatic launch can overlap with its
+  // predecessor's tail inside a graph).
   float* keys = reinterpret_cast<float*>(scratch + kNoAllocControl);
   float* scores = keys + T * N;
   e = launch_decode(x, dt == NVR_BF16, T, D, W_fp4, W_scales, w_gsa, N, bias, k, routed_scaling,

@@ -748,3 +748,17 @@ def test_router_up_to_384_experts_all_rows(N, T, k, raw):
     assert R.last_router_plan()["sequence"] == "fused"
     res = case.check(ids, wts, np.arange(T))
     assert compare.topk_ok(res), res
+
+
+def test_router_384_experts_two_launch_plan():
+    """More token tiles than the GPU holds at once (T = 20000: 157 tiles of
+    128 rows > 152 CTAs): the amax kernel, then the fused kernel for 384
+    experts reading its record; every row against the oracle."""
+    import nvfp4_router_gate_gb300 as R
+    w = WL.Workload("wide_gate_large", 20000, 7168, 384, 8, 2.5, False, "bf16", "lognormal_rows", 0.02,
+                    "uniform", 0.05)
+    case = Case(w)
+    ids, wts = case.run()
+    assert R.last_router_plan()["sequence"] == "amax+fused", R.last_router_plan()
+    res = case.check(ids, wts, np.arange(w.T))
+    assert compare.topk_ok(res), res
