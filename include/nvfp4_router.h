@@ -102,7 +102,8 @@ enum {
   NVR_FLAG_FORCE_TENSOR_CORE = 2u,
   NVR_FLAG_FORCE_DECODE = 4u,
   /* Tensor-core kernel choice (each implies FORCE_TENSOR_CORE; at most one).
-   * By default heads of up to 256 experts split K over a cluster of S CTAs
+   * By default heads of up to 256 experts (bf16 x: 384) split K over a
+   * cluster of S CTAs
    * per token tile (S and the tile height, 128 or 112 rows, from T, D and
    * the number of clusters the device holds at once; fp32 partial logits
    * pass through the workspace, L2-resident, to the CTAs of the same
@@ -118,7 +119,8 @@ enum {
   /* Forces the weight-streaming kernel (T <= 128; NVR_ERR_UNSUPPORTED for
    * more tokens): the 128-row weight tiles are the MMA's M and the tokens its
    * N, the weight is read once, per-token top-k lists are merged across CTAs.
-   * The default for heads of more than 256 experts at T <= 128. */
+   * The default for heads of more than 384 experts (fp32 x: 256) at
+   * T <= 128. */
   NVR_FLAG_STREAM = 128u,
   /* The one-launch prefill router is launched cooperatively by default (the
    * runtime then guarantees that its whole grid is resident at once, which
@@ -317,7 +319,7 @@ size_t router_gate_x_gsa_offset(void);
  *   - T <= 16 (decode): one kernel; for T >= 2 its CTAs form clusters of 4
  *     that share the staging and quantization of x through distributed
  *     shared memory.
- *   - bf16 x, N <= 256: one kernel that takes max|x| itself (a bounded grid
+ *   - bf16 x, N <= 384: one kernel that takes max|x| itself (a bounded grid
  *     barrier in the workspace, or an exchange through distributed shared
  *     memory when the grid is one cluster), quantizes x inside the K-split
  *     GEMM and routes each tile's tokens from the fp32 partial logits
@@ -327,11 +329,13 @@ size_t router_gate_x_gsa_offset(void);
  *     amax kernel runs first and the same kernel skips its own max|x| pass.
  *   - fp32 x, N <= 256: amax, quantize, K-split GEMM and a warp-per-token
  *     epilogue kernel.
- *   - N > 256, T <= 128: amax, quantize and the weight-streaming GEMM (the
+ *   - N > 384 (fp32 x: N > 256), T <= 128: amax, quantize and the
+ *     weight-streaming GEMM (the
  *     weight rows are the MMA's M, the tokens its N; each weight byte is read
  *     once), which routes from the logits in tensor memory and merges the
  *     CTAs' per-token lists in its last CTA.
- *   - N > 256, T > 128: amax, quantize and the N-split GEMM, which routes
+ *   - N > 384 (fp32 x: N > 256), T > 128: amax, quantize and the N-split
+ *     GEMM, which routes
  *     from the logits in tensor memory.
  */
 nvr_status router_gate_topk(const void* x, nvr_dtype dt, int64_t T, int64_t D,
