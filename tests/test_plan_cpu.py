@@ -152,3 +152,12 @@ def test_plan_query_rejects_bad_arguments():
         assert L.nvr_plan_router(*args) == _native.NVR_ERR_INVALID_ARG, args
     assert L.nvr_plan_router(64, D, 384, _native.NVR_BF16, _native.NVR_FLAG_SPLIT_K_4, SMS, caps, BLOCKS,
                              out) == _native.NVR_ERR_UNSUPPORTED
+
+
+def test_tiny_fp32_router_is_one_launch():
+    """The fp32 tiny router (T = 4, D = 256, E = 16) runs the single-launch
+    decode kernel: one launch for fp32 activations too, at decode sizes."""
+    _lib()
+    import nvfp4_router_gate_gb300 as R
+    p = R.plan_router(4, 256, 16, num_sms=SMS, cluster_capacity=CAPS, block_capacity=BLOCKS, dtype="f32", flags=0)
+    assert p["sequence"] == "decode", p
