@@ -716,7 +716,8 @@ def run_reference(args, rank):
 def profile_launches():
     """One warm-up call and one measured call of every hot path, for a
     profiler's launch filter (each call reads its inputs cold under ncu):
-    the prefill router (fused_qgemm_kernel), the decode router at T = 1
+    the prefill router (fused_qgemm_kernel), the standalone quantizer on the
+    prefill batch (amax_bulk_kernel, quantize_kernel), the decode router at T = 1
     (decode_router_kernel), the N = 129280 raw head at T = 32 with k = 8 and
     as a bf16 linear (gemm_stream_kernel), the grouped expert GEMM and its
     combine on the prefill routing (moe_* kernels), the adversarial batch
@@ -737,6 +738,14 @@ def profile_launches():
                         routed_scaling=pw.routed_scaling, max_tokens=pw.T)
     for _ in range(2):
         ids, wts = gate(xp)
+    # the standalone quantizer on the prefill batch (amax_bulk_kernel, quantize_kernel)
+    codes = torch.empty((pw.T, pw.D // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty(R.nvr_sf_bytes(pw.T, pw.D, "tiled"), dtype=torch.uint8, device=dev)
+    gsa = torch.empty(1, dtype=torch.float32, device=dev)
+    wsq = R.new_workspace(R.nvfp4_quantize_workspace_size(pw.T, pw.D), dev)
+    for _ in range(2):
+        R.nvfp4_quantize_act(xp, "tiled", codes, sf, gsa, wsq)
+    del codes, sf
     dw = WL.WORKLOADS["decode"]
     dgate = R.RouterGate(bf16(WL.make_w(dw)), torch.from_numpy(WL.make_bias(dw)).to(dev), k=dw.k,
                          routed_scaling=dw.routed_scaling, max_tokens=1)

@@ -24,7 +24,7 @@ constexpr float kGsaDivisor = 2688.0f;     // 6 (E2M1 max) * 448 (E4M3 max)
 constexpr int kWsStatus = 0;
 constexpr int kWsAmaxTicket = 4;
 constexpr int kWsDecodeTicket = 8;
-constexpr int kWsAmaxChunk = 12;           // amax: next chunk to claim
+// (byte 12 is unused)
 constexpr int kWsFusedAmax = 16;           // fused router's in-kernel amax: 5 words (2 maxima, 2 arrivals, generation)
 constexpr uint32_t kStatusTimeout = 6;     // == NVR_ERR_TIMEOUT
 

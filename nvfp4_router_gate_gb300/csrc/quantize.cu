@@ -82,13 +82,14 @@ amax_kernel(const void* __restrict__ x, int64_t n_vec16, uint32_t* __restrict__ 
 }
 
 // The same reduction fed by bulk copies: a persistent grid (one CTA per SM)
-// streams 32 KB chunks through a 4-stage shared-memory ring; one thread issues
-// cp.async.bulk for the chunks ahead while all threads reduce the landed
-// ones.  Chunks are claimed from a counter in the workspace, so CTAs that
-// start early (on SMs the previous kernel left free) take more of them.
-// Bulk copies keep far more bytes in flight per SM than per-thread loads,
-// which is what a pure HBM stream needs.  Waits on the ring are bounded
-// (about a second); a timeout is recorded in the status word.
+// streams 32 KB chunks through a 6-stage shared-memory ring (192 KB in flight
+// per SM); one thread issues cp.async.bulk for the chunks ahead while all
+// threads reduce the landed ones.  CTA b takes chunks b, b + G, b + 2G, ...
+// (G CTAs): the refill of a stage needs no claim from a counter in memory,
+// whose round trip to L2 per chunk halved the stream rate.  Bulk copies keep
+// far more bytes in flight per SM than per-thread loads, which is what a pure
+// HBM stream needs.  Waits on the ring are bounded (about a second); a
+// timeout is recorded in the status word.
 //
 // Launched with programmatic dependent launch: the grid may become resident
 // while the previous kernel of the stream finishes, but it waits for it
@@ -97,61 +98,53 @@ amax_kernel(const void* __restrict__ x, int64_t n_vec16, uint32_t* __restrict__ 
 // workspace.  Each CTA lets the next kernel launch once its share of x has
 // been read.
 constexpr int kAmaxChunk = 32 * 1024;
-constexpr int kAmaxStages = 4;
+constexpr int kAmaxStages = 6;
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kAmaxThreads, 1)
 amax_bulk_kernel(const uint8_t* __restrict__ x, int64_t nbytes, uint32_t* __restrict__ partials,
-                 uint32_t* __restrict__ ticket, uint32_t* __restrict__ chunk_ctr, float* __restrict__ gsa_out,
-                 float* __restrict__ qrec, uint32_t* __restrict__ status) {
+                 uint32_t* __restrict__ ticket, float* __restrict__ gsa_out, float* __restrict__ qrec,
+                 uint32_t* __restrict__ status) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[kAmaxStages];
-  __shared__ int64_t s_chunk[kAmaxStages];       // chunk held by each stage (>= n_chunks: none)
   __shared__ uint32_t red[kAmaxThreads / 32];
   __shared__ bool last;
   const int64_t n_chunks = (nbytes + kAmaxChunk - 1) / kAmaxChunk;
-  auto grab_and_issue = [&](int st, int (&fills)[kAmaxStages]) {   // thread 0: next chunk for stage st
-    const int64_t c = atomicAdd(chunk_ctr, 1u);
-    s_chunk[st] = c;
-    if (c < n_chunks) {
-      ++fills[st];
-      const int64_t off = c * kAmaxChunk;
-      const uint32_t bytes = static_cast<uint32_t>(nbytes - off < kAmaxChunk ? nbytes - off : kAmaxChunk);
-      mbar_arrive_expect_tx(full + st, bytes);
-      bulk_load(ring + st * kAmaxChunk, x + off, bytes, full + st);
-    }
+  const int64_t my_n = n_chunks > blockIdx.x ? (n_chunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto issue = [&](int64_t j, int (&fills)[kAmaxStages]) {     // thread 0: this CTA's chunk j
+    const int st = static_cast<int>(j % kAmaxStages);
+    const int64_t off = (blockIdx.x + j * gridDim.x) * static_cast<int64_t>(kAmaxChunk);
+    const uint32_t bytes = static_cast<uint32_t>(nbytes - off < kAmaxChunk ? nbytes - off : kAmaxChunk);
+    ++fills[st];
+    mbar_arrive_expect_tx(full + st, bytes);
+    bulk_load(ring + st * kAmaxChunk, x + off, bytes, full + st);
   };
-  int fills[kAmaxStages] = {0, 0, 0, 0};           // thread 0: copies issued per stage
+  int fills[kAmaxStages] = {0, 0, 0, 0, 0, 0};     // thread 0: copies issued per stage
   if (threadIdx.x == 0) {
     for (int st = 0; st < kAmaxStages; ++st) mbar_init(full + st, 1);
     fence_mbar_init();
   }
   // x and the workspace counters may be written by the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < kAmaxStages; ++st) grab_and_issue(st, fills);
-  }
+  if (threadIdx.x == 0)
+    for (int64_t j = 0; j < kAmaxStages && j < my_n; ++j) issue(j, fills);
   __syncthreads();
   const uint64_t deadline = globaltimer_ns() + 1000000000ull;
   volatile int never = 0;
   uint32_t m = 0;
   bool ok = true;
-  for (int64_t i = 0;; ++i) {
-    const int st = static_cast<int>(i % kAmaxStages);
-    const int64_t c = s_chunk[st];
-    // claims only grow, so the first exhausted stage ends the walk
-    if (c >= n_chunks) break;
-    const uint32_t parity = static_cast<uint32_t>((i / kAmaxStages) & 1);
+  for (int64_t j = 0; j < my_n; ++j) {
+    const int st = static_cast<int>(j % kAmaxStages);
+    const uint32_t parity = static_cast<uint32_t>((j / kAmaxStages) & 1);
     ok = __syncthreads_and(mbar_wait(full + st, parity, deadline, &never)) != 0;
     if (!ok) break;
-    const int64_t off = c * static_cast<int64_t>(kAmaxChunk);
+    const int64_t off = (blockIdx.x + j * gridDim.x) * static_cast<int64_t>(kAmaxChunk);
     const int nvec = static_cast<int>((nbytes - off < kAmaxChunk ? nbytes - off : kAmaxChunk) / 16);
     const uint4* v = reinterpret_cast<const uint4*>(ring + st * kAmaxChunk);
-#pragma unroll 4
+#pragma unroll 8
     for (int u = threadIdx.x; u < nvec; u += kAmaxThreads) m = max(m, absmax_bits16B<kBF16>(v[u]));
     __syncthreads();                               // the stage has been read
-    if (threadIdx.x == 0) grab_and_issue(st, fills);
-    __syncthreads();                               // its new chunk id is visible
+    if (threadIdx.x == 0 && j + kAmaxStages < my_n) issue(j + kAmaxStages, fills);
   }
   if (!ok) {
     // wait (bounded) for this CTA's copies still in flight, then give up
@@ -200,8 +193,7 @@ amax_bulk_kernel(const uint8_t* __restrict__ x, int64_t nbytes, uint32_t* __rest
     qrec[1] = qs.rgsa;
     qrec[2] = __int_as_float(qs.mode);
     qrec[3] = amax;
-    *ticket = 0u;
-    *chunk_ctr = 0u;                               // ready for the next call
+    *ticket = 0u;                                  // ready for the next call
   }
 }
 
@@ -283,7 +275,6 @@ cudaError_t launch_amax_bulk(const void* x, bool bf16, int64_t n_elems, uint32_t
   }
   const int64_t nbytes = n_elems * (bf16 ? 2 : 4);
   const uint8_t* xb = static_cast<const uint8_t*>(x);
-  uint32_t* chunk_ctr = ticket + (kWsAmaxChunk - kWsAmaxTicket) / 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kAmaxThreads);
@@ -295,10 +286,8 @@ cudaError_t launch_amax_bulk(const void* x, bool bf16, int64_t n_elems, uint32_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (bf16)
-    return cudaLaunchKernelEx(&cfg, amax_bulk_kernel<true>, xb, nbytes, partials, ticket, chunk_ctr, gsa_out, qrec,
-                              status);
-  return cudaLaunchKernelEx(&cfg, amax_bulk_kernel<false>, xb, nbytes, partials, ticket, chunk_ctr, gsa_out, qrec,
-                            status);
+    return cudaLaunchKernelEx(&cfg, amax_bulk_kernel<true>, xb, nbytes, partials, ticket, gsa_out, qrec, status);
+  return cudaLaunchKernelEx(&cfg, amax_bulk_kernel<false>, xb, nbytes, partials, ticket, gsa_out, qrec, status);
 }
 
 cudaError_t launch_quantize(const void* x, bool bf16, int64_t rows, int64_t D, bool tiled,
