@@ -220,7 +220,7 @@ struct RouterPlan {
 // and block_cap of its CTAs without clusters.  Host arithmetic only: the
 // dispatch and nvr_plan_router both call it.  flags: normalised.
 //
-// The fused kernel (bf16, <= 256 experts): token tiles of 128 or 112 rows,
+// The fused kernel (bf16, <= 384 experts): token tiles of 128 or 112 rows,
 // S CTAs per tile (S a power of two no larger than the K-split plan; each CTA
 // routes rows/S tokens) that form a cluster or, without clusters, meet at a
 // barrier in the workspace.  Among the grids resident at once the one with

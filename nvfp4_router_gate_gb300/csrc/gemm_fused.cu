@@ -1,4 +1,4 @@
-// gemm_fused.cu -- the router for up to 256 experts on bf16 activations in one
+// gemm_fused.cu -- the router for up to 384 experts on bf16 activations in one
 // launch: max|x| over the CTAs' own x boxes and a grid barrier (or, when the
 // grid cannot be resident at once, the amax kernel launched before), then the
 // runtime NVFP4 quantization of x inside a K-split tensor-core GEMM and the
@@ -107,7 +107,7 @@ static_assert(16 * 4096 <= kFXRing, "store staging fits the x ring");
 
 struct FusedParams {
   CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
-  CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 x (128 * n_half)
+  CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 bytes x 128 n_groups rows (kNT = 3: 128)
   float* qrec;                 // quantizer record {gsa, 1/gsa, mode, amax}: from the amax kernel, or
                                // published by this kernel's last CTA when amax_sync is set
   uint32_t* amax_sync;         // in-kernel amax: 5 workspace words (grid_amax), or null
@@ -445,7 +445,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   uint64_t* q_done = a_empty + kFASlots;                               // [kFASlots]
   uint64_t* acc_full = q_done + kFASlots;
   uint64_t* amax_mbar = acc_full + 1;           // one-cluster grids: the S CTAs' maxima have landed
-  uint64_t* full_c = amax_mbar + 1;             // [kFChunkSlots] max|x| pass chunk ring
+  uint64_t* full_c = amax_mbar + 1;             // [kFChunkSlots] max|x| pass ring
   uint64_t* empty_c = full_c + kFChunkSlots;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(empty_c + kFChunkSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -460,7 +460,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
   const int st0 = (rank * n_st) / p.S;
   const int my_st = ((rank + 1) * n_st) / p.S - st0;
   // the max|x| pass reads the CTA's own 2 my_st x boxes, in reverse K order
-  const int n_chunks = 2 * my_st;
+  const int n_chunks = 2 * my_st;                    // boxes of the max|x| pass
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFStagesW; ++s) { mbar_init(full_w + s, 1); mbar_init(empty_w + s, 1); }

@@ -107,7 +107,8 @@ nvr_status launch_gemm_stream(const uint8_t* x_codes, const uint8_t* x_sf, const
 
 // Router for N <= 256: the GEMM split along K over S CTAs (fp32 partials in
 // the workspace), then the warp-per-token epilogue kernel.
-// splitk_partial_rows(T): rows (of 256 fp32) the partial region holds for T
+// splitk_partial_rows(T): rows (of 256 fp32; 384 for the fused kernel's
+// 257-384-expert heads, whose partial region is sized accordingly) the partial region holds for T
 // tokens, an upper bound of S * T_pad for every S plan_splitk picks on a GPU
 // with at most 256 SMs; plan_splitk: S for T tokens.
 constexpr int kMaxSplitK = 16;
@@ -116,7 +117,7 @@ int plan_splitk(int64_t T, int64_t D, int num_sms);
 nvr_status launch_splitk_gemm(const uint8_t* x_codes, const uint8_t* x_sf, int64_t T, int64_t D,
                               const uint8_t* W_codes, const uint8_t* W_sf, int64_t N, float* partials,
                               uint32_t* status, int S, bool test_stall, cudaStream_t s);
-// The router for bf16 activations and N <= 256 in one kernel: quantization
+// The router for bf16 activations and N <= 384 in one kernel: quantization
 // inside the K-split GEMM, partials through L2 and the epilogue (S CTAs per
 // token tile of tile_rows = 128 or 112 rows, S in {1,2,4,8,16}).  With
 // amax_sync (5 zeroed workspace words) the kernel also computes max|x| itself
