@@ -40,7 +40,8 @@
 // token and appends only its entries at or above the bound to the token's
 // candidates in the workspace, then takes a ticket; the last CTA (no
 // waiting) selects each token's k best from its candidates -- a superset of
-// them, a few per k once the bound has risen -- one warp per token,
+// them, a few per k once the bound has risen -- one warp per token (with at
+// most 32 candidates each lane ranks one of them against the others),
 // renormalises and writes ids and weights.
 //
 // Tensor memory (512 columns): kNacc accumulators of TN columns from column
@@ -104,7 +105,7 @@ __device__ __forceinline__ uint32_t bf16_rn_bits(float v) {
 // holds the best word published among ids = r (mod 32), so the k largest
 // slot words are k distinct entries and the k-th largest of them is at most
 // the token's k-th best (0 while fewer than k slots are set).  The words are
-// read from shared memory (stage_slot_words) in a loop that is not unrolled:
+// read from shared memory (copied there asynchronously) in a loop that is not unrolled:
 // this runs once per CTA, and compact code matters more there than
 // instruction-level parallelism.
 template <int KMAX>
@@ -127,14 +128,6 @@ __device__ __forceinline__ unsigned long long slot_bound(const unsigned long lon
   for (int i = 0; i < KMAX; ++i)
     if (i + 1 == k) b = top[i];
   return b;
-}
-
-// The slot words of tokens [0, T) into shared memory (T x 32 words), by the
-// `n` threads with index `i0` (16-byte loads from L2, all in flight at once).
-__device__ __forceinline__ void stage_slot_words(unsigned long long* s_words, const unsigned long long* slots, int T,
-                                                 int i0, int n) {
-  for (int i = i0; i < T * 16; i += n)
-    reinterpret_cast<ulonglong2*>(s_words)[i] = __ldcg(reinterpret_cast<const ulonglong2*>(slots) + i);
 }
 
 template <int TN, int KMAX, bool kLogits>
@@ -410,6 +403,21 @@ gemm_stream_kernel(const __grid_constant__ StreamParams p) {
       if (et == 0) *epi_abort = *abort_flag;
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (!*epi_abort) {
+        // The token slots' words (see below) start on their way into the ring
+        // now, past the lists of the group merge, so that their round trip
+        // to L2 overlaps the merge: the ring is idle (every copy into it has
+        // landed, since the MMAs of the last tile have read them).  The
+        // snapshot is a few microseconds older than after the merge, so its
+        // bound may be a little lower -- still a valid lower bound.
+        unsigned long long* s_words = reinterpret_cast<unsigned long long*>(smem + 65536);
+        if (p.n_splits > 1) {
+          for (int i = et; i < p.T * 16; i += kSEpi)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::
+                         "r"(smem_u32(reinterpret_cast<ulonglong2*>(s_words) + i)),
+                         "l"(reinterpret_cast<uint64_t>(reinterpret_cast<const ulonglong2*>(p.tok_slots) + i))
+                         : "memory");
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        }
         // the kSEpi / TN groups of a token merge in a tree: in each round the
         // upper half of the groups hands its lists through shared memory (the
         // ring: every copy into it has landed, since the MMAs of the last
@@ -457,9 +465,8 @@ gemm_stream_kernel(const __grid_constant__ StreamParams p) {
           // best, so an entry below g cannot be among its k best: only the
           // prefix of the sorted list at or above g is appended to the
           // token's candidates.
-          // the ring past the lists of the group merge holds the slot words
-          unsigned long long* s_words = reinterpret_cast<unsigned long long*>(smem + 65536);
-          stage_slot_words(s_words, p.tok_slots, p.T, et, kSEpi);
+          // the slot words issued before the merge
+          asm volatile("cp.async.wait_all;" ::: "memory");
           asm volatile("bar.sync 1, 256;" ::: "memory");
           if (grp == 0 && tok_ok) {
             const unsigned long long g = slot_bound<KMAX>(s_words + tok * 32, p.k);
@@ -473,9 +480,16 @@ gemm_stream_kernel(const __grid_constant__ StreamParams p) {
             for (int i = 0; i < KMAX; ++i)
               if (i < n) dst[i] = make_float4(tk.key[i], __int_as_float(tk.id[i]), tk.sc[i], 0.f);
           }
-          __threadfence();
+          // The barrier orders the epilogue threads' appends before thread
+          // 0's ticket, an acquire-release atomic at gpu scope: it publishes
+          // them (release, cumulative over the barrier) and, in the last
+          // CTA, makes every other CTA's appends visible (acquire).
           asm volatile("bar.sync 1, 256;" ::: "memory");
-          if (et == 0) *last_flag = atomicAdd(p.ticket, 1u) == static_cast<uint32_t>(p.n_splits - 1) ? 1 : 0;
+          if (et == 0) {
+            uint32_t old;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ticket) : "memory");
+            *last_flag = old == static_cast<uint32_t>(p.n_splits - 1) ? 1 : 0;
+          }
           asm volatile("bar.sync 1, 256;" ::: "memory");
         }
       }
@@ -510,9 +524,44 @@ gemm_stream_kernel(const __grid_constant__ StreamParams p) {
     }
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     __syncthreads();
+    // a warp's k winners by rank (id, score), for the sum in rank order
+    float2* s_win = reinterpret_cast<float2*>(s_cnt + 128) + warp * KMAX;
 #pragma unroll 1
     for (int tt = warp; tt < p.T; tt += kWarps) {
       const int cnt = static_cast<int>(s_cnt[tt]);
+      if (KMAX > 1 && cnt <= 32) {
+        // At most one candidate per lane (the usual case: the bound lets a
+        // few per k through): each lane's rank among the token's candidates
+        // (key descending, lower id first; the ids are distinct) is the
+        // number of them that beat it, counted over broadcast reads -- no
+        // serial rounds.  The winners land at their rank, so the weights'
+        // sum runs in rank order whatever order the candidates came in.
+        const float4* cand = s_first + tt * 32;
+        const bool has = lane < cnt;
+        const float4 v = has ? cand[lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        const int vid = __float_as_int(v.y);
+        int rank = 0;
+#pragma unroll 4
+        for (int q = 0; q < cnt; ++q) {
+          const float4 u = cand[q];
+          rank += topk_better(u.x, __float_as_int(u.y), v.x, vid) ? 1 : 0;
+        }
+        if (has && rank < p.k) s_win[rank] = make_float2(__int_as_float(vid), v.z);
+        __syncwarp();
+        const bool mine = lane < p.k && lane < cnt;
+        const float2 w = mine ? s_win[lane] : make_float2(__int_as_float(0x7FFFFFFF), 0.f);
+        float sum = mine ? w.y : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+        if (lane < p.k) {
+          p.out_ids[tt * p.k + lane] = __float_as_int(w.x);
+          p.out_w[tt * p.k + lane] =
+              p.raw ? w.y : (sum > 0.0f ? __fdiv_rn(__fmul_rn(p.routed_scaling, w.y), sum) : 0.0f);
+        }
+        if (lane == 0) p.tok_count[tt] = 0u;
+        __syncwarp();                                  // s_win is reused by the warp's next token
+        continue;
+      }
       TopK<KMAX> mine;
       mine.init();
       if (lane < cnt) {
