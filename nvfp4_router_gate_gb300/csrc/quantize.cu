@@ -21,9 +21,8 @@
 
 namespace nvr {
 
-// Per-call quantizer constants published by the amax kernel's last CTA:
-// {gsa, RN(1/gsa), division mode (as int bits), amax}.
-constexpr int kQrecWords = 4;
+// The amax kernel's last CTA publishes the per-call quantizer record `qrec`:
+// four words {gsa, RN(1/gsa), division mode (as int bits), amax}.
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kAmaxThreads, 4)
