@@ -136,8 +136,11 @@ enum {
   /* Failure-detection test hook (with FORCE_TENSOR_CORE or a SPLIT flag): the tensor-core
    * kernel's MMA issuer issues nothing, so its bounded waits run out after
    * about one second; the kernel stores NVR_ERR_TIMEOUT in the workspace
-   * status word, releases its tensor memory and returns.  The call itself
-   * returns NVR_OK (the failure is on the device); outputs are unspecified. */
+   * status word, releases its tensor memory and returns.  With FORCE_DECODE
+   * (up to 256 experts): the decode CTAs other than the collector store no
+   * keys, so the collector's poll runs out after about one second and stores
+   * NVR_ERR_TIMEOUT.  The call itself returns NVR_OK (the failure is on the
+   * device); outputs are unspecified. */
   NVR_FLAG_TEST_STALL = 1u << 30
 };
 
@@ -307,7 +310,8 @@ size_t router_gate_x_gsa_offset(void);
  *   routed_scaling  multiplies the renormalised weights
  *   flags        0 or NVR_FLAG_RAW_LOGITS, optionally with one kernel-choice
  *                flag (FORCE_TENSOR_CORE, FORCE_DECODE, SPLIT_K_2/4/8,
- *                SPLIT_N, STREAM) and, with a tensor-core choice, TEST_STALL
+ *                SPLIT_N, STREAM) and, with a tensor-core choice or
+ *                FORCE_DECODE, TEST_STALL
  *   out_ids      out [T, k] int32: expert ids, best first (key descending,
  *                equal keys: lower id first)
  *   out_w        out [T, k] fp32: routed_scaling * s_id / sum of the k

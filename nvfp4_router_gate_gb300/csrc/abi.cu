@@ -75,7 +75,8 @@ WsLayout router_ws_layout(int64_t T, int64_t D, int64_t N) {
   // regions may cover the words another call expects at zero.
   L.tickets = L.total;
   L.tile_sync = a256(L.tickets + static_cast<size_t>(kMaxTicketTiles) * 4);
-  L.x_codes = a256(L.tile_sync + static_cast<size_t>(kMaxFlatTiles) * 8);
+  L.dec_words = a256(L.tile_sync + static_cast<size_t>(kMaxFlatTiles) * 8);
+  L.x_codes = a256(L.dec_words + static_cast<size_t>(kDecodeWords) * 8);
   L.x_sf = a256(L.x_codes + static_cast<size_t>(rows_pad) * (D / 2));
   L.partials = a256(L.x_sf + static_cast<size_t>(rows_pad) * (D / 16));
   const int splits = split_bound(m_tiles, n_tiles);
@@ -201,7 +202,8 @@ nvr_status normalize_flags(uint32_t& flags) {
   if (kernel_flags & (kernel_flags - 1)) return NVR_ERR_INVALID_ARG;          // at most one
   if (kernel_flags) flags |= NVR_FLAG_FORCE_TENSOR_CORE;
   if ((flags & NVR_FLAG_FORCE_TENSOR_CORE) && (flags & NVR_FLAG_FORCE_DECODE)) return NVR_ERR_INVALID_ARG;
-  if ((flags & NVR_FLAG_TEST_STALL) && !(flags & NVR_FLAG_FORCE_TENSOR_CORE)) return NVR_ERR_INVALID_ARG;
+  if ((flags & NVR_FLAG_TEST_STALL) && !(flags & (NVR_FLAG_FORCE_TENSOR_CORE | NVR_FLAG_FORCE_DECODE)))
+    return NVR_ERR_INVALID_ARG;
   return NVR_OK;
 }
 
@@ -361,9 +363,13 @@ nvr_status router_impl(const void* x, nvr_dtype dt, int64_t T, int64_t D, const 
     float* scores = keys + T * N;
     ProfileScope prof(s);
     prof.before();
+    // up to 256 experts CTA 0 collects the keys from the fixed words region
+    uint64_t* words = N <= 256 ? reinterpret_cast<uint64_t*>(w + L.dec_words) : nullptr;
     cudaError_t e = launch_decode(x, bf16, T, D, W_fp4, W_sf, w_gsa, N, bias, k, routed_scaling, raw,
                                   out_ids, out_w, logits, keys, scores,
-                                  reinterpret_cast<uint32_t*>(w + kWsDecodeTicket), rp.dp, s);
+                                  reinterpret_cast<uint32_t*>(w + kWsDecodeTicket), words,
+                                  reinterpret_cast<uint32_t*>(w + kWsStatus),
+                                  (flags & NVR_FLAG_TEST_STALL) != 0, rp.dp, s);
     prof.after();
     return cuda_status(e);
   }
@@ -534,9 +540,9 @@ size_t router_gate_workspace_size(int64_t T_max, int64_t D, int64_t N, int k) {
   }
   const int64_t t_dec = T_max < 16 ? T_max : 16;
   return quantize_ws_layout(T_max, D).total + static_cast<size_t>(kMaxTicketTiles) * 4 +
-         static_cast<size_t>(kMaxFlatTiles) * 8 +
+         static_cast<size_t>(kMaxFlatTiles) * 8 + static_cast<size_t>(kDecodeWords) * 8 +
          static_cast<size_t>(rows_pad) * (D / 2) + static_cast<size_t>(rows_pad) * (D / 16) + part +
-         static_cast<size_t>(t_dec) * N * 8 + 8 * 256;
+         static_cast<size_t>(t_dec) * N * 8 + 9 * 256;
 }
 
 size_t router_gate_x_gsa_offset(void) { return router_ws_layout(1, 64, 1).scalars; }

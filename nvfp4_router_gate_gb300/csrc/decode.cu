@@ -52,6 +52,11 @@ struct DecodeParams {
   float* ws_keys;
   float* ws_scores;
   uint32_t* ticket;
+  // null: the last CTA (ticket) collects the keys; else (N <= 256) the
+  // collector words of every (token, expert) pair, zero between calls
+  uint64_t* ws_words;
+  uint32_t* status;            // timeout of the collector's poll, or null
+  int test_stall;              // test hook: CTAs other than the collector store no words
   // CTAs per thread-block cluster (1: every CTA stages, reduces and
   // quantizes all of x itself; C > 1: the C CTAs of a cluster split these
   // and exchange the results through distributed shared memory)
@@ -80,6 +85,27 @@ __device__ __forceinline__ uint64_t dec_pack_key(float key, int id) {
 }
 
 constexpr int kCandCap = 64;
+
+// A collector word: the key's order-preserving bits (never 0: a word of 0
+// means "not written yet") above the score's bits.
+__device__ __forceinline__ uint64_t dec_word(float key, float score) {
+  const uint32_t b = __float_as_uint(key);
+  uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  ord = ord > 1u ? ord : 1u;                       // only a NaN pattern maps to 0
+  return (static_cast<uint64_t>(ord) << 32) | __float_as_uint(score);
+}
+__device__ __forceinline__ float dec_word_key(uint64_t w) {
+  const uint32_t ord = static_cast<uint32_t>(w >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // Top-k (k <= 16) of one token's N <= 256 keys with one warp, in order (key
 // descending, lower id first): lane l holds keys l, l+32, ...  The k-th
@@ -153,6 +179,7 @@ __device__ __forceinline__ void warp_topk_256(const float* kt, int N, int k, int
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kMaxBlocksPerThread = 8;    // W blocks a thread prefetches into registers
+constexpr size_t kCollectBytes = 4096;    // shared memory of the one-token collector
 constexpr int kMaxT = 16;                 // tokens of one decode call
 
 // Shared memory of one CTA: the raw activations (reused for the last CTA's
@@ -170,7 +197,11 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(int T, int D, int N, in
   const size_t slice = (static_cast<size_t>(T) * KB + C - 1) / C;
   const size_t raw_bytes = slice * kBlock * elt;
   const size_t kv_bytes = static_cast<size_t>(T) * N * 8;
-  L.xv = align_up(raw_bytes > kv_bytes ? raw_bytes : kv_bytes, 16);
+  // (at least the one-token collector's 4 KB: 256 order words, 256 scores
+  // and 128 candidates, clear of the regions still read before it starts)
+  size_t xr = raw_bytes > kv_bytes ? raw_bytes : kv_bytes;
+  xr = xr > kCollectBytes ? xr : kCollectBytes;
+  L.xv = align_up(xr, 16);
   L.xs = align_up(L.xv + static_cast<size_t>(T) * D, 16);
   L.red = align_up(L.xs + static_cast<size_t>(T) * KB * 4, 16);
   // cross-warp partial sums, later the last CTA's candidate lists (8 B each)
@@ -214,6 +245,7 @@ decode_router_kernel(const DecodeParams p) {
   __shared__ uint32_t s_cmax[kMaxDecodeCluster];
   __shared__ int s_last;
   __shared__ int s_sel[kMaxT * 16];
+  __shared__ float s_rcp[128];                                   // RN(1 / dec(b)) of scale byte b
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gs = kDecodeThreads / p.epc;                       // threads per expert
@@ -260,6 +292,16 @@ decode_router_kernel(const DecodeParams p) {
       wsb[i] = 0;
     }
   }
+  // The threads that finish an expert's logit (step 4) load the gate's global
+  // scale and the expert's bias now, off the path to the keys.
+  const int g_out = tid / kMaxT, t_out = tid - g_out * kMaxT;
+  const int e_out = blockIdx.x * p.epc + g_out;
+  const bool out_thread = tid < p.epc * kMaxT && t_out < T && e_out < N;
+  float w_gsa = 0.0f, bias_e = 0.0f;
+  if (out_thread) {
+    w_gsa = __ldg(p.w_gsa);
+    if (p.bias) bias_e = __ldg(p.bias + e_out);
+  }
   // The blocks of x (block b = t * KB + c: 16 elements of token t) this CTA
   // stages, reduces and quantizes: all of them, or in a cluster of C CTAs
   // the slice [b_lo, b_hi) of its rank.
@@ -282,7 +324,11 @@ decode_router_kernel(const DecodeParams p) {
   for (int v = b_lo * kVecPerBlock + tid; v < b_hi * kVecPerBlock; v += kDecodeThreads)
     cp_async16(xraw + 16 * static_cast<size_t>(v - b_lo * kVecPerBlock),
                static_cast<const uint8_t*>(p.x) + 16 * static_cast<size_t>(v));
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  // the quantizer's reciprocal table (the bits __frcp_rn gives), while the
+  // copies are in flight; byte 127 (NaN) never occurs
+  if (tid < 128) s_rcp[tid] = (tid >= 1 && tid <= 126) ? __frcp_rn(e4m3_value(tid)) : 0.0f;
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   // 1. max |x| over the staged blocks; in a cluster, every CTA's maximum goes
   //    to every CTA (thread i writes CTA i's slot), so each one finds the
@@ -314,7 +360,7 @@ decode_router_kernel(const DecodeParams p) {
     Block16 blk;
     load_block16_shared<kBF16>(xraw, static_cast<size_t>(b - b_lo) * kBlock, blk);   // xraw holds [b_lo, b_hi)
     uint32_t lo, hi;
-    const uint32_t byte = quant_block16_bracket(blk, qs, lo, hi);
+    const uint32_t byte = quant_block16_bracket(blk, qs, lo, hi, s_rcp);
     uint4 q;
     q.x = e2m1x4_to_s8x4(lo & 0xFFFFu);
     q.y = e2m1x4_to_s8x4(lo >> 16);
@@ -406,52 +452,144 @@ decode_router_kernel(const DecodeParams p) {
   __syncthreads();
 
   // 4. per (expert, token): logit, score, key
-  if (tid < p.epc * kMaxT) {
-    const int g = tid / kMaxT, t = tid - g * kMaxT;
-    const int e2 = blockIdx.x * p.epc + g;
-    if (t < T && e2 < N) {
-      const int wpg = kDecodeWarps / p.epc;
-      float sacc = 0.0f;
-      for (int w = 0; w < wpg; ++w) sacc = __fadd_rn(sacc, red[(g * wpg + w) * kMaxT + t]);
-      const float gscale = __fmul_rn(qs.gsa, __ldg(p.w_gsa));
-      const float l = __fmul_rn(__fmul_rn(sacc, 0.25f), gscale);   // the sums count 2a * 2b
-      const size_t o = static_cast<size_t>(t) * N + e2;
-      if (p.logits) {
-        p.logits[o] = l;
-      } else if (p.raw) {
-        p.ws_keys[o] = l;
-        p.ws_scores[o] = l;
+  if (out_thread) {
+    const int g = g_out, t = t_out, e2 = e_out;
+    const int wpg = kDecodeWarps / p.epc;
+    float sacc = 0.0f;
+    for (int w = 0; w < wpg; ++w) sacc = __fadd_rn(sacc, red[(g * wpg + w) * kMaxT + t]);
+    const float gscale = __fmul_rn(qs.gsa, w_gsa);
+    const float l = __fmul_rn(__fmul_rn(sacc, 0.25f), gscale);     // the sums count 2a * 2b
+    const size_t o = static_cast<size_t>(t) * N + e2;
+    if (p.logits) {
+      p.logits[o] = l;
+    } else {
+      const float sc = p.raw ? l : sigmoid_f32(l);
+      const float key = p.bias ? __fadd_rn(sc, bias_e) : sc;
+      if (p.ws_words) {
+        if (!p.test_stall || blockIdx.x == 0) st_relaxed_u64(p.ws_words + o, dec_word(key, sc));
       } else {
-        const float sc = sigmoid_f32(l);
-        p.ws_keys[o] = p.bias ? __fadd_rn(sc, __ldg(p.bias + e2)) : sc;
+        p.ws_keys[o] = key;
         p.ws_scores[o] = sc;
       }
     }
   }
   if (p.logits) return;
 
-  // 5. the last CTA to finish selects, renormalises and writes
-  // The CTA barrier orders every thread's key stores before thread 0's
-  // ticket, an acquire-release atomic at gpu scope: it publishes them
-  // (release, cumulative over the barrier) and, in the last CTA, makes every
-  // other CTA's published keys visible to the threads that read them after
-  // the next barrier (acquire) -- one round trip instead of a fence and an
-  // atomic.
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ticket) : "memory");
-    s_last = old == gridDim.x - 1 ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
+  // 5. one CTA selects, renormalises and writes
   float* kbuf = reinterpret_cast<float*>(xraw);                 // x is no longer needed
   float* sbuf = kbuf + static_cast<size_t>(T) * N;
-  for (int i = tid; i < T * N; i += kDecodeThreads) {
-    kbuf[i] = __ldcg(p.ws_keys + i);
-    sbuf[i] = __ldcg(p.ws_scores + i);
+  if (p.ws_words) {
+    // Up to 256 experts: CTA 0 collects.  Every other CTA has stored its
+    // words and exits without waiting; CTA 0 polls the T x N words (each
+    // thread up to eight, all its loads in flight at once) until none is
+    // zero -- the data is its own flag, so the last word is seen about one
+    // round trip after it lands, with no ticket and no second read -- and
+    // puts each back to zero for the next call (nothing else writes it in
+    // this call).  The poll is bounded (1 s; a timeout goes to the status
+    // word and leaves the outputs unspecified).
+    if (blockIdx.x != 0) return;
+    constexpr int kPoll = kDecodeWords / kDecodeThreads;
+    const int nw = T * N;
+    uint64_t wv[kPoll];
+#pragma unroll
+    for (int u = 0; u < kPoll; ++u) {
+      const int i = tid + u * kDecodeThreads;
+      wv[u] = i < nw ? ld_relaxed_u64(p.ws_words + i) : 1ull;
+    }
+    const uint64_t deadline = globaltimer_ns() + 1000000000ull;
+    for (;;) {
+      bool all = true;
+#pragma unroll
+      for (int u = 0; u < kPoll; ++u) all = all && wv[u] != 0;
+      if (all) break;
+      if (globaltimer_ns() > deadline) {
+        report_timeout(p.status);
+        break;
+      }
+#pragma unroll
+      for (int u = 0; u < kPoll; ++u)
+        if (wv[u] == 0) wv[u] = ld_relaxed_u64(p.ws_words + tid + u * kDecodeThreads);
+    }
+#pragma unroll
+    for (int u = 0; u < kPoll; ++u) {
+      const int i = tid + u * kDecodeThreads;
+      if (i < nw) st_relaxed_u64(p.ws_words + i, 0ull);
+    }
+    if (T == 1) {
+      // One token: eight warps rank 32 keys each among themselves (the k best
+      // of every warp are candidates: the k best overall are among them), then
+      // each of the 8k candidates is ranked among the candidates; ranks follow
+      // (key descending, lower id first).
+      uint64_t* s_pk = reinterpret_cast<uint64_t*>(xraw);                 // [256] order words
+      float* s_sc = reinterpret_cast<float*>(xraw + 256 * 8);              // [256] scores
+      uint64_t* s_cand = reinterpret_cast<uint64_t*>(xraw + 256 * 12);     // [8 k]
+      const int k = p.k;
+      if (warp < 8) {
+        const uint64_t r = tid < N ? ((wv[0] >> 32) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(tid)) : 0ull;
+        if (tid < N) s_sc[tid] = __uint_as_float(static_cast<uint32_t>(wv[0]));
+        s_pk[tid] = r;
+        if (lane < k) s_cand[warp * k + lane] = 0ull;
+        __syncwarp();
+        int rk = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) rk += s_pk[warp * 32 + q] > r ? 1 : 0;
+        if (r != 0 && rk < k) s_cand[warp * k + rk] = r;
+      }
+      __syncthreads();
+      const int nc = 8 * k;
+      if (tid < nc) {
+        const uint64_t c = s_cand[tid];
+        if (c != 0) {
+          int rk = 0;
+#pragma unroll 8
+          for (int q = 0; q < nc; ++q) rk += s_cand[q] > c ? 1 : 0;
+          if (rk < k) s_sel[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(c));
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int id = lane < k ? s_sel[lane] : 0;
+        const float sc = lane < k ? s_sc[id & 255] : 0.0f;
+        float sum = sc;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+        if (lane < k) {
+          p.out_ids[lane] = id;
+          p.out_w[lane] = p.raw ? sc : (sum > 0.0f ? __fdiv_rn(__fmul_rn(p.routed_scaling, sc), sum) : 0.0f);
+        }
+      }
+      return;
+    }
+#pragma unroll
+    for (int u = 0; u < kPoll; ++u) {
+      const int i = tid + u * kDecodeThreads;
+      if (i < nw) {
+        kbuf[i] = dec_word_key(wv[u]);
+        sbuf[i] = __uint_as_float(static_cast<uint32_t>(wv[u]));
+      }
+    }
+    __syncthreads();
+  } else {
+    // The last CTA to finish collects.  The CTA barrier orders every
+    // thread's key stores before thread 0's ticket, an acquire-release atomic
+    // at gpu scope: it publishes them (release, cumulative over the barrier)
+    // and, in the last CTA, makes every other CTA's published keys visible to
+    // the threads that read them after the next barrier (acquire) -- one
+    // round trip instead of a fence and an atomic.
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t old;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.ticket) : "memory");
+      s_last = old == gridDim.x - 1 ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    for (int i = tid; i < T * N; i += kDecodeThreads) {
+      kbuf[i] = __ldcg(p.ws_keys + i);
+      sbuf[i] = __ldcg(p.ws_scores + i);
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (N <= 256) {
     // one warp per token: candidate selection, then the renormalised weights
     uint64_t* cand = reinterpret_cast<uint64_t*>(red) + warp * kCandCap;   // red is no longer needed
@@ -469,7 +607,7 @@ decode_router_kernel(const DecodeParams p) {
             p.raw ? sc : (sum > 0.0f ? __fdiv_rn(__fmul_rn(p.routed_scaling, sc), sum) : 0.0f);
       }
     }
-    if (tid == 0) *p.ticket = 0u;
+    if (tid == 0 && !p.ws_words) *p.ticket = 0u;
     return;
   }
   if (T * N <= kDecodeThreads) {
@@ -618,7 +756,8 @@ cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const 
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,
                           int k, float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                           float* logits, float* ws_keys, float* ws_scores, uint32_t* ticket,
-                          const DecodePlan& plan, cudaStream_t s) {
+                          uint64_t* ws_words, uint32_t* status, bool test_stall, const DecodePlan& plan,
+                          cudaStream_t s) {
   DecodeParams p;
   p.cluster = plan.cluster;
   p.x = x; p.T = static_cast<int>(T); p.D = static_cast<int>(D);
@@ -627,6 +766,9 @@ cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const 
   p.raw = raw ? 1 : 0; p.epc = plan.epc;
   p.out_ids = out_ids; p.out_w = out_w; p.logits = logits;
   p.ws_keys = ws_keys; p.ws_scores = ws_scores; p.ticket = ticket;
+  p.ws_words = N <= 256 && T <= kMaxT ? ws_words : nullptr;
+  p.status = status;
+  p.test_stall = test_stall && p.ws_words ? 1 : 0;
   return bf16 ? launch_t<true>(p, plan, s) : launch_t<false>(p, plan, s);
 }
 

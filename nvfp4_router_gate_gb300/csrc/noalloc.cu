@@ -94,8 +94,9 @@ extern "C" nvr_status router_gate_topk_noalloc(const void* x, nvr_dtype dt, int6
   // predecessor's tail inside a graph).
   float* keys = reinterpret_cast<float*>(scratch + kNoAllocControl);
   float* scores = keys + T * N;
+  // the last CTA's ticket, never a wait: a call here has no status word
   e = launch_decode(x, dt == NVR_BF16, T, D, W_fp4, W_scales, w_gsa, N, bias, k, routed_scaling,
                     (flags & NVR_FLAG_RAW_LOGITS) != 0, out_ids, out_w, nullptr, keys, scores,
-                    reinterpret_cast<uint32_t*>(scratch + kWsDecodeTicket), dp, s);
+                    reinterpret_cast<uint32_t*>(scratch + kWsDecodeTicket), nullptr, nullptr, false, dp, s);
   return cuda_status(e);
 }

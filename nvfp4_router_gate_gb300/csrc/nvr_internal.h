@@ -20,6 +20,7 @@ constexpr int kMaxKmax = 16;             // largest top-k list
 constexpr int kMaxDevices = 64;
 constexpr int kMaxTicketTiles = 65536;   // token tiles of the N-split router (T <= 8,388,608)
 constexpr int kMaxFlatTiles = 1024;      // token tiles of a fused router launched without clusters
+constexpr int kDecodeWords = 16 * 256;   // decode collector words: up to 16 tokens x 256 experts
 
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
 // link-time dependency on libcuda).
@@ -63,6 +64,7 @@ struct WsLayout {
   size_t scalars = 0;        // x gsa (router path), quantizer record {gsa, 1/gsa, mode, amax} -- 256 bytes
   size_t tickets = 0;        // kMaxTicketTiles x u32: the N-split router's per-tile tickets
   size_t tile_sync = 0;      // 2 x kMaxFlatTiles u32: the fused router's tile-barrier counters (no clusters)
+  size_t dec_words = 0;      // kDecodeWords u64: the decode collector's (key, score) words, zero between calls
   size_t x_codes = 0;        // [rows_pad, D/2]
   size_t x_sf = 0;           // tile layout, rows_pad rows
   size_t partials = 0;       // N-split top-k lists, or the K-split fp32 partial logits
@@ -142,10 +144,16 @@ nvr_status launch_router_epilogue(const float* partials, int S, const float* x_g
                                   int64_t T, int64_t N, const float* bias, int k, float routed_scaling,
                                   bool raw, int32_t* out_ids, float* out_w, float* logits, cudaStream_t s);
 
+// ws_words: null, or (for N <= 256) kDecodeWords zeroed words at a fixed
+// workspace offset -- then CTA 0 collects the other CTAs' keys by polling
+// them (bounded; a timeout goes to *status) instead of the last CTA's ticket.
+// test_stall (with ws_words): the other CTAs store no words, so the poll
+// runs out.
 cudaError_t launch_decode(const void* x, bool bf16, int64_t T, int64_t D, const uint8_t* W_codes,
                           const uint8_t* W_sf, const float* w_gsa, int64_t N, const float* bias,
                           int k, float routed_scaling, bool raw, int32_t* out_ids, float* out_w,
                           float* logits, float* ws_keys, float* ws_scores, uint32_t* ticket,
-                          const DecodePlan& plan, cudaStream_t s);
+                          uint64_t* ws_words, uint32_t* status, bool test_stall, const DecodePlan& plan,
+                          cudaStream_t s);
 
 }  // namespace nvr

@@ -184,6 +184,24 @@ def test_workspace_counters_do_not_move_with_T():
             prev = v
 
 
+def test_workspace_size_covers_every_call_size():
+    """A workspace of router_gate_workspace_size(T_max, ...) bytes passes the
+    router's own size check for every T <= T_max (the check runs before any
+    device call; without a GPU the call then stops at the device query)."""
+    nat = _lib()
+    L = nat.lib()
+    fake = ctypes.c_void_p(0x10000)          # aligned, never dereferenced
+    for N in (16, 256, 300, 384, 129280):
+        for T_max in (1, 16, 17, 600, 4096):
+            ws = L.router_gate_workspace_size(T_max, 7168, N, 8)
+            for T in sorted({1, 2, 15, 16, 17, 128, 129, 300, T_max}):
+                if T > T_max:
+                    continue
+                st = L.router_gate_topk(fake, nat.NVR_BF16, T, 7168, fake, fake, fake, N, None, 8, 1.0, 0,
+                                        fake, fake, fake, ws, None)
+                assert st != nat.NVR_ERR_WORKSPACE, (N, T_max, T)
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     from nvfp4_router_gate_gb300 import _native
     monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "missing.so"))

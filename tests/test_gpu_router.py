@@ -533,6 +533,67 @@ def test_decode_shared_quantization_back_to_back_on_one_workspace():
         assert compare.topk_ok(res), (scale, res)
 
 
+# Decode calls of up to 256 experts: CTA 0 collects every (token, expert)
+# key by polling words that each call leaves at zero (a fixed region of the
+# workspace, clear of the regions whose place depends on T).  Calls of every
+# decode shape, raw and biased, with a prefill call between them, on one
+# workspace: a word left behind by one call would route the next wrongly.
+
+def _oracle_check(case, x_bits, ids, wts, k, raw):
+    x32 = WL.bf16_bits_to_float32(x_bits)
+    gsa = Q.global_scale(x32)
+    xq, xs, _ = Q.quantize(x32, gsa=gsa)
+    L, B = gemm.logits(xq, xs, gsa, case.wq, case.ws, case.wg)
+    keys = router.selection_keys(L, case.bias, raw)
+    return compare.check_topk(ids, wts, L, B, keys, case.bias, case.w.routed_scaling, raw)
+
+
+def test_decode_collector_words_across_calls_and_shapes():
+    import nvfp4_router_gate_gb300 as R
+    w = WL.WORKLOADS["decode"].with_T(16)
+    case = Case(w)
+    pre = WL.WORKLOADS["prefill"].with_T(600)
+    x_pre = to_device(WL.make_x(pre), "bf16")
+    ws = R.new_workspace(R.router_gate_workspace_size(600, w.D, w.N, 16))
+    plan = [(1, 1.0, 8, False), (16, 2.0 ** 6, 8, False), (1, 3.0, 8, True), ("prefill", 0, 8, False),
+            (1, 2.0 ** -9, 16, False), (8, 1.0, 1, False), (5, 0.5, 8, True), (1, 1.0, 8, False)]
+    for T, scale, k, raw in plan:
+        if T == "prefill":
+            R.router_gate_topk(x_pre, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5, workspace=ws)
+            continue
+        bits = WL.float32_to_bf16_bits((case.x32[:T] * np.float32(scale)).astype(np.float32))
+        ids, wts = R.router_gate_topk(to_device(bits, "bf16"), case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev,
+                                      k, w.routed_scaling, raw, workspace=ws, flags=DEC)
+        torch.cuda.synchronize()
+        assert R.last_router_plan()["sequence"] == "decode"
+        res = _oracle_check(case, bits, ids.cpu().numpy(), wts.cpu().numpy(), k, raw)
+        assert compare.topk_ok(res), (T, scale, k, raw, res)
+    assert R.nvr_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_collector_timeout_reports_status(T):
+    """Failure detection without a GPU fault: with the stall hook the decode
+    CTAs other than the collector store no keys, the collector's poll runs
+    out after about a second, records NVR_ERR_TIMEOUT and returns; after
+    re-zeroing the workspace the next call routes correctly."""
+    import nvfp4_router_gate_gb300 as R
+    from nvfp4_router_gate_gb300 import _native
+    case = Case(WL.WORKLOADS["decode"].with_T(T))
+    ws = R.new_workspace(R.router_gate_workspace_size(T, 7168, 256, 8))
+    R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5,
+                       workspace=ws, flags=DEC | _native.NVR_FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert R.nvr_read_device_status(ws) == _native.NVR_ERR_TIMEOUT
+    ws.zero_()
+    ids, w = R.router_gate_topk(case.x_dev, case.W_fp4, case.W_sf, case.w_gsa, case.bias_dev, 8, 2.5,
+                                workspace=ws, flags=DEC)
+    torch.cuda.synchronize()
+    assert R.nvr_read_device_status(ws) == 0
+    res = case.check(ids.cpu().numpy(), w.cpu().numpy(), np.arange(T))
+    assert compare.topk_ok(res), res
+
+
 # ------------------------------------------------ quantization inside the GEMM
 # bf16 activations on heads of up to 256 experts are quantized inside the GEMM
 # kernel; the codes never reach memory.  A one-hot gate weight makes every
