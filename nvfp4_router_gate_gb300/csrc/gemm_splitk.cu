@@ -285,6 +285,7 @@ struct EpiParams {
 __global__ void __launch_bounds__(kEpiWarpsPerCta * 32)
 router_epilogue_kernel(const __grid_constant__ EpiParams p) {
   __shared__ float4 s_row[kEpiWarpsPerCta][kRouteSlot];   // each warp's token slot
+  __shared__ __align__(16) uint8_t s_scr[kEpiWarpsPerCta][kRouteScratch];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kEpiWarpsPerCta + warp;
   TokenRouter rt;
@@ -294,8 +295,8 @@ router_epilogue_kernel(const __grid_constant__ EpiParams p) {
   if (t >= p.T) return;                              // whole warp
   const float gscale = __fmul_rn(__ldg(p.x_gsa), __ldg(p.w_gsa));
   const int64_t tt[1] = {t};
-  rt.route<1>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row[warp], lane, p.out_ids, p.out_w,
-              p.logits);
+  rt.route<1, true>(p.partials, static_cast<size_t>(p.T) * 256, p.S, tt, gscale, s_row[warp], lane, p.out_ids,
+                    p.out_w, p.logits, nullptr, s_scr[warp]);
 }
 
 }  // namespace

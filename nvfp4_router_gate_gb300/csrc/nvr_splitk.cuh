@@ -141,15 +141,23 @@ inline bool encode_partials(CUtensorMap* map, float* ptr, int64_t T, int S) {
 // of every group g (coalesced 512-byte rows).  The partials are added in
 // rank order (the result does not depend on timing), scaled by
 // gsa_x * gsa_w; keys are sigmoid(logit) + bias (RAW: the logit).
-// Selection: each lane sorts its keys of groups 0-1 (8 (key, id) pairs packed
-// into order-preserving 64-bit words) and, with NG = 3, those of group 2 in a
-// second list of 4; k rounds then take the best head of the warp (two 32-bit
-// max reductions: the key's bits, then the complemented id among the lanes
-// holding that key) and the winning lane pops its head.  Exact for any keys,
-// ties included (equal keys: lower id first), with no data-dependent trip
-// counts.  The selected experts' logits come back from the warp's copy of the
-// row in shared memory; the weights are routed_scaling * score / (sum of the
-// k scores).
+// Selection, on (key, id) pairs packed into order-preserving 64-bit words:
+// - sorted lists: each lane sorts its words of groups 0-1 (8) and, with
+//   NG = 3, those of group 2 in a second list of 4; k rounds take the best
+//   head of the warp (two 32-bit max reductions: the key's bits, then the
+//   complemented id among the lanes holding that key) and the winning lane
+//   pops it;
+// - rank selection (NG = 2): the k-th largest of the 32 lanes' maxima of the
+//   key bits (ranked by counting, one reduction) bounds the k-th best key
+//   from below, the words at or above it (typically k to 2k) are gathered
+//   into one list by ballots, and each candidate's rank among them -- a
+//   count of better candidates -- is its rank overall; with more than 32
+//   candidates (many equal keys) the bound is taken again on whole words,
+//   else the sorted lists select.
+// Both exact for any keys, ties included (equal keys: lower id first).  The
+// selected experts' logits come back from the warp's copy of the row in
+// shared memory; the weights are routed_scaling * score / (sum of the k
+// scores).
 
 // (key descending, id ascending) as one unsigned 64-bit order: the float's
 // order-preserving bit pattern above the complemented id.  Never 0 for a
@@ -191,9 +199,91 @@ struct RouteSlot {
   static constexpr int kFloat4 = 32 * NG;
 };
 constexpr int kRouteSlot = RouteSlot<2>::kFloat4;
+// Shared memory of one token slot's selection: 32 lane maxima, up to 32
+// candidate words and the k <= 16 selected ids.
+constexpr int kRouteScratch = 32 * 4 + 32 * 8 + 16 * 4;
 
 __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+// Rank selection of the k best of a warp's words (at most 32 candidates at
+// or above `bound`, gathered into s_c by ballots) -- the candidates' ranks
+// among themselves are their ranks overall; returns false (s_sel untouched)
+// when more than 32 words reach the bound.
+template <int kE>
+__device__ __forceinline__ bool select_by_rank(const uint64_t (&pw)[kE], uint64_t bound, int k, int lane,
+                                               uint64_t* s_c, int* s_sel) {
+  const uint32_t lt = (1u << lane) - 1u;
+  int base = 0;
+#pragma unroll
+  for (int j = 0; j < kE; ++j) {
+    const bool c = pw[j] != 0 && pw[j] >= bound;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, c);
+    const int pos = base + __popc(bal & lt);
+    if (c && pos < 32) s_c[pos] = pw[j];
+    base += __popc(bal);
+  }
+  if (base > 32) return false;
+  __syncwarp();
+  if (lane < base) {
+    const uint64_t me = s_c[lane];
+    int rk = 0;
+#pragma unroll 4
+    for (int q = 0; q < base; ++q) rk += s_c[q] > me ? 1 : 0;
+    if (rk < k) s_sel[rk] = static_cast<int>(~static_cast<uint32_t>(me));
+  }
+  return true;
+}
+
+// The k best of a warp's words when many share their key bits: the k-th
+// largest lane maximum of the whole words bounds them (exact ties then leave
+// the lowest ids, about 4k words); past 32 candidates each lane sorts its
+// words and k rounds take the best head of the warp (two 32-bit max
+// reductions: the key's bits, then the complemented id among the lanes
+// holding that key), the winning lane popping it.
+template <int kE>
+__device__ __forceinline__ void select_ties(uint64_t (&pw)[kE], int k, int lane, uint64_t* s_c, int* s_sel) {
+  uint64_t m = 0;
+#pragma unroll
+  for (int j = 0; j < kE; ++j) m = pw[j] > m ? pw[j] : m;
+  __syncwarp();
+  s_c[lane] = m;
+  __syncwarp();
+  int rk = 0;
+#pragma unroll 8
+  for (int q = 0; q < 32; ++q) rk += s_c[q] > m ? 1 : 0;
+  __syncwarp();
+  const uint64_t v = rk < k ? m : ~0ull;
+  const uint32_t hmin = __reduce_min_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32));
+  const uint32_t lmin = __reduce_min_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32) == hmin
+                                                           ? static_cast<uint32_t>(v) : 0xFFFFFFFFu);
+  if (select_by_rank(pw, (static_cast<uint64_t>(hmin) << 32) | lmin, k, lane, s_c, s_sel)) return;
+  constexpr int kB = kE > 8 ? kE - 8 : 1;
+  uint64_t pa[8], pb[kB];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) pa[j] = pw[j];
+#pragma unroll
+  for (int j = 0; j < kB; ++j) pb[j] = kE > 8 ? pw[8 + j] : 0;
+  sort8_desc(pa);
+  if constexpr (kB == 4) sort4_desc(pb);
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    const bool from_b = kE > 8 && pb[0] > pa[0];
+    const uint64_t h = from_b ? pb[0] : pa[0];
+    const uint32_t hi = static_cast<uint32_t>(h >> 32), lo = static_cast<uint32_t>(h);
+    const uint32_t hmax = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t lmax = __reduce_max_sync(0xFFFFFFFFu, hi == hmax ? lo : 0u);
+    const bool win = hi == hmax && lo == lmax;                 // ids are unique
+    const bool wa = win && !from_b, wb = win && from_b;
+#pragma unroll
+    for (int j = 0; j < 7; ++j) pa[j] = wa ? pa[j + 1] : pa[j];
+    pa[7] = wa ? 0 : pa[7];
+#pragma unroll
+    for (int j = 0; j + 1 < kB; ++j) pb[j] = wb ? pb[j + 1] : pb[j];
+    pb[kB - 1] = wb ? 0 : pb[kB - 1];
+    if (lane == 0) s_sel[r] = static_cast<int>(~lmax);
+  }
 }
 
 template <int NG>
@@ -222,15 +312,20 @@ struct TokenRouterT {
 
   // Routes NT tokens at once (independent dependency chains interleave);
   // t[i] < 0 marks an unused slot.  s_row: NT token slots of
-  // RouteSlot<NG>::kFloat4 float4 for the warp.  stage: null, or shared
+  // RouteSlot<NG>::kFloat4 float4 for the warp.  kRank (up to 256 experts):
+  // the rank selection, with scratch = NT x kRouteScratch bytes (16-byte
+  // aligned) of the warp's selection lists; else the sorted lists and k
+  // rounds of a warp arg-max.  (Measured: the rank selection shortens the
+  // separate epilogue kernel, one token per warp, by ~0.9 us at T = 4096;
+  // inside the fused kernel its code and registers cost as much as it saves.)  stage: null, or shared
   // memory for the warp's partial rows (row n * S + s: 32 NG float4 of token
   // slot n, plane s; only the rows of valid slots are touched) -- then every
   // partial row is copied in at once (asynchronous copies, one round trip to
   // L2 whatever S) before the sums.
-  template <int NT>
+  template <int NT, bool kRank = false>
   __device__ __forceinline__ void route(const float* partials, size_t plane, int S, const int64_t (&t)[NT],
                                         float gscale, float4* s_row, int lane, int32_t* out_ids, float* out_w,
-                                        float* logits, float4* stage = nullptr) const {
+                                        float* logits, float4* stage = nullptr, uint8_t* scratch = nullptr) const {
     constexpr int kSlot = RouteSlot<NG>::kFloat4;
     float4 a[NT][NG];
     if (stage) {
@@ -297,61 +392,124 @@ struct TokenRouterT {
           if (t[n] >= 0 && col_of(j, lane) < N) logits[t[n] * N + col_of(j, lane)] = l[n][j];
       return;
     }
-    // lists: groups 0-1 (8 words), and group 2 (4 words) when NG = 3
-    constexpr int kB = NG == 3 ? 4 : 1;
-    uint64_t pa[NT][8], pb[NT][kB];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-#pragma unroll
-      for (int g = 0; g < NG; ++g)
-        s_row[kSlot * n + 32 * g + lane] = make_float4(l[n][4 * g], l[n][4 * g + 1], l[n][4 * g + 2], l[n][4 * g + 3]);
-#pragma unroll
-      for (int j = 0; j < kE; ++j) {
-        const float key = raw ? l[n][j] : __fadd_rn(sigmoid_f32(l[n][j]), b[j]);
-        const uint64_t w = col_of(j, lane) < N ? pack_key(key, col_of(j, lane)) : 0;
-        if (j < 8) pa[n][j] = w;
-        else pb[n][(j - 8) & (kB - 1)] = w;
-      }
-      sort8_desc(pa[n]);
-      if constexpr (NG == 3) sort4_desc(pb[n]);
-      else pb[n][0] = 0;
-    }
     int sel_id[NT];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) sel_id[n] = 0;
-    // Each reduction takes ~90 cycles and issue is in order: the NT tokens'
-    // reductions of a round are issued back to back so their latencies overlap.
-#pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-      uint32_t hi[NT], lo[NT], hmax[NT], lmax[NT];
-      bool from_b[NT];
+    if constexpr (!kRank || NG == 3) {
+      // the lanes' sorted lists and k rounds of a warp arg-max
+      // lists: groups 0-1 (8 words), and group 2 (4 words) when NG = 3
+      constexpr int kB = NG == 3 ? 4 : 1;
+      uint64_t pa[NT][8], pb[NT][kB];
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        from_b[n] = NG == 3 && pb[n][0] > pa[n][0];
-        const uint64_t h = from_b[n] ? pb[n][0] : pa[n][0];
-        hi[n] = static_cast<uint32_t>(h >> 32);
-        lo[n] = static_cast<uint32_t>(h);
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+          s_row[kSlot * n + 32 * g + lane] = make_float4(l[n][4 * g], l[n][4 * g + 1], l[n][4 * g + 2], l[n][4 * g + 3]);
+#pragma unroll
+        for (int j = 0; j < kE; ++j) {
+          const float key = raw ? l[n][j] : __fadd_rn(sigmoid_f32(l[n][j]), b[j]);
+          const uint64_t w = col_of(j, lane) < N ? pack_key(key, col_of(j, lane)) : 0;
+          if (j < 8) pa[n][j] = w;
+          else pb[n][(j - 8) & (kB - 1)] = w;
+        }
+        sort8_desc(pa[n]);
+        if constexpr (NG == 3) sort4_desc(pb[n]);
+        else pb[n][0] = 0;
       }
 #pragma unroll
-      for (int n = 0; n < NT; ++n) hmax[n] = __reduce_max_sync(0xFFFFFFFFu, hi[n]);
+      for (int n = 0; n < NT; ++n) sel_id[n] = 0;
+      // Each reduction takes ~90 cycles and issue is in order: the NT tokens'
+      // reductions of a round are issued back to back so their latencies overlap.
+#pragma unroll 1
+      for (int r = 0; r < k; ++r) {
+        uint32_t hi[NT], lo[NT], hmax[NT], lmax[NT];
+        bool from_b[NT];
 #pragma unroll
-      for (int n = 0; n < NT; ++n) lmax[n] = __reduce_max_sync(0xFFFFFFFFu, hi[n] == hmax[n] ? lo[n] : 0u);
+        for (int n = 0; n < NT; ++n) {
+          from_b[n] = NG == 3 && pb[n][0] > pa[n][0];
+          const uint64_t h = from_b[n] ? pb[n][0] : pa[n][0];
+          hi[n] = static_cast<uint32_t>(h >> 32);
+          lo[n] = static_cast<uint32_t>(h);
+        }
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        if (lane == r) sel_id[n] = static_cast<int>(~lmax[n]);   // the winning expert
-        const bool win = hi[n] == hmax[n] && lo[n] == lmax[n];     // its lane (ids are unique)
-        const bool wa = win && !from_b[n], wb = win && from_b[n];
+        for (int n = 0; n < NT; ++n) hmax[n] = __reduce_max_sync(0xFFFFFFFFu, hi[n]);
 #pragma unroll
-        for (int j = 0; j < 7; ++j) pa[n][j] = wa ? pa[n][j + 1] : pa[n][j];
-        pa[n][7] = wa ? 0 : pa[n][7];
-        if constexpr (NG == 3) {
+        for (int n = 0; n < NT; ++n) lmax[n] = __reduce_max_sync(0xFFFFFFFFu, hi[n] == hmax[n] ? lo[n] : 0u);
 #pragma unroll
-          for (int j = 0; j < 3; ++j) pb[n][j] = wb ? pb[n][j + 1] : pb[n][j];
-          pb[n][3] = wb ? 0 : pb[n][3];
+        for (int n = 0; n < NT; ++n) {
+          if (lane == r) sel_id[n] = static_cast<int>(~lmax[n]);   // the winning expert
+          const bool win = hi[n] == hmax[n] && lo[n] == lmax[n];     // its lane (ids are unique)
+          const bool wa = win && !from_b[n], wb = win && from_b[n];
+#pragma unroll
+          for (int j = 0; j < 7; ++j) pa[n][j] = wa ? pa[n][j + 1] : pa[n][j];
+          pa[n][7] = wa ? 0 : pa[n][7];
+          if constexpr (NG == 3) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) pb[n][j] = wb ? pb[n][j + 1] : pb[n][j];
+            pb[n][3] = wb ? 0 : pb[n][3];
+          }
         }
       }
+      __syncwarp();
+    } else {
+      // (key, id) words of this lane's experts (0: no expert)
+      uint64_t pw[NT][kE];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+          s_row[kSlot * n + 32 * g + lane] = make_float4(l[n][4 * g], l[n][4 * g + 1], l[n][4 * g + 2], l[n][4 * g + 3]);
+#pragma unroll
+        for (int j = 0; j < kE; ++j) {
+          const float key = raw ? l[n][j] : __fadd_rn(sigmoid_f32(l[n][j]), b[j]);
+          pw[n][j] = col_of(j, lane) < N ? pack_key(key, col_of(j, lane)) : 0;
+        }
+      }
+      // A lower bound of the k-th best key: the k-th largest of the 32 lanes'
+      // maxima of the key bits (the k largest maxima are k keys at least that
+      // large), found as the least maximum whose rank among the maxima (count
+      // of larger ones) is below k.
+      uint32_t* s_m = reinterpret_cast<uint32_t*>(scratch);                        // [NT][32]
+      uint64_t* s_c = reinterpret_cast<uint64_t*>(scratch + NT * 128);              // [NT][32]
+      int* s_sel = reinterpret_cast<int*>(scratch + NT * 384);                      // [NT][16]
+      uint32_t bound[NT];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < kE; ++j) m = max(m, static_cast<uint32_t>(pw[n][j] >> 32));
+        bound[n] = m;
+        s_m[32 * n + lane] = m;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        int rk = 0;
+        const uint4* q4 = reinterpret_cast<const uint4*>(s_m + 32 * n);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = q4[q];
+          rk += (v.x > bound[n]) + (v.y > bound[n]) + (v.z > bound[n]) + (v.w > bound[n]);
+        }
+        bound[n] = rk < k ? bound[n] : 0xFFFFFFFFu;
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) bound[n] = __reduce_min_sync(0xFFFFFFFFu, bound[n]);
+      // Candidates: the words whose key bits reach the bound (the k best are
+      // among them), packed into the slot's list by per-expert ballots.
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        sel_id[n] = 0;
+        if (!select_by_rank(pw[n], static_cast<uint64_t>(bound[n]) << 32, k, lane, s_c + 32 * n, s_sel + 16 * n)) {
+          // many equal key bits: the bound again on whole words (the id breaks
+          // the ties, so exact ties leave about 4k candidates), else sorted
+          // lists and k rounds of a warp arg-max
+          select_ties(pw[n], k, lane, s_c + 32 * n, s_sel + 16 * n);
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int n = 0; n < NT; ++n) sel_id[n] = lane < k ? s_sel[16 * n + lane] : 0;
+      __syncwarp();
     }
-    __syncwarp();
     const bool mine = lane < k;
     float sc[NT], sum[NT];
 #pragma unroll
