@@ -322,7 +322,10 @@ size_t router_gate_x_gsa_offset(void);
  * host involvement):
  *   - T <= 16 (decode): one kernel; for T >= 2 its CTAs form clusters of 4
  *     that share the staging and quantization of x through distributed
- *     shared memory.
+ *     shared memory.  Up to 256 experts CTA 0 selects: it polls the (key,
+ *     score) words the other CTAs store into the workspace (bounded: a
+ *     timeout records NVR_ERR_TIMEOUT in the status word) and puts them back
+ *     to zero; wider heads end with the last CTA (an atomic ticket).
  *   - bf16 x, N <= 384: one kernel that takes max|x| itself (a bounded grid
  *     barrier in the workspace, or an exchange through distributed shared
  *     memory when the grid is one cluster), quantizes x inside the K-split
