@@ -24,7 +24,8 @@ step reads its input from L2), plus
                 batch (tokens/s), the standalone quantizer and the decode
                 kernel's own duration, each against the measured HBM copy rate;
   no_cooperative  the same steps launched with NVR_FLAG_NO_COOPERATIVE;
-  cpu_baseline  the CPU oracle on a bounded sample of the same batch;
+  cpu_baseline  the CPU oracle on a bounded sample of the same batch (all
+                cores, and one BLAS thread in a child process);
   clocks        SM clocks and throttle reasons sampled during the timed region.
 
 --impl reference times the CPU oracle itself on the host cores (the pages
@@ -148,6 +149,31 @@ def oracle_tokens_per_s(w, x32_all, packed_w, bias, budget_s=12.0, rows_per_call
         if el >= budget_s:
             break
     return done / el, done, el
+
+
+def oracle_sample_json(budget_s):
+    """The oracle sample above on the prefill batch, as one JSON line (run in
+    a child process by oracle_single_thread)."""
+    from oracle import pipeline
+    w = WL.WORKLOADS["prefill"]
+    x32 = WL.bf16_bits_to_float32(WL.make_x(w, seed=WL.SEED))
+    packed = pipeline.pack_weight(WL.bf16_bits_to_float32(WL.make_w(w)))
+    tps, done, el = oracle_tokens_per_s(w, x32, packed, WL.make_bias(w), budget_s=budget_s)
+    return json.dumps({"value": tps, "done": done, "seconds": el})
+
+
+def oracle_single_thread(budget_s=8.0):
+    """The same oracle sample with one BLAS / OpenMP thread, in a child
+    process (the thread count of a BLAS library is fixed when it loads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", str(budget_s)], env=env,
+                           capture_output=True, text=True, timeout=600)
+        d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    except Exception as e:  # reported, not fatal: the all-cores figure stands
+        return {"error": "%s: %s" % (type(e).__name__, e)}
+    return {"value": d["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d tokens in 64-token slices (%.1f s), one BLAS thread" % (d["done"], d["seconds"])}
 
 
 # ------------------------------------------------------------------ ranks
@@ -457,7 +483,8 @@ def run_gpu(args, rank, world, local_rank):
         tps, done, el = oracle_tokens_per_s(w, x32, packed, bias_np)
         cpu = {"value": tps, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": "%d tokens of the T=4096 batch in 64-token slices (%.1f s), batch gsa; "
-                         "NumPy quantize + float64 GEMM + epilogue" % (done, el)}
+                         "NumPy quantize + float64 GEMM + epilogue" % (done, el),
+               "single_thread": oracle_single_thread()}
 
     return {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -794,9 +821,14 @@ def main():
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--oracle-sample", type=float, default=None,
+                    help="time the CPU oracle for this many seconds, print one JSON line and exit")
     ap.add_argument("--profile-launches", action="store_true",
                     help="run each hot path twice and exit (for a profiler's launch filter)")
     args = ap.parse_args()
+    if args.oracle_sample is not None:
+        print(oracle_sample_json(args.oracle_sample))
+        return
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
