@@ -11,7 +11,11 @@ NVFP4 gate weight resident on the GPU.  Synthetic, seeded inputs.
 
 Printed (rank 0, one JSON line): prefill tokens/s over exactly --steps timed
 steps (inputs resident in HBM, four rotating 58.7 MB activation buffers so no
-step reads its input from L2), plus
+step reads its input from L2).  The timed steps are replays of a CUDA graph of
+16 router calls (and one graph of the remaining --steps % 16), as a serving
+loop captures its step; plus
+  eager         the same steps launched directly, one call after another (the
+                cooperative launch then waits for the previous call to end);
   e2e           the same call with the batch copied from pinned host memory and
                 the ids/weights copied back inside every timed step;
   roofline      the dominant kernel's algorithmic bytes per launch / its mean
@@ -55,6 +59,7 @@ METRIC = ("router tokens/s (prefill) & µs/call (decode T=1); % of FP4 tensor / 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense ratio (fp4 13.5 PF vs bf16 2.25 PF)
+GRAPH_CALLS = 16                      # router calls per captured graph in the timed region
 
 
 def load_peaks():
@@ -276,12 +281,27 @@ def run_gpu(args, rank, world, local_rank):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    # the timed steps: replays of a graph of GRAPH_CALLS calls and one graph of
+    # the remaining steps % GRAPH_CALLS (captured after the warm-up, which also
+    # settles the launch attributes outside capture)
+    n_graph, n_rem = divmod(args.steps, GRAPH_CALLS)
+    graphs = {}
+    for n in {GRAPH_CALLS if n_graph else 0, n_rem} - {0}:
+        graphs[n] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graphs[n]):
+            for i in range(n):
+                step(i)
+        for _ in range(2):
+            graphs[n].replay()
+    torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    for _ in range(n_graph):
+        graphs[GRAPH_CALLS].replay()
+    if n_rem:
+        graphs[n_rem].replay()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -292,6 +312,17 @@ def run_gpu(args, rank, world, local_rank):
     ms_per_step = ms / args.steps
     value = job_throughput(world, T, args.steps, ms)
     plan["cooperative"] = int(_native.lib().nvr_router_cooperative_state())
+
+    # the same steps launched directly
+    n_eager = max(3, min(args.steps, 2000))
+    e0.record(stream)
+    for i in range(n_eager):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eg_ms = e0.elapsed_time(e1) / n_eager
+    eager = {"ms_per_step": eg_ms, "tokens_per_s": T / (eg_ms / 1e3), "steps": n_eager,
+             "hbm_frac": algorithmic(w, T, "fused")[0] / (eg_ms / 1e3) / 1e9 / load_peaks()[0]}
 
     # the same steps without the cooperative launch (NVR_FLAG_NO_COOPERATIVE:
     # for a caller that owns the GPU; the next call's launch then overlaps the
@@ -496,10 +527,13 @@ def run_gpu(args, rank, world, local_rank):
                                "routed_scaling 2.5",
                    "T": T, "D": w.D, "E": w.N, "k": w.k,
                    "l2": "inputs larger than L2: 4 rotating 58.7 MB activation buffers",
+                   "timing": "%d replays of a CUDA graph of %d router calls and %d of one of %d; 'eager' "
+                             "launches every step directly" % (n_graph, GRAPH_CALLS, 1 if n_rem else 0, n_rem),
                    "plan": plan,
                    "parallelism": "replicas" if world > 1 else "single"},
         "e2e": e2e, "gpu_launches": len(names) * args.steps, "roofline": roof, "kernels": kernels,
-        "no_cooperative": no_coop, "decode": decode, "other_rooflines": extra, "cpu_baseline": cpu,
+        "eager": eager, "no_cooperative": no_coop, "decode": decode, "other_rooflines": extra,
+        "cpu_baseline": cpu,
         "clocks": clocks,
     }
 
