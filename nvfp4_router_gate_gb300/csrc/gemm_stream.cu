@@ -502,15 +502,18 @@ gemm_stream_kernel(const __grid_constant__ StreamParams p) {
     // the order-preserving 64-bit (key, id) word) and the winning lane drops
     // it.
     constexpr int kWarps = kSThreads / 32;
-    // every token's count and first 32 candidates into the (idle) ring at
-    // once: all loads in flight together
+    // every token's count and the first 32 slots of its candidates (those
+    // past the count are not read later) into the (idle) ring at once: one
+    // round trip to L2 for all of them
     uint32_t* s_cnt = reinterpret_cast<uint32_t*>(s_tr);                 // [T]
     float4* s_first = reinterpret_cast<float4*>(smem);                    // [T][32]
-    for (int t = threadIdx.x; t < p.T; t += kSThreads) s_cnt[t] = __ldcg(p.tok_count + t);
-    __syncthreads();
+    for (int t = 4 * threadIdx.x; t < p.T; t += 4 * kSThreads)          // [128] counts: 16-byte pieces
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(s_cnt + t)),
+                   "l"(reinterpret_cast<uint64_t>(p.tok_count + t)) : "memory");
+    const int n_first = p.surv_stride < 32 ? p.surv_stride : 32;       // inside the token's region
     for (int i = threadIdx.x; i < p.T * 32; i += kSThreads) {
       const int t = i >> 5, j = i & 31;
-      if (j < static_cast<int>(s_cnt[t]))
+      if (j < n_first)
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(s_first + i)),
                      "l"(reinterpret_cast<uint64_t>(p.surv + static_cast<size_t>(t) * p.surv_stride + j))
                      : "memory");
