@@ -38,7 +38,7 @@ constexpr int kRouteThreads = 1024;
 constexpr int kMoeMaxExperts = 1024;
 constexpr int kMThreads = 320;                  // producer, MMA, 8 epilogue warps
 constexpr int kMEpi = 256;
-constexpr int kMStages = 4;
+constexpr int kMStages = 6;
 constexpr int kMTile = 128 * 128;               // 128 rows x 128 bytes of codes
 constexpr int kMSlab = 4 * 512;                 // 4 scale atoms
 constexpr int kMStage = 2 * kMTile + 2 * kMSlab;
