@@ -551,48 +551,104 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
         if ((filled_c >> cs) & 1u)
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty_c + cs, (bits_c >> cs) & 1u, deadline, abort_flag));
     }
-    for (int s = 0; s < my_st && ok; ++s) {
-      const int ks = st0 + s;
-      // the stage's two x boxes (a box past D or T reads zeros)
-      for (int hs = 0; hs < 2; ++hs, ++xi) {
-        const int xs = xi % kFXSlots;
-        const uint32_t xph = (xi / kFXSlots) & 1;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_x + xs, xph ^ 1u, deadline, abort_flag))) {
+    if constexpr (kNT == 3) {
+      // kNT = 3 (one W stage): the x boxes and the W tiles are issued
+      // independently, each as soon as its ring slot is free, so that the x
+      // ring runs as far ahead as its slots allow while a W tile waits for the
+      // MMAs that free its slot (issuing the next stage's boxes only after the
+      // W slot -- the order below for kNT = 2 -- left the quantizer warps
+      // waiting on x: adversarial batch 146.0 -> 139.6 us).  Non-blocking
+      // tests, with a short sleep when neither ring has room.
+      const int nx = 2 * my_st;
+      int wi = 0;                                        // W stages issued so far
+      uint64_t polls = 0;
+      while (ok && (xi < nx || wi < my_st)) {
+        bool progressed = false;
+        if (xi < nx) {
+          const int xs = xi % kFXSlots;
+          const uint32_t xph = (xi / kFXSlots) & 1;
+          if (__all_sync(0xFFFFFFFFu, mbar_test_wait(empty_x + xs, xph ^ 1u))) {
+            const int ks = st0 + xi / 2, hs = xi & 1;     // box hs of stage ks (past D or T: zeros)
+            if (elect_one()) {
+              mbar_arrive_expect_tx(full_x + xs, kBoxBytes);
+              tma_load_2d(xring + xs * kFXBox, &p.tmap_x, ks * 256 + hs * 128, m_tile * kRows, full_x + xs);
+            }
+            __syncwarp();
+            filled_x |= 1u << xs;
+            bits_x = (bits_x & ~(1u << xs)) | (xph << xs);
+            ++xi;
+            progressed = true;
+          }
+        }
+        if (wi < my_st && __all_sync(0xFFFFFFFFu, mbar_test_wait(empty_w + wst, wph ^ 1u))) {
+          const int ks = st0 + wi;
+          const int nkk = min(4, KB / 4 - 4 * ks);
+          uint8_t* b = wring + wst * kFWStage;
+          uint8_t* sb = b + kFWTile;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(full_w + wst, static_cast<uint32_t>(p.n_groups * (128 * 128 + 512 * nkk)));
+            for (int h = 0; h < p.n_groups; ++h)                          // 128-row boxes
+              tma_load_2d(b + h * 16384, &p.tmap_b, ks * 128, h * 128, full_w + wst);
+            for (int h = 0; h < p.n_groups; ++h)
+              bulk_load(sb + h * 2048, p.sfb + (static_cast<size_t>(h) * (KB / 4) + 4 * ks) * 512, 512u * nkk,
+                        full_w + wst);
+          }
+          __syncwarp();
+          filled_w |= 1u << wst;
+          bits_w = (bits_w & ~(1u << wst)) | (wph << wst);
+          if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
+          ++wi;
+          progressed = true;
+        }
+        if (!progressed) {
+          __nanosleep(32);                               // leave the issue slots to the quantizer warps
+          if ((++polls & 63) == 0 && (*abort_flag || globaltimer_ns() > deadline)) ok = false;
+        }
+      }
+    } else {
+      for (int s = 0; s < my_st && ok; ++s) {
+        const int ks = st0 + s;
+        // the stage's two x boxes (a box past D or T reads zeros)
+        for (int hs = 0; hs < 2; ++hs, ++xi) {
+          const int xs = xi % kFXSlots;
+          const uint32_t xph = (xi / kFXSlots) & 1;
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_x + xs, xph ^ 1u, deadline, abort_flag))) {
+            ok = false;
+            break;
+          }
+          if (elect_one()) {
+            mbar_arrive_expect_tx(full_x + xs, kBoxBytes);
+            tma_load_2d(xring + xs * kFXBox, &p.tmap_x, ks * 256 + hs * 128, m_tile * kRows, full_x + xs);
+          }
+          __syncwarp();
+          filled_x |= 1u << xs;
+          bits_x = (bits_x & ~(1u << xs)) | (xph << xs);
+        }
+        if (!ok) break;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_w + wst, wph ^ 1u, deadline, abort_flag))) {
           ok = false;
           break;
         }
+        const int nkk = min(4, KB / 4 - 4 * ks);
+        uint8_t* b = wring + wst * kFWStage;
+        uint8_t* sb = b + kFWTile;
         if (elect_one()) {
-          mbar_arrive_expect_tx(full_x + xs, kBoxBytes);
-          tma_load_2d(xring + xs * kFXBox, &p.tmap_x, ks * 256 + hs * 128, m_tile * kRows, full_x + xs);
+          mbar_arrive_expect_tx(full_w + wst, static_cast<uint32_t>(p.n_groups * (128 * 128 + 512 * nkk)));
+          if (kNT == 2) {
+            tma_load_2d(b, &p.tmap_b, ks * 128, 0, full_w + wst);      // 128 or 256 rows in one box
+          } else {
+            for (int h = 0; h < p.n_groups; ++h)                        // 128-row boxes
+              tma_load_2d(b + h * 16384, &p.tmap_b, ks * 128, h * 128, full_w + wst);
+          }
+          for (int h = 0; h < p.n_groups; ++h)
+            bulk_load(sb + h * 2048, p.sfb + (static_cast<size_t>(h) * (KB / 4) + 4 * ks) * 512, 512u * nkk,
+                      full_w + wst);
         }
         __syncwarp();
-        filled_x |= 1u << xs;
-        bits_x = (bits_x & ~(1u << xs)) | (xph << xs);
+        filled_w |= 1u << wst;
+        bits_w = (bits_w & ~(1u << wst)) | (wph << wst);
+        if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
       }
-      if (!ok) break;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_w + wst, wph ^ 1u, deadline, abort_flag))) {
-        ok = false;
-        break;
-      }
-      const int nkk = min(4, KB / 4 - 4 * ks);
-      uint8_t* b = wring + wst * kFWStage;
-      uint8_t* sb = b + kFWTile;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(full_w + wst, static_cast<uint32_t>(p.n_groups * (128 * 128 + 512 * nkk)));
-        if (kNT == 2) {
-          tma_load_2d(b, &p.tmap_b, ks * 128, 0, full_w + wst);      // 128 or 256 rows in one box
-        } else {
-          for (int h = 0; h < p.n_groups; ++h)                        // 128-row boxes
-            tma_load_2d(b + h * 16384, &p.tmap_b, ks * 128, h * 128, full_w + wst);
-        }
-        for (int h = 0; h < p.n_groups; ++h)
-          bulk_load(sb + h * 2048, p.sfb + (static_cast<size_t>(h) * (KB / 4) + 4 * ks) * 512, 512u * nkk,
-                    full_w + wst);
-      }
-      __syncwarp();
-      filled_w |= 1u << wst;
-      bits_w = (bits_w & ~(1u << wst)) | (wph << wst);
-      if (++wst == kFStagesW) { wst = 0; wph ^= 1u; }
     }
     if (!ok && lane == 0) {
       report_timeout(p.status);
