@@ -536,15 +536,21 @@ decode_router_kernel(const DecodeParams p) {
         if (r != 0 && rk < k) s_cand[warp * k + rk] = r;
       }
       __syncthreads();
+      // each candidate is ranked by eight threads at once (consecutive lanes),
+      // each counting the better ones among an eighth of the candidates
+      // (measured at T = 1: 0.40 us, against 0.67 us with one thread per
+      // candidate)
       const int nc = 8 * k;
-      if (tid < nc) {
-        const uint64_t c = s_cand[tid];
-        if (c != 0) {
-          int rk = 0;
-#pragma unroll 8
-          for (int q = 0; q < nc; ++q) rk += s_cand[q] > c ? 1 : 0;
-          if (rk < k) s_sel[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(c));
-        }
+      for (int c0 = 0; c0 < nc; c0 += kDecodeThreads / 8) {
+        const int ci = c0 + (tid >> 3), part = tid & 7;
+        const uint64_t c = ci < nc ? s_cand[ci] : 0ull;
+        int rk = 0;
+        if (ci < nc)
+          for (int q = part; q < nc; q += 8) rk += s_cand[q] > c ? 1 : 0;
+        rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 1);
+        rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 2);
+        rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 4);
+        if (part == 0 && c != 0 && rk < k) s_sel[rk] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(c));
       }
       __syncthreads();
       if (warp == 0) {
