@@ -336,13 +336,11 @@ decode_router_kernel(const DecodeParams p) {
   const uint4* x4 = reinterpret_cast<const uint4*>(xraw);
   uint32_t m = 0;
   for (int v = tid; v < (b_hi - b_lo) * kVecPerBlock; v += kDecodeThreads) m = max(m, absmax_bits16B<kBF16>(x4[v]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
   if (lane == 0) s_red[warp] = m;
   __syncthreads();
-  uint32_t mb = 0;
-#pragma unroll
-  for (int w = 0; w < kDecodeWarps; ++w) mb = max(mb, s_red[w]);
+  static_assert(kDecodeWarps <= 32, "one warp reduces the warps' maxima");
+  uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, lane < kDecodeWarps ? s_red[lane] : 0u);
   if (C > 1) {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     if (tid < C) st_cluster_u32(cluster_addr(s_cmax + crank, tid), mb);
