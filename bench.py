@@ -285,13 +285,14 @@ def run_gpu(args, rank, world, local_rank):
     # the remaining steps % GRAPH_CALLS (captured after the warm-up, which also
     # settles the launch attributes outside capture)
     n_graph, n_rem = divmod(args.steps, GRAPH_CALLS)
+    sizes = ([GRAPH_CALLS] if n_graph else []) + ([n_rem] if n_rem else [])
     graphs = {}
-    for n in {GRAPH_CALLS if n_graph else 0, n_rem} - {0}:
+    for n in sizes:                                   # calls per graph
         graphs[n] = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graphs[n]):
             for i in range(n):
                 step(i)
-        for _ in range(2):
+        for _ in range(2):                            # untimed replays
             graphs[n].replay()
     torch.cuda.synchronize()
     barrier()
