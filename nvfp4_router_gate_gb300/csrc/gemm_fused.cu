@@ -42,7 +42,8 @@
 //               fp32 accumulator (kNT = 3, 257-384 experts: an N=256 and an
 //               N=128 MMA into columns 0-255 and 256-383);
 //   warps 2-17  after the last MMA: the fp32 partial (128 x 128 kNT) goes from
-//               tensor memory to partial plane r of the workspace (L2); after a
+//               tensor memory through shared memory (TMA stores) to partial
+//               plane r of the workspace (L2); after a
 //               cluster (or tile) barrier each CTA routes its own 128/S tokens
 //               from the S planes, one warp per token (TokenRouter,
 //               nvr_splitk.cuh).
@@ -108,6 +109,7 @@ static_assert(16 * 4096 <= kFXRing, "store staging fits the x ring");
 struct FusedParams {
   CUtensorMap tmap_x;          // bf16 activations [T, D], box 128 x 128, no swizzle
   CUtensorMap tmap_b;          // W codes [N, D/2] uint8, box 128 bytes x 128 n_groups rows (kNT = 3: 128)
+  CUtensorMap tmap_p;          // partial rows [S][T][128 kNT] fp32, box 32 x 16 x 1, 128-byte swizzle
   float* qrec;                 // quantizer record {gsa, 1/gsa, mode, amax}: from the amax kernel, or
                                // published by this kernel's last CTA when amax_sync is set
   uint32_t* amax_sync;         // in-kernel amax: 5 workspace words (grid_amax), or null
@@ -476,6 +478,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     fence_mbar_init();
     tma_prefetch_map(&p.tmap_x);
     tma_prefetch_map(&p.tmap_b);
+    tma_prefetch_map(&p.tmap_p);
   }
   if (threadIdx.x < 128) {
     const uint32_t b = threadIdx.x;
@@ -879,11 +882,17 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
       }
     }
     tc_fence_after();
-    // every x box has been read (the last MMA needed them all): the x ring
-    // stages the stores
-    store_partial_rows(p.partials + static_cast<size_t>(rank) * p.T * (128 * kNT), xring, tmem, warp, lane,
-                       static_cast<int64_t>(m_tile) * kRows, min(kRows, p.T - m_tile * kRows), p.n_groups,
-                       my_st > 0 && acc_ok, kFQWarps, 128 * kNT);
+    // every x box and W tile has been read (the last MMA needed them all):
+    // the rings stage the stores -- up to 256 experts two buffers per warp in
+    // the W and x rings (contiguous), else one in the x ring
+    static_assert(kNT == 3 || 16 * 2 * 4096 <= kFWRing + kFXRing, "two staging buffers per warp");
+    static_assert(kFWRing % 1024 == 0, "the staging buffers are 1024-byte aligned (128-byte swizzle)");
+    if constexpr (kNT == 2)
+      store_partial_rows_tma<2>(&p.tmap_p, wring, tmem, warp, lane, m_tile * kRows, min(kRows, p.T - m_tile * kRows),
+                                rank, p.n_groups, my_st > 0 && acc_ok, kFQWarps);
+    else
+      store_partial_rows_tma<1>(&p.tmap_p, xring, tmem, warp, lane, m_tile * kRows, min(kRows, p.T - m_tile * kRows),
+                                rank, p.n_groups, my_st > 0 && acc_ok, kFQWarps);
   }
 
   // The S CTAs of this token tile form the cluster, or meet at the tile's
@@ -1081,6 +1090,7 @@ nvr_status launch_fused_router(const uint16_t* x, float* qrec, float* x_gsa, uin
   const int nt = N > 256 ? 3 : 2;
   if (!encode_x(&g.tmap_x, x, T, D, static_cast<uint32_t>(tile_rows))) return NVR_ERR_UNSUPPORTED;
   if (!encode_codes(&g.tmap_b, W_codes, N, D, nt == 2 ? 128u * n_groups : 128u)) return NVR_ERR_UNSUPPORTED;
+  if (!encode_partial_rows(&g.tmap_p, partials, T, S, 128 * nt)) return NVR_ERR_UNSUPPORTED;
   g.qrec = qrec; g.sfb = W_sf; g.partials = partials;
   g.amax_sync = amax_sync; g.tile_sync = tile_sync; g.flat = flat ? 1 : 0; g.gsa_out = x_gsa;
   g.T = static_cast<int>(T); g.D = static_cast<int>(D); g.N = static_cast<int>(N); g.n_groups = n_groups; g.S = S;
