@@ -75,8 +75,9 @@ __device__ __forceinline__ void store_partial_tile(const CUtensorMap* tmap_p, ui
 // stores (tmap_p: encode_partial_rows) as two 16-row boxes -- a 112-row tile
 // ends half-way through a lane quarter, and a 32-row box there would write
 // the next tile's first rows; rows past T are clipped by the map.  Measured
-// against coalesced stores from the warps (the same staging read back):
-// prefill T = 4096 40.3 -> 39.5 us per call.  Returns after the writes have
+// against coalesced stores from the warps (the same staging read back),
+// prefill T = 4096: 39.8 against 40.0 us per call in graph replays (the CTAs'
+// stores and tile barrier 0.3 us shorter).  Returns after the writes have
 // completed (lane 0 waits for its bulk groups, then orders them before the
 // generic proxy), so the caller's barrier publishes them like ordinary
 // stores.  `have_acc` false stores zeros.
