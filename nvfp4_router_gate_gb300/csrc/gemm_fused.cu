@@ -154,12 +154,16 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
 // all then wait (acquire, bounded) until every CTA has arrived -- nobody has
 // to answer anybody -- and read the complete max.  CTA 0 then bumps the
 // generation for the next call (every CTA of this call read it before
-// arriving).  Each call zeroes the other generation's words at its start
+// arriving: `gen`, read before the CTA's max|x| pass, so that no round trip
+// for it lies between the last CTA's pass and the barrier -- 0.3 us earlier
+// at T = 4096).  Each call zeroes the other generation's words at its start
 // (the call that used them has completed).  All CTAs of the grid must be
-// resident.
-__device__ bool grid_amax(uint32_t* sync, uint32_t cta_max, uint32_t n_ctas, uint32_t& amax_bits,
+// resident.  Measured and not kept: per-CTA maximum words with a presence
+// bit, every CTA reading all of them instead of an arrival counter (no
+// counter, no second read): the 148 pollers' reads contend at the L2 and the
+// barrier ended 1.9 us later.
+__device__ bool grid_amax(uint32_t* sync, uint32_t gen, uint32_t cta_max, uint32_t n_ctas, uint32_t& amax_bits,
                           uint64_t deadline, volatile int* abort_flag) {
-  const uint32_t gen = ld_acquire_gpu(sync + 4);
   const uint32_t par = gen & 1u;
   asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" :: "l"(sync + par), "r"(cta_max) : "memory");
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(sync + 2 + par) : "memory");
@@ -721,6 +725,11 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
     const int q16 = warp - 2, qw = q16 & 7, qh = q16 >> 3;
     bool ok = true;
     int xi = 0;                                        // x boxes consumed so far
+    // the grid barrier's generation, read before the max|x| pass so that the
+    // barrier does not wait for it (after the grid-dependency wait the
+    // previous call's bump is visible; this call bumps it only after every
+    // CTA has arrived)
+    const uint32_t gen = p.amax_sync && warp == 2 && lane == 0 ? ld_acquire_gpu(p.amax_sync + 4) : 0u;
     if (p.amax_sync) {
       // ---- in-kernel amax: max |x| over this CTA's boxes (the same
       // bit-pattern max as the amax kernel), then the grid-wide record
@@ -778,7 +787,7 @@ fused_qgemm_kernel(const __grid_constant__ FusedParams p) {
             for (int r = 0; r < p.S; ++r) bits = max(bits, s_cmax[r]);
           }
         } else if (lane == 0) {
-          gok = grid_amax(p.amax_sync, cm, gridDim.x, bits, deadline, abort_flag);
+          gok = grid_amax(p.amax_sync, gen, cm, gridDim.x, bits, deadline, abort_flag);
         }
         if (lane == 0) {
           s_wmax[kFQWarps] = bits;
